@@ -1,0 +1,22 @@
+"""CPU oracle for paged-KV decode -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline /
+reference arm may import this package.  The product (``paged_kv_cache_190_gb300``)
+never imports it and shares no code with it; the two meet only through the
+seeded input generators in ``pa_inputs``.
+
+Contents, each written from the pages (cited in the modules):
+  * ``decode_f64``         -- fp64 gather-then-attend over the block table (plain C).
+  * ``reshape_and_cache``  -- byte copy of each new token's K/V into its slot.
+  * ``copy_blocks``        -- byte copy of whole pages for copy-on-write.
+  * ``RefBlockManager``    -- the teaching allocator of "PagedAttention原理" §3.3.4
+                              with the reference counts of §3.3.3 and copy-on-write.
+"""
+from ._decode import build, decode_f64, library_path, max_threads, widen
+from ._cache_ops import copy_blocks, reshape_and_cache
+from .ref_block_manager import OutOfBlocks, RefBlockManager
+
+__all__ = [
+    "build", "decode_f64", "library_path", "max_threads", "widen",
+    "copy_blocks", "reshape_and_cache", "OutOfBlocks", "RefBlockManager",
+]

@@ -1,0 +1,292 @@
+"""Seeded synthetic inputs for paged-KV decode.
+
+This module serves both the CUDA path and the CPU oracle.  It draws random
+numbers and lays them out; it holds none of the attention arithmetic and makes
+no block-management decision (no free list, no reference counts, no
+copy-on-write) -- those belong to the two implementations under test.
+
+Everything comes from ``numpy.random.Generator(PCG64(seed))``.  Draw order for a
+decode case: context lengths -> pool permutation -> prefill K/V -> new-token
+K/V -> q.  Values are drawn in float32 and, for bf16 cases, rounded to bf16 with
+round-to-nearest-even (torch's ``.to(torch.bfloat16)``); bf16 data is carried as
+its uint16 bit patterns.
+
+Pool layout: ``[num_blocks][num_kv_heads][block_size][head_dim]`` for K and for V.
+Slots that hold no token are filled with NaN so that any read of them by an
+implementation shows up in its output.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+BF16_NAN = np.uint16(0x7FC0)
+
+# The five workloads: decode over a paged pool, by name.
+WORKLOADS = {
+    "tiny_fp32": dict(seed=1001, dtype="f32", num_seqs=4, num_q_heads=8, num_kv_heads=8,
+                      head_dim=64, block_size=16, lens=("uniform", 17, 200), num_blocks=64,
+                      std=1.0),
+    "mha_bf16": dict(seed=1002, dtype="bf16", num_seqs=64, num_q_heads=32, num_kv_heads=32,
+                     head_dim=128, block_size=16, lens=("uniform", 512, 4096), std=1.0),
+    "gqa_bf16": dict(seed=1003, dtype="bf16", num_seqs=256, num_q_heads=32, num_kv_heads=8,
+                     head_dim=128, block_size=16, lens=("lognormal", 1024, 1.0, 16, 8192),
+                     std=1.0),
+    "long128k_bf16": dict(seed=1004, dtype="bf16", num_seqs=4, num_q_heads=32, num_kv_heads=8,
+                          head_dim=128, block_size=32, lens=("fixed", 131072), std=0.5),
+}
+
+SHARED_PREFIX = dict(seed=1005, dtype="bf16", num_parents=8, children_per_parent=16,
+                     prompt_len=2048, parent_extra=(1, 15), tail=(0, 512), num_q_heads=32,
+                     num_kv_heads=8, head_dim=128, block_size=16, std=1.0)
+
+
+def to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
+    """float32 samples -> stored form (float32, or bf16 bits as uint16, RNE)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if dtype == "f32":
+        return x
+    import torch
+    return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def storage_dtype(dtype: str):
+    return np.uint16 if dtype == "bf16" else np.float32
+
+
+def nan_fill(shape, dtype: str) -> np.ndarray:
+    if dtype == "bf16":
+        return np.full(shape, BF16_NAN, dtype=np.uint16)
+    return np.full(shape, np.nan, dtype=np.float32)
+
+
+def draw_lengths(rng: np.random.Generator, spec, num_seqs: int) -> np.ndarray:
+    kind = spec[0]
+    if kind == "uniform":
+        return rng.integers(spec[1], spec[2] + 1, size=num_seqs).astype(np.int32)
+    if kind == "lognormal":
+        median, sigma, lo, hi = spec[1:]
+        raw = rng.lognormal(mean=math.log(median), sigma=sigma, size=num_seqs)
+        return np.clip(np.rint(raw), lo, hi).astype(np.int32)
+    if kind == "fixed":
+        return np.full(num_seqs, spec[1], dtype=np.int32)
+    if kind == "list":
+        return np.asarray(spec[1], dtype=np.int32)
+    raise ValueError(kind)
+
+
+@dataclass
+class DecodeCase:
+    """One decode step's inputs.  ``context_lens`` counts the new token: position
+    L_b - 1 is written by the step's cache write, positions 0 .. L_b - 2 are
+    already in the pool."""
+    name: str
+    dtype: str
+    num_seqs: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    scale: float
+    context_lens: np.ndarray      # int32 [B]
+    block_tables: np.ndarray      # int32 [B, max_blocks], -1 past each sequence's pages
+    slot_mapping: np.ndarray      # int64 [B], slot of position L_b - 1 (-1 when L_b == 0)
+    k_cache: np.ndarray           # [NB, Hkv, bs, D] storage
+    v_cache: np.ndarray
+    k_new: np.ndarray             # [B, Hkv, D] storage
+    v_new: np.ndarray
+    q: np.ndarray                 # [B, Hq, D] storage
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def max_blocks_per_seq(self) -> int:
+        return int(self.block_tables.shape[1])
+
+    @property
+    def max_context_len(self) -> int:
+        return int(self.context_lens.max()) if self.num_seqs else 0
+
+    def kv_bytes(self) -> int:
+        """Bytes of K and V of the valid tokens (what one decode step must read)."""
+        elt = 2 if self.dtype == "bf16" else 4
+        return int(self.context_lens.astype(np.int64).sum()) * 2 * self.num_kv_heads * self.head_dim * elt
+
+
+def _draw_normal(rng, shape, std):
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    if std != 1.0:
+        x *= np.float32(std)
+    return x
+
+
+def make_decode_case(name="custom", *, seed, dtype, num_seqs, num_q_heads, num_kv_heads,
+                     head_dim, block_size, lens, std=1.0, num_blocks=None, slack=0.10,
+                     scale=None, max_blocks_per_seq=None) -> DecodeCase:
+    """Build a seeded decode case; ``lens`` is a length spec (see ``draw_lengths``)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    B, Hq, Hkv, D, bs = num_seqs, num_q_heads, num_kv_heads, head_dim, block_size
+    L = draw_lengths(rng, lens, B)
+    pages = [(int(l) + bs - 1) // bs for l in L]
+    need = int(sum(pages))
+    NB = int(num_blocks) if num_blocks is not None else max(1, int(math.ceil((1.0 + slack) * need)))
+    if need > NB:
+        raise ValueError(f"pool of {NB} blocks cannot hold {need} pages")
+    perm = rng.permutation(NB).astype(np.int32)
+    mb = max_blocks_per_seq if max_blocks_per_seq is not None else max(1, max(pages) if pages else 1)
+    tables = np.full((B, mb), -1, dtype=np.int32)
+    # physical pages are dealt from the end of the permutation, one sequence after another
+    cursor = NB
+    for b in range(B):
+        tables[b, :pages[b]] = perm[cursor - pages[b]:cursor][::-1]
+        cursor -= pages[b]
+
+    k_cache = nan_fill((NB, Hkv, bs, D), dtype)
+    v_cache = nan_fill((NB, Hkv, bs, D), dtype)
+    for b in range(B):
+        n_old = max(int(L[b]) - 1, 0)
+        if n_old == 0:
+            continue
+        kb = to_storage(_draw_normal(rng, (n_old, Hkv, D), std), dtype)
+        vb = to_storage(_draw_normal(rng, (n_old, Hkv, D), std), dtype)
+        _lay_out_prefix(k_cache, tables[b], kb, bs)
+        _lay_out_prefix(v_cache, tables[b], vb, bs)
+    k_new = to_storage(_draw_normal(rng, (B, Hkv, D), std), dtype)
+    v_new = to_storage(_draw_normal(rng, (B, Hkv, D), std), dtype)
+    q = to_storage(_draw_normal(rng, (B, Hq, D), std), dtype)
+    slots = np.full(B, -1, dtype=np.int64)
+    for b in range(B):
+        if L[b] > 0:
+            pos = int(L[b]) - 1
+            slots[b] = int(tables[b, pos // bs]) * bs + pos % bs
+    return DecodeCase(name=name, dtype=dtype, num_seqs=B, num_q_heads=Hq, num_kv_heads=Hkv,
+                      head_dim=D, block_size=bs, num_blocks=NB,
+                      scale=float(scale) if scale is not None else 1.0 / math.sqrt(D),
+                      context_lens=L, block_tables=tables, slot_mapping=slots,
+                      k_cache=k_cache, v_cache=v_cache, k_new=k_new, v_new=v_new, q=q)
+
+
+def _lay_out_prefix(pool, table_row, rows, bs):
+    """Put rows[t] (shape [T, Hkv, D]) at logical position t of the sequence whose
+    pages are ``table_row``: page table_row[t // bs], offset t % bs."""
+    T = rows.shape[0]
+    full = T // bs
+    if full:
+        blk = rows[:full * bs].reshape(full, bs, rows.shape[1], rows.shape[2]).transpose(0, 2, 1, 3)
+        pool[table_row[:full]] = blk
+    rem = T - full * bs
+    if rem:
+        pool[table_row[full], :, :rem, :] = rows[full * bs:].transpose(1, 0, 2)
+
+
+def place_at_slots(pool, slots, rows, block_size):
+    """Put rows[t] (shape [T, Hkv, D]) at global slot slots[t] (prefill of a pool
+    whose slots were handed out by a block manager)."""
+    slots = np.asarray(slots, dtype=np.int64)
+    pool[slots // block_size, :, slots % block_size, :] = rows
+
+
+def workload(name: str, **overrides) -> DecodeCase:
+    spec = dict(WORKLOADS[name])
+    spec.update(overrides)
+    return make_decode_case(name, **spec)
+
+
+def scaled_workload(name: str, num_seqs: int, seed_offset: int = 0, **overrides) -> DecodeCase:
+    """The named workload's shapes and distributions with fewer sequences (for the
+    oracle to finish in seconds)."""
+    spec = dict(WORKLOADS[name])
+    spec["num_seqs"] = num_seqs
+    spec["seed"] = spec["seed"] + seed_offset
+    if "num_blocks" in spec and name != "tiny_fp32":
+        spec.pop("num_blocks")
+    spec.update(overrides)
+    return make_decode_case(f"{name}[B={num_seqs}]", **spec)
+
+
+# --------------------------------------------------------------------------
+# Shared-prefix / beam workload: the random draws only.  The block manager
+# under test turns the script into page tables, slots and copy pairs.
+# --------------------------------------------------------------------------
+@dataclass
+class SharedPrefixScript:
+    dtype: str
+    num_parents: int
+    children_per_parent: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    scale: float
+    prefix_lens: np.ndarray          # int32 [P]  tokens each parent holds when it forks
+    tails: np.ndarray                # int32 [P * C]  further tokens each child generates
+    prefix_k: list                   # P arrays [prefix_len, Hkv, D] storage
+    prefix_v: list
+    k_new: np.ndarray                # [P * C, Hkv, D] storage (the step's new token)
+    v_new: np.ndarray
+    q: np.ndarray                    # [P * C, Hq, D]
+    finish_keys: np.ndarray          # float64 [P * C]: ties among children finishing together
+    initial_free_order: np.ndarray   # int32 [NB]: a seeded permutation of the pool
+
+    @property
+    def num_children(self) -> int:
+        return self.num_parents * self.children_per_parent
+
+
+def shared_prefix_script(scale_parents=None, scale_children=None, seed=None,
+                         prompt_len=None, tail=None) -> SharedPrefixScript:
+    spec = dict(SHARED_PREFIX)
+    if seed is not None:
+        spec["seed"] = seed
+    P = scale_parents or spec["num_parents"]
+    C = scale_children or spec["children_per_parent"]
+    prompt = prompt_len if prompt_len is not None else spec["prompt_len"]
+    t_lo, t_hi = tail if tail is not None else spec["tail"]
+    Hq, Hkv, D, bs = spec["num_q_heads"], spec["num_kv_heads"], spec["head_dim"], spec["block_size"]
+    dtype, std = spec["dtype"], spec["std"]
+    rng = np.random.Generator(np.random.PCG64(spec["seed"]))
+    g_lo, g_hi = spec["parent_extra"]
+    extra = rng.integers(g_lo, g_hi + 1, size=P)
+    prefix_lens = (prompt + extra).astype(np.int32)
+    tails = rng.integers(t_lo, t_hi + 1, size=P * C).astype(np.int32)
+    # pool: shared pages once per family, plus every private page the run can need
+    shared_pages = sum((int(n) + bs - 1) // bs for n in prefix_lens)
+    private = 0
+    for p in range(P):
+        for c in range(C):
+            total = int(prefix_lens[p]) + 1 + int(tails[p * C + c])
+            private += (total + bs - 1) // bs - int(prefix_lens[p]) // bs
+    NB = int(math.ceil(1.10 * (shared_pages + private)))
+    free_order = rng.permutation(NB).astype(np.int32)
+    prefix_k, prefix_v = [], []
+    for p in range(P):
+        n = int(prefix_lens[p])
+        prefix_k.append(to_storage(_draw_normal(rng, (n, Hkv, D), std), dtype))
+        prefix_v.append(to_storage(_draw_normal(rng, (n, Hkv, D), std), dtype))
+    k_new = to_storage(_draw_normal(rng, (P * C, Hkv, D), std), dtype)
+    v_new = to_storage(_draw_normal(rng, (P * C, Hkv, D), std), dtype)
+    q = to_storage(_draw_normal(rng, (P * C, Hq, D), std), dtype)
+    finish_keys = rng.random(P * C)
+    return SharedPrefixScript(dtype=dtype, num_parents=P, children_per_parent=C,
+                              num_q_heads=Hq, num_kv_heads=Hkv, head_dim=D, block_size=bs,
+                              num_blocks=NB, scale=1.0 / math.sqrt(D), prefix_lens=prefix_lens,
+                              tails=tails, prefix_k=prefix_k, prefix_v=prefix_v, k_new=k_new,
+                              v_new=v_new, q=q, finish_keys=finish_keys,
+                              initial_free_order=free_order)
+
+
+def random_bm_ops(seed: int, num_ops: int, max_seqs: int = 6):
+    """A seeded random sequence of block-manager operations (names and operands
+    only; whether each succeeds is up to the manager under test)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    kinds = ["add", "append", "append", "append", "fork", "free"]
+    ops = []
+    for _ in range(num_ops):
+        kind = kinds[int(rng.integers(0, len(kinds)))]
+        a = int(rng.integers(0, max_seqs))
+        b = int(rng.integers(0, max_seqs))
+        ops.append((kind, a, b))
+    return ops
