@@ -1,0 +1,527 @@
+"""Benchmark: one decode step of the paged-KV path per timed step.
+
+A step is the hot path over one batch: the new tokens' cache write
+(pa_reshape_and_cache; for the shared-prefix workload the copy-on-write page
+copies first) followed by paged decode attention (pa_decode: plan, persistent
+decode kernel, split-K merge).  Inputs are seeded synthetic data
+(pa_inputs) already resident in HBM; the K/V working set of the default
+workload (2.4 GB) is far larger than L2, so no flush is needed between steps.
+
+Prints one JSON line.  `value` is KV-read GB/s: the algorithmic bytes of the
+step (valid tokens' K and V, q, out, block-table entries, lengths, and the
+cache write) divided by the device time of the step, summed over ranks.
+
+`--impl reference` times the CPU oracle (fp64, OpenMP on the host cores) on a
+bounded sample of the same workload and prints the same line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import pa_inputs  # noqa: E402
+
+METRIC = "paged decode KV-read GB/s (% of GB300 HBM peak); decode steps/s, µs/step"
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_WORKLOAD = "mha_bf16"   # Llama-2-7B-shaped MHA decode, bf16, batch 64
+DECODE_SOURCES = ["paged_decode.cuh", "decode_launch.cu", "decode_instances.cuh", "pa_device.cuh"]
+
+
+# ------------------------------------------------------------------ helpers
+def algorithmic_bytes(case) -> dict:
+    elt = 2 if case.dtype == "bf16" else 4
+    L = case.context_lens.astype(np.int64)
+    B, Hq, Hkv, D, bs = (case.num_seqs, case.num_q_heads, case.num_kv_heads, case.head_dim,
+                         case.block_size)
+    kv = int(L.sum()) * 2 * Hkv * D * elt
+    q = B * Hq * D * elt
+    out = B * Hq * D * elt
+    tables = 4 * (int(((L + bs - 1) // bs).sum()) + B)
+    decode = kv + q + out + tables
+    write = 2 * 2 * B * Hkv * D * elt + 8 * B            # read new k/v, write them, slots
+    return dict(kv=kv, decode=decode, write=write, step=decode + write)
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            data = json.load(open(path))
+
+            def find(d):
+                if isinstance(d, dict):
+                    for k, v in d.items():
+                        if isinstance(v, (int, float)) and "hbm" in k.lower() and "gb" in k.lower():
+                            return float(v)
+                        r = find(v)
+                        if r:
+                            return r
+                return None
+            v = find(data)
+            if v:
+                return v, "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest(names) -> str:
+    h = hashlib.sha256()
+    for n in names:
+        h.update(open(os.path.join(ROOT, "paged_kv_cache_190_gb300", "csrc", n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, or None when
+    the decode sources changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("source_digest") != source_digest(DECODE_SOURCES):
+        return None
+    try:
+        return int(float(fields["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while timing."""
+    QUERY = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        else:
+            self.lines = []
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, flag in zip(names, parts[2:6]):
+                if flag.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+# ------------------------------------------------------------- GPU workload
+class GpuStep:
+    """Device-resident inputs of one workload and the step that runs on them."""
+
+    def __init__(self, name: str, device, torch, pa):
+        self.torch, self.pa, self.device = torch, pa, device
+        self.name = name
+        if name == "shared_prefix_bf16":
+            self._init_shared_prefix()
+        else:
+            self._init_decode(pa_inputs.workload(name))
+
+    def _t(self, a, bf16=False):
+        t = self.torch.from_numpy(np.ascontiguousarray(a))
+        if bf16:
+            t = t.view(self.torch.int16).view(self.torch.bfloat16)
+        return t.to(self.device)
+
+    def _init_decode(self, case):
+        torch = self.torch
+        bf = case.dtype == "bf16"
+        self.case = case
+        self.k_cache, self.v_cache = self._t(case.k_cache, bf), self._t(case.v_cache, bf)
+        self.k_new, self.v_new = self._t(case.k_new, bf), self._t(case.v_new, bf)
+        self.q = self._t(case.q, bf)
+        self.slots = self._t(case.slot_mapping)
+        self.tables = self._t(case.block_tables)
+        self.lens = self._t(case.context_lens)
+        self.pairs = None
+        self.out = torch.empty(self.q.shape, dtype=self.q.dtype, device=self.device)
+        self.max_len = case.max_context_len
+        self.Hkv = case.num_kv_heads
+        self.scale = case.scale
+        self.bytes = algorithmic_bytes(case)
+        self.host_inputs = dict(q=case.q, k_new=case.k_new, v_new=case.v_new,
+                                slots=case.slot_mapping, tables=case.block_tables,
+                                lens=case.context_lens)
+        self.bf16 = bf
+        self._finish_init()
+
+    def _init_shared_prefix(self):
+        """Shared-prefix step: the library's block manager forks each parent's
+        pages to its children; the step copies the partial shared page for all
+        but the last child of each family, writes the new tokens, decodes."""
+        pa = self.pa
+        s = pa_inputs.shared_prefix_script()
+        bm = pa.BlockManager(s.num_blocks, s.block_size, s.initial_free_order)
+        prefix_slots = pa_inputs.shared_prefix_prefill(bm, s)
+        _, children = pa_inputs.shared_prefix_ids(s)
+        kc = pa_inputs.nan_fill((s.num_blocks, s.num_kv_heads, s.block_size, s.head_dim), s.dtype)
+        vc = pa_inputs.nan_fill(kc.shape, s.dtype)
+        for p, sl in enumerate(prefix_slots):
+            pa_inputs.place_at_slots(kc, sl, s.prefix_k[p], s.block_size)
+            pa_inputs.place_at_slots(vc, sl, s.prefix_v[p], s.block_size)
+        slots, pairs = bm.append_slots(children)
+        mb = max(len(bm.block_table(c)[0]) for c in children)
+        tables, lens = bm.build_block_tables(children, mb)
+        case = pa_inputs.DecodeCase(
+            name="shared_prefix_bf16", dtype=s.dtype, num_seqs=len(children),
+            num_q_heads=s.num_q_heads, num_kv_heads=s.num_kv_heads, head_dim=s.head_dim,
+            block_size=s.block_size, num_blocks=s.num_blocks, scale=s.scale, context_lens=lens,
+            block_tables=tables, slot_mapping=slots, k_cache=kc, v_cache=vc, k_new=s.k_new,
+            v_new=s.v_new, q=s.q)
+        self._init_decode(case)
+        self.pairs = self._t(pairs)
+        self.host_inputs["pairs"] = pairs
+        elt = 2
+        self.bytes["copy"] = 2 * 2 * len(pairs) * s.num_kv_heads * s.block_size * s.head_dim * elt
+        self.bytes["step"] += self.bytes["copy"]
+
+    def _finish_init(self):
+        torch, pa = self.torch, self.pa
+        c = self.case
+        self.ws_bytes = pa.pa_decode_workspace_size(c.num_seqs, c.num_q_heads, c.num_kv_heads,
+                                                    c.head_dim, c.block_size, self.max_len)
+        self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8,
+                                     device=self.device)
+        self.errs = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.chunk = pa.pa_decode_chunk_tokens(c.num_seqs, c.num_kv_heads, c.block_size,
+                                               self.max_len)
+        # kernels of ours per step: [copy_blocks] + reshape + plan + decode [+ merge]
+        self.launches_per_step = (1 if self.pairs is not None else 0) + 3 + (
+            1 if self.max_len > self.chunk else 0)
+
+    def write(self):
+        pa = self.pa
+        if self.pairs is not None:
+            pa.pa_copy_blocks(self.k_cache, self.v_cache, self.pairs, device_errors=self.errs)
+        pa.pa_reshape_and_cache(self.k_new, self.v_new, self.k_cache, self.v_cache, self.slots,
+                                device_errors=self.errs)
+
+    def decode(self):
+        self.pa.pa_decode(self.out, self.q, self.k_cache, self.v_cache, self.tables, self.lens,
+                          self.scale, self.Hkv, self.max_len, workspace=self.workspace,
+                          device_errors=self.errs)
+
+    def step(self):
+        self.write()
+        self.decode()
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+    import paged_kv_cache_190_gb300 as pa
+    pa.library()
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    ws = GpuStep(args.workload, device, torch, pa)
+    stream = torch.cuda.current_stream(device)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # warm-up
+    for _ in range(args.warmup):
+        ws.step()
+    torch.cuda.synchronize(device)
+    flags = pa.pa_read_device_errors(ws.errs)
+    if flags:
+        raise RuntimeError(f"device error bits {flags} during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier()
+    torch.cuda.synchronize(device)
+    with ClockSampler(device.index if device.index is not None else 0) as clocks:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(K):
+            ev[i][0].record(stream)
+            ws.write()
+            ev[i][1].record(stream)
+            ws.decode()
+            ev[i][2].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(device)
+        # keep the sampler running for a moment so short regions still get a sample
+        if K * 0.5e-3 < 0.3:
+            time.sleep(0.3)
+    barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    decode_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    write_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    ms_per_step = total_ms / K
+    if world > 1:
+        t = torch.tensor([ms_per_step], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    flags = pa.pa_read_device_errors(ws.errs)
+    if flags:
+        raise RuntimeError(f"device error bits {flags} during the timed steps")
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(ws, args, torch, pa, device, stream, barrier, world)
+
+    if rank != 0:
+        return None
+    peak, peak_src = hbm_peak()
+    b = ws.bytes
+    value = world * b["step"] / (ms_per_step * 1e-3) / 1e9
+    dec_avg_ms = statistics.mean(decode_ms)
+    achieved = b["decode"] / (dec_avg_ms * 1e-3) / 1e9
+    traffic = ncu_traffic(args.workload)
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "us_per_step": round(ms_per_step * 1e3, 2),
+        "steps_per_s": round(world * 1e3 / ms_per_step, 1),
+        "hbm_frac_step": round(value / world / peak, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+        if ws.bf16 else "f32", "data": "synthetic (seeded pa_inputs; no dataset or weights)",
+        "config": {
+            "workload": args.workload, "num_seqs": ws.case.num_seqs,
+            "num_q_heads": ws.case.num_q_heads, "num_kv_heads": ws.case.num_kv_heads,
+            "head_dim": ws.case.head_dim, "block_size": ws.case.block_size,
+            "num_blocks": ws.case.num_blocks, "mean_context": float(ws.case.context_lens.mean()),
+            "max_context": ws.max_len, "chunk_tokens": ws.chunk,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "no flush: the step reads %.2f GB of K/V, far above the 129 MB L2"
+                  % (b["kv"] / 1e9) if b["kv"] > 1e9 else "working set may sit in L2",
+            "step": ("copy_blocks + " if ws.pairs is not None else "")
+            + "reshape_and_cache + decode (plan, persistent decode, split-K merge)",
+            "algorithmic_bytes_per_step": b["step"],
+        },
+        "roofline": {
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic,
+            "kernel": "pa_decode call (plan + paged_decode_kernel + merge), CUDA events",
+            "algorithmic_bytes_per_launch": b["decode"], "avg_launch_us": round(dec_avg_ms * 1e3, 2),
+            "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json hbm' if peak_src == 'measured' else 'profiling recipe fallback 6.8 TB/s'})",
+        },
+        "write_avg_us": round(statistics.mean(write_ms) * 1e3, 2),
+        "e2e": e2e,
+        "gpu_launches": ws.launches_per_step * K,
+        "clocks": clocks.summary(),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        result["cpu_baseline"] = cpu_baseline(ws.case, budget_s=args.cpu_budget)
+    return result
+
+
+def run_e2e(ws, args, torch, pa, device, stream, barrier, world):
+    """Every step: pinned host inputs copied to the device, the step through the
+    C ABI, the output copied back to pinned host memory, stream synchronised."""
+    def pinned(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).pin_memory()
+
+    host = {k: pinned(v) for k, v in ws.host_inputs.items()}
+    dev = dict(q=ws.q, k_new=ws.k_new, v_new=ws.v_new, slots=ws.slots, tables=ws.tables,
+               lens=ws.lens)
+    if "pairs" in host:
+        dev["pairs"] = ws.pairs
+    out_host = torch.empty(ws.out.shape, dtype=ws.out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def one():
+        for k, h in host.items():
+            d = dev[k]
+            d.view(torch.uint8).view(-1).copy_(h.view(torch.uint8).view(-1), non_blocking=True)
+        ws.step()
+        out_host.copy_(ws.out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(max(3, args.warmup // 4)):
+        one()
+    n = max(10, min(args.steps, 500))
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(n):
+        one()
+    t1 = time.perf_counter()
+    barrier()
+    sec = (t1 - t0) / n
+    if world > 1:
+        t = torch.tensor([sec], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        sec = float(t.item())
+    return {"value": round(world * ws.bytes["step"] / sec / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "us_per_step": round(sec * 1e6, 2), "steps": n}
+
+
+# -------------------------------------------------------------- CPU oracle
+def _oracle_sample(case, n_rows, rng):
+    rows = [(int(rng.integers(case.num_seqs)), int(rng.integers(case.num_q_heads)))
+            for _ in range(n_rows)]
+    elt = 2 if case.dtype == "bf16" else 4
+    D = case.head_dim
+    # bytes the sampled rows stand for: each row reads its sequence's K and V for
+    # one head (shared by the GQA group, counted once per group member here is
+    # avoided by dividing by the group size), plus its q and out row
+    G = case.num_q_heads // case.num_kv_heads
+    nbytes = sum(int(case.context_lens[b]) * 2 * D * elt / G + 2 * D * elt for b, _ in rows)
+    return rows, nbytes
+
+
+def cpu_baseline(case, budget_s=15.0, kind="oracle"):
+    import oracle
+    kc, vc = case.k_cache.copy(), case.v_cache.copy()
+    oracle.reshape_and_cache(case.k_new, case.v_new, kc, vc, case.slot_mapping)
+    threads = oracle.max_threads()
+    rng = np.random.default_rng(9)
+    # calibrate on a few rows, then size the sample to the budget
+    rows, nbytes = _oracle_sample(case, 8, rng)
+    t0 = time.perf_counter()
+    oracle.decode_f64(case.q, kc, vc, case.block_tables, case.context_lens, case.scale,
+                      case.num_kv_heads, case.dtype, rows=rows)
+    dt = time.perf_counter() - t0
+    n = int(max(8, min(case.num_seqs * case.num_q_heads, 8 * budget_s / max(dt, 1e-6))))
+    rows, nbytes = _oracle_sample(case, n, rng)
+    t0 = time.perf_counter()
+    oracle.decode_f64(case.q, kc, vc, case.block_tables, case.context_lens, case.scale,
+                      case.num_kv_heads, case.dtype, rows=rows)
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": kind, "sample": f"{n} random (sequence, query head) rows of the {case.name} "
+                                     f"step, fp64 gather-then-attend, {dt:.1f} s",
+            "seconds": round(dt, 2)}
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle on a bounded sample per step."""
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    if args.workload == "shared_prefix_bf16":
+        case = pa_inputs.workload("gqa_bf16")
+    else:
+        case = pa_inputs.workload(args.workload)
+    kc, vc = case.k_cache.copy(), case.v_cache.copy()
+    threads = oracle.max_threads()
+    rng = np.random.default_rng(11)
+    # size a step so K + W steps take about two minutes
+    rows, _ = _oracle_sample(case, 4, rng)
+    t0 = time.perf_counter()
+    oracle.decode_f64(case.q, kc, vc, case.block_tables, case.context_lens, case.scale,
+                      case.num_kv_heads, case.dtype, rows=rows)
+    per_row = (time.perf_counter() - t0) / 4
+    total_steps = args.steps + args.warmup
+    n_rows = int(max(1, min(4 * threads, 120.0 / max(total_steps, 1) / max(per_row, 1e-6))))
+    samples = [_oracle_sample(case, n_rows, rng) for _ in range(args.steps + args.warmup)]
+    elapsed, nbytes_total = 0.0, 0.0
+    for i, (rows, nbytes) in enumerate(samples):
+        t0 = time.perf_counter()
+        oracle.reshape_and_cache(case.k_new, case.v_new, kc, vc, case.slot_mapping)
+        oracle.decode_f64(case.q, kc, vc, case.block_tables, case.context_lens, case.scale,
+                          case.num_kv_heads, case.dtype, rows=rows)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            elapsed += dt
+            nbytes_total += nbytes
+    value = nbytes_total / elapsed / 1e9
+    ms = elapsed / args.steps * 1e3
+    return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic (seeded pa_inputs)", "impl": "reference",
+            "config": {"workload": case.name, "num_seqs": case.num_seqs,
+                       "rows_per_step": n_rows},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle",
+                             "sample": f"{n_rows} random (sequence, query head) rows per step"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=list(pa_inputs.WORKLOADS) + ["shared_prefix_bf16"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("at least 3 warm-up steps")
+    world, rank, local = dist_env()
+    if args.gpus != world and world > 1:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE {world}")
+    if args.impl == "reference":
+        res = run_reference(args, world, rank)
+    else:
+        res = run_gpu(args, world, rank, local)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,192 @@
+/*
+ * pa.h -- C ABI of libpagedattn: paged-KV-cache decode for NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the statement of the problem on the pages this library
+ * is built from:
+ *   - "PagedAttention原理" (ch. 3 of a vLLM long-sequence inference memory guide),
+ *     §3.2 (the KV cache is cut into fixed-size pages; logically contiguous tokens
+ *     live in scattered physical pages reached through a page table), §3.3.1
+ *     (page size 16 or 32 tokens), §3.3.2 (pages are taken on demand and returned
+ *     when a request ends), §3.3.3 (pages shared between requests carry reference
+ *     counts), §3.3.4 (teaching allocator: a LIFO free list, out-of-memory when it
+ *     is empty), §3.4 (paging leaves the attention mathematics unchanged);
+ *   - "PagedAttentionMetal", sections "块表管理" (the block table maps logical to
+ *     physical pages) and "注意力计算优化" (the kernel looks the physical page up,
+ *     loads the K/V block into shared memory, and batches variable-length
+ *     sequences without padding);
+ *   - "mlx-paged-attention", feature 2 (shared prefixes with copy-on-write).
+ *
+ * Conventions for every call:
+ *   - Device pointers are raw CUDA device addresses owned by the caller; the
+ *     library allocates no device memory and keeps no pointer after returning.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Every device call only enqueues work on that stream and never
+ *     synchronises; results are ready when the caller's stream work is.
+ *   - Each call returns an int status: PA_OK (0) or a negative PA_ERR_*.  All
+ *     argument checks happen on the host before anything is enqueued; a failing
+ *     check enqueues nothing.
+ *   - `device_errors` (nullable) is a caller-owned device int32 into which the
+ *     kernels OR PA_DEVERR_* bits when they meet data they refuse (an
+ *     out-of-range block id or slot, a length outside the table); the kernels
+ *     skip that work instead of faulting.  Read it with pa_read_device_errors.
+ *   - Layouts are row-major and contiguous:
+ *       k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim]
+ *       q, out           : [num_seqs][num_q_heads][head_dim]
+ *       k, v (new tokens): [num_tokens][num_kv_heads][head_dim]
+ *       block_tables     : int32 [num_seqs][max_blocks_per_seq]
+ *     Element type: PA_F32 (IEEE binary32) or PA_BF16 (bfloat16); all float
+ *     tensors of one call share it.  Supported: head_dim 64 or 128, block_size 16
+ *     or 32, num_q_heads / num_kv_heads in {1, 2, 4, 8}.  Device buffers must be
+ *     16-byte aligned.
+ */
+#ifndef PAGEDATTN_PA_H
+#define PAGEDATTN_PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Status codes. */
+#define PA_OK 0
+#define PA_ERR_INVALID_ARG (-1)   /* null pointer, bad size, misaligned buffer   */
+#define PA_ERR_UNSUPPORTED (-2)   /* dtype / head_dim / block_size / group size  */
+#define PA_ERR_OUT_OF_BLOCKS (-3) /* block manager: the free list is empty       */
+#define PA_ERR_CUDA (-4)          /* a CUDA runtime call or launch failed        */
+#define PA_ERR_NOT_FOUND (-5)     /* block manager: unknown sequence id          */
+#define PA_ERR_EXISTS (-6)        /* block manager: sequence id already in use   */
+#define PA_ERR_WORKSPACE (-7)     /* decode workspace missing or too small       */
+
+/* Bits the kernels OR into *device_errors. */
+#define PA_DEVERR_BAD_BLOCK 1     /* block id outside [0, num_blocks)            */
+#define PA_DEVERR_BAD_LENGTH 2    /* context length < 0 or beyond its table      */
+#define PA_DEVERR_BAD_SLOT 4      /* slot outside the pool                       */
+#define PA_DEVERR_TIMEOUT 8       /* a bounded pipeline wait expired             */
+
+/* Human-readable text of a status code (static storage, never NULL). */
+const char* pa_get_error_string(int status);
+
+/*
+ * Cache write ("PagedAttention原理" §3.3.4, append_token: a new token's K/V goes
+ * into the next position of its sequence's last page).  For every token t with
+ * slot = slot_mapping[t] >= 0:
+ *     k_cache[slot / block_size][h][slot % block_size][:] = k[t][h][:]   (all h)
+ * and the same for v.  Negative slots are padding and write nothing; a slot at
+ * or beyond num_blocks * block_size sets PA_DEVERR_BAD_SLOT and writes nothing.
+ * slot_mapping is a device int64 array of num_tokens entries.  Bytes are copied
+ * exactly.  Slots must be distinct (two tokens to one slot race).
+ */
+int pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                         const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                         int head_dim, int block_size, int num_blocks, pa_dtype dtype,
+                         int32_t* device_errors, void* stream);
+
+/*
+ * Copy-on-write page copy ("mlx-paged-attention", feature 2).  For each pair
+ * (src, dst) in src_dst_pairs (device int64 [num_pairs][2]):
+ *     k_cache[dst] = k_cache[src]; v_cache[dst] = v_cache[src]
+ * where one "block" is block_bytes bytes (num_kv_heads * block_size * head_dim *
+ * element size, a multiple of 16).  Destinations must be distinct and must not
+ * also be sources.  Ids outside [0, num_blocks) set PA_DEVERR_BAD_BLOCK and that
+ * pair is skipped.
+ */
+int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst_pairs, int num_pairs,
+                   size_t block_bytes, int num_blocks, int32_t* device_errors, void* stream);
+
+/*
+ * Split size (in tokens) pa_decode uses when chunk_tokens == 0: the work of each
+ * (sequence, kv head) is cut into chunks of this many tokens, chosen from the
+ * batch, the longest context and the current device's SM count.
+ */
+int pa_decode_chunk_tokens(int num_seqs, int num_kv_heads, int block_size, int max_context_len);
+
+/* Bytes of workspace pa_decode needs for these arguments on the current device. */
+size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int block_size, int max_context_len, int chunk_tokens);
+
+/*
+ * Single-token paged decode attention ("PagedAttentionMetal", "注意力计算优化";
+ * "PagedAttention原理" §3.4: the mathematics is ordinary softmax attention).
+ * For sequence b, query head i, kv head h = i / (num_q_heads / num_kv_heads),
+ * length L = context_lens[b] (it counts the token just written), tokens
+ * t = 0 .. L-1 at page block_tables[b][t / block_size], offset t % block_size:
+ *     s_t = scale * <q[b][i], K_t>,  p = softmax(s),  out[b][i] = sum_t p_t V_t.
+ * Rows with L == 0 are written as zeros.  Accumulation is fp32; out has the
+ * input element type.  Table entries past a sequence's pages are not read.
+ *
+ * max_context_len must be >= every context_lens[b] and <= max_blocks_per_seq *
+ * block_size (it sizes the launch and the workspace); a length outside
+ * [0, max_context_len] sets PA_DEVERR_BAD_LENGTH and is clamped.
+ * chunk_tokens: 0 chooses automatically (pa_decode_chunk_tokens); otherwise a
+ * multiple of 16 and of block_size, at most 32 * block_size.  Contexts longer
+ * than one chunk are split and merged by a second kernel (log-sum-exp).
+ * workspace: caller-owned device scratch of at least pa_decode_workspace_size()
+ * bytes with the same arguments, 256-byte aligned; it carries no state between
+ * calls, but two calls in flight at once must not share it.
+ */
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, const int32_t* context_lens, float scale,
+              int num_kv_heads, int num_seqs, int num_q_heads, int head_dim, int block_size,
+              int num_blocks, int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
+              int chunk_tokens, void* workspace, size_t workspace_bytes,
+              int32_t* device_errors, void* stream);
+
+/* Synchronise `stream`, copy *device_errors to *host_flags, and zero it on the
+ * device when `clear` is non-zero.  This is the one call that waits. */
+int pa_read_device_errors(int32_t* device_errors, int32_t* host_flags, int clear, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Host block manager ("PagedAttention原理" §3.3.2-§3.3.4, "mlx-paged-attention"
+ * feature 2).  Host memory only, no CUDA.  Not thread-safe: one owner at a time.
+ *   - The free list starts as initial_free_order (or 0..num_blocks-1 when NULL);
+ *     pages are taken from its END and returned to its end (LIFO), in page-table
+ *     order when a sequence is freed.
+ *   - add_seq gives a new sequence its first page at once (length 0).
+ *   - append_slot reserves the slot of the sequence's next token: a new page when
+ *     the last one is full; a copy when the target page is shared (refcount > 1):
+ *     a fresh page replaces it in this sequence's table, the old page loses one
+ *     reference, and (*cow_src, *cow_dst) name the copy the caller must run with
+ *     pa_copy_blocks before writing the token.  Otherwise *cow_src = *cow_dst = -1.
+ *     slot = physical_page * block_size + offset.
+ *   - fork gives `child` the parent's table and length, one more reference each.
+ *   - free drops one reference per page; pages at zero return to the free list.
+ *   - PA_ERR_OUT_OF_BLOCKS leaves every piece of state unchanged.
+ * ------------------------------------------------------------------------- */
+typedef struct pa_bm pa_bm;
+
+int pa_bm_create(int num_blocks, int block_size, const int32_t* initial_free_order, pa_bm** out);
+void pa_bm_destroy(pa_bm* bm);
+int pa_bm_add_seq(pa_bm* bm, int64_t seq_id);
+int pa_bm_append_slot(pa_bm* bm, int64_t seq_id, int64_t* slot, int64_t* cow_src, int64_t* cow_dst);
+int pa_bm_fork(pa_bm* bm, int64_t parent, int64_t child);
+int pa_bm_free(pa_bm* bm, int64_t seq_id);
+/* Copy up to `cap` page ids of seq_id's table to out; *num_pages and *length
+ * receive its page count and token count. */
+int pa_bm_block_table(const pa_bm* bm, int64_t seq_id, int32_t* out, int cap, int* num_pages,
+                      int* length);
+/* Reference count of a page (>= 0), or PA_ERR_INVALID_ARG. */
+int pa_bm_refcount(const pa_bm* bm, int32_t block);
+int pa_bm_num_free(const pa_bm* bm);
+/* Copy the free list, bottom to top (the next page taken is the last), up to cap. */
+int pa_bm_free_list(const pa_bm* bm, int32_t* out, int cap);
+/* out4 = {pages in use, free pages, pages shared (refcount > 1),
+ *         unused token slots summed over each sequence's pages}. */
+int pa_bm_stats(const pa_bm* bm, int64_t* out4);
+/* One decode step for n sequences, in the given order: append_slot for each,
+ * slots[j] its slot, and each copy needed appended to cow_pairs ([n][2] capacity)
+ * with *num_cow their count.  On PA_ERR_OUT_OF_BLOCKS, *num_done sequences were
+ * served (their effects stay) and the rest untouched. */
+int pa_bm_append_slots(pa_bm* bm, const int64_t* seq_ids, int n, int64_t* slots,
+                       int64_t* cow_pairs, int* num_cow, int* num_done);
+/* Fill tables [n][max_blocks] (padded with -1) and context_lens [n] for seq_ids. */
+int pa_bm_build_block_tables(const pa_bm* bm, const int64_t* seq_ids, int n, int32_t* tables,
+                             int max_blocks, int32_t* context_lens);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PAGEDATTN_PA_H */

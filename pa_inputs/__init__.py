@@ -290,3 +290,38 @@ def random_bm_ops(seed: int, num_ops: int, max_seqs: int = 6):
         b = int(rng.integers(0, max_seqs))
         ops.append((kind, a, b))
     return ops
+
+
+# --------------------------------------------------------------------------
+# Driving a block manager through the shared-prefix script.  Every decision
+# (which page, whether to copy) is the manager's; this only issues the calls.
+# --------------------------------------------------------------------------
+def shared_prefix_ids(script: SharedPrefixScript):
+    P, C = script.num_parents, script.children_per_parent
+    parents = [1_000_000 + p for p in range(P)]
+    children = [p * C + c for p in range(P) for c in range(C)]
+    return parents, children
+
+
+def shared_prefix_prefill(manager, script: SharedPrefixScript):
+    """Parents take their prompt plus generated tokens, fork their children and
+    leave.  Returns per-parent slot arrays (where the prefix rows go)."""
+    parents, _ = shared_prefix_ids(script)
+    C = script.children_per_parent
+    prefix_slots = []
+    for p, pid in enumerate(parents):
+        manager.add_seq(pid)
+        slots = [manager.append_slot(pid)[0] for _ in range(int(script.prefix_lens[p]))]
+        prefix_slots.append(np.asarray(slots, dtype=np.int64))
+        for c in range(C):
+            manager.fork(pid, p * C + c)
+        manager.free(pid)
+    return prefix_slots
+
+
+def shared_prefix_finish_order(script: SharedPrefixScript):
+    """Step at which each child finishes (after its tail) and the order of the
+    children finishing at the same step."""
+    _, children = shared_prefix_ids(script)
+    order = sorted(children, key=lambda c: (int(script.tails[c]), float(script.finish_keys[c])))
+    return order

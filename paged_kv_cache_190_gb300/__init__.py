@@ -1,0 +1,17 @@
+"""GB300-native paged-KV-cache decode.
+
+A thin Python binding of ``libpagedattn.so`` (CUDA C++ for sm_103a, C ABI in
+``include/pa.h``).  Each function here has the C entry point's name and only
+marshals arguments: torch tensors become raw device pointers, the current CUDA
+stream becomes a ``cudaStream_t``.  Every step of the path runs in the library's
+kernels; there is no fallback -- if the library is missing or was not built,
+the first call raises.
+
+PyTorch provides device memory and streams; nothing else.
+"""
+from ._lib import (  # noqa: F401
+    PA_BF16, PA_F32, PA_DEVERR_BAD_BLOCK, PA_DEVERR_BAD_LENGTH, PA_DEVERR_BAD_SLOT,
+    PA_DEVERR_TIMEOUT, BlockManager, OutOfBlocks, PaError, library, library_path,
+    pa_copy_blocks, pa_decode, pa_decode_chunk_tokens, pa_decode_workspace_size,
+    pa_get_error_string, pa_read_device_errors, pa_reshape_and_cache, EXPORTED_SYMBOLS,
+)

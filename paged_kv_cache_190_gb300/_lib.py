@@ -1,0 +1,317 @@
+"""ctypes binding of libpagedattn (argument marshalling only)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(PKG, "libpagedattn.so")
+
+PA_F32, PA_BF16 = 0, 1
+PA_OK = 0
+PA_ERR_OUT_OF_BLOCKS = -3
+PA_DEVERR_BAD_BLOCK, PA_DEVERR_BAD_LENGTH, PA_DEVERR_BAD_SLOT, PA_DEVERR_TIMEOUT = 1, 2, 4, 8
+
+# Every function include/pa.h declares (checked by the tests).
+EXPORTED_SYMBOLS = [
+    "pa_get_error_string", "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_chunk_tokens",
+    "pa_decode_workspace_size", "pa_decode", "pa_read_device_errors",
+    "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq", "pa_bm_append_slot", "pa_bm_fork",
+    "pa_bm_free", "pa_bm_block_table", "pa_bm_refcount", "pa_bm_num_free", "pa_bm_free_list",
+    "pa_bm_stats", "pa_bm_append_slots", "pa_bm_build_block_tables",
+]
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int
+_i64 = ctypes.c_int64
+_sz = ctypes.c_size_t
+_pi32 = ctypes.POINTER(ctypes.c_int32)
+_pi64 = ctypes.POINTER(ctypes.c_int64)
+
+_SIGNATURES = {
+    "pa_get_error_string": (ctypes.c_char_p, [_i32]),
+    "pa_reshape_and_cache": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32,
+                                    _vp, _vp]),
+    "pa_copy_blocks": (_i32, [_vp, _vp, _vp, _i32, _sz, _i32, _vp, _vp]),
+    "pa_decode_chunk_tokens": (_i32, [_i32, _i32, _i32, _i32]),
+    "pa_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
+    "pa_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _i32, _i32, _i32, _i32,
+                         _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
+    "pa_read_device_errors": (_i32, [_vp, _pi32, _i32, _vp]),
+    "pa_bm_create": (_i32, [_i32, _i32, _pi32, ctypes.POINTER(_vp)]),
+    "pa_bm_destroy": (None, [_vp]),
+    "pa_bm_add_seq": (_i32, [_vp, _i64]),
+    "pa_bm_append_slot": (_i32, [_vp, _i64, _pi64, _pi64, _pi64]),
+    "pa_bm_fork": (_i32, [_vp, _i64, _i64]),
+    "pa_bm_free": (_i32, [_vp, _i64]),
+    "pa_bm_block_table": (_i32, [_vp, _i64, _pi32, _i32, _pi32, _pi32]),
+    "pa_bm_refcount": (_i32, [_vp, ctypes.c_int32]),
+    "pa_bm_num_free": (_i32, [_vp]),
+    "pa_bm_free_list": (_i32, [_vp, _pi32, _i32]),
+    "pa_bm_stats": (_i32, [_vp, _pi64]),
+    "pa_bm_append_slots": (_i32, [_vp, _pi64, _i32, _pi64, _pi64, _pi32, _pi32]),
+    "pa_bm_build_block_tables": (_i32, [_vp, _pi64, _i32, _pi32, _i32, _pi32]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def library():
+    """Load libpagedattn.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"{_LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                    "g.build()\"` (needs nvcc); there is no fallback implementation")
+            lib = ctypes.CDLL(_LIB_PATH)
+            for name, (res, args) in _SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+class PaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {pa_get_error_string(status)} (status {status})")
+
+
+class OutOfBlocks(PaError):
+    pass
+
+
+def _check(rc: int, what: str):
+    if rc != PA_OK:
+        if rc == PA_ERR_OUT_OF_BLOCKS:
+            raise OutOfBlocks(rc, what)
+        raise PaError(rc, what)
+
+
+def pa_get_error_string(status: int) -> str:
+    return library().pa_get_error_string(int(status)).decode()
+
+
+# ---------------------------------------------------------------- marshalling
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    import torch
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    if t.dtype == torch.float32:
+        return PA_F32
+    raise TypeError(f"unsupported element type {t.dtype}")
+
+
+def _need_cuda_contig(name, t):
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+# ----------------------------------------------------------------- device ops
+def pa_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, device_errors=None, stream=None):
+    """k, v [T, Hkv, D]; caches [NB, Hkv, bs, D]; slot_mapping int64 [T] (see pa.h)."""
+    import torch
+    for n, t in (("k", k), ("v", v), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("slot_mapping", slot_mapping)):
+        _need_cuda_contig(n, t)
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    NB, Hkv, bs, D = k_cache.shape
+    rc = library().pa_reshape_and_cache(
+        _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), int(k.shape[0]),
+        int(Hkv), int(D), int(bs), int(NB), _dtype_code(k_cache), _ptr(device_errors),
+        _stream(stream, k_cache.device))
+    _check(rc, "pa_reshape_and_cache")
+
+
+def pa_copy_blocks(k_cache, v_cache, src_dst_pairs, device_errors=None, stream=None):
+    """src_dst_pairs int64 [P, 2] on the device (see pa.h)."""
+    import torch
+    for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("src_dst_pairs", src_dst_pairs)):
+        _need_cuda_contig(n, t)
+    if src_dst_pairs.dtype != torch.int64:
+        raise TypeError("src_dst_pairs must be int64")
+    NB = k_cache.shape[0]
+    block_bytes = k_cache[0].numel() * k_cache.element_size()
+    rc = library().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(src_dst_pairs),
+                                  int(src_dst_pairs.shape[0]), block_bytes, int(NB),
+                                  _ptr(device_errors), _stream(stream, k_cache.device))
+    _check(rc, "pa_copy_blocks")
+
+
+def pa_decode_chunk_tokens(num_seqs, num_kv_heads, block_size, max_context_len) -> int:
+    rc = library().pa_decode_chunk_tokens(int(num_seqs), int(num_kv_heads), int(block_size),
+                                          int(max_context_len))
+    if rc < 0:
+        _check(rc, "pa_decode_chunk_tokens")
+    return rc
+
+
+def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                             max_context_len, chunk_tokens=0) -> int:
+    return int(library().pa_decode_workspace_size(int(num_seqs), int(num_q_heads),
+                                                  int(num_kv_heads), int(head_dim),
+                                                  int(block_size), int(max_context_len),
+                                                  int(chunk_tokens)))
+
+
+def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
+              max_context_len, workspace=None, chunk_tokens=0, device_errors=None, stream=None):
+    """out, q [B, Hq, D]; caches [NB, Hkv, bs, D]; block_tables int32 [B, max_blocks];
+    context_lens int32 [B] (see pa.h).  ``workspace``: a uint8 CUDA tensor of at
+    least pa_decode_workspace_size() bytes; allocated here when None."""
+    import torch
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("block_tables", block_tables), ("context_lens", context_lens)):
+        _need_cuda_contig(n, t)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    if int(Hkv) != int(num_kv_heads):
+        raise ValueError("num_kv_heads does not match the cache shape")
+    if workspace is None:
+        nbytes = pa_decode_workspace_size(B, Hq, Hkv, D, bs, max_context_len, chunk_tokens)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    rc = library().pa_decode(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        float(scale), int(num_kv_heads), int(B), int(Hq), int(D), int(bs), int(NB),
+        int(block_tables.shape[1]), int(max_context_len), _dtype_code(q), int(chunk_tokens),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(device_errors),
+        _stream(stream, q.device))
+    _check(rc, "pa_decode")
+    return out
+
+
+def pa_read_device_errors(device_errors, clear=True, stream=None) -> int:
+    """Synchronise the stream and return (and optionally clear) the error bits."""
+    flags = ctypes.c_int32(0)
+    rc = library().pa_read_device_errors(_ptr(device_errors), ctypes.byref(flags), int(clear),
+                                         _stream(stream, device_errors.device))
+    _check(rc, "pa_read_device_errors")
+    return int(flags.value)
+
+
+# -------------------------------------------------------------- block manager
+def _i64p(a):
+    return a.ctypes.data_as(_pi64)
+
+
+def _i32p(a):
+    return a.ctypes.data_as(_pi32)
+
+
+class BlockManager:
+    """Host block manager (C++ in the library): LIFO free list, reference
+    counts, fork and copy-on-write -- see pa.h for the exact rules."""
+
+    def __init__(self, num_blocks: int, block_size: int, initial_free_order=None):
+        lib = library()
+        self._lib = lib
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+        handle = ctypes.c_void_p()
+        order = None
+        if initial_free_order is not None:
+            self._order = np.ascontiguousarray(initial_free_order, dtype=np.int32)
+            order = _i32p(self._order)
+        _check(lib.pa_bm_create(self.num_blocks, self.block_size, order, ctypes.byref(handle)),
+               "pa_bm_create")
+        self._h = handle
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.pa_bm_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def add_seq(self, seq_id: int):
+        _check(self._lib.pa_bm_add_seq(self._h, int(seq_id)), "pa_bm_add_seq")
+
+    def append_slot(self, seq_id: int):
+        slot, src, dst = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(self._lib.pa_bm_append_slot(self._h, int(seq_id), ctypes.byref(slot),
+                                           ctypes.byref(src), ctypes.byref(dst)),
+               "pa_bm_append_slot")
+        return slot.value, src.value, dst.value
+
+    def fork(self, parent: int, child: int):
+        _check(self._lib.pa_bm_fork(self._h, int(parent), int(child)), "pa_bm_fork")
+
+    def free(self, seq_id: int):
+        _check(self._lib.pa_bm_free(self._h, int(seq_id)), "pa_bm_free")
+
+    def block_table(self, seq_id: int):
+        n, length = ctypes.c_int(), ctypes.c_int()
+        _check(self._lib.pa_bm_block_table(self._h, int(seq_id), None, 0, ctypes.byref(n),
+                                           ctypes.byref(length)), "pa_bm_block_table")
+        out = np.zeros(max(n.value, 1), dtype=np.int32)
+        _check(self._lib.pa_bm_block_table(self._h, int(seq_id), _i32p(out), n.value,
+                                           ctypes.byref(n), ctypes.byref(length)),
+               "pa_bm_block_table")
+        return out[:n.value].tolist(), length.value
+
+    def refcount(self, block: int) -> int:
+        rc = self._lib.pa_bm_refcount(self._h, int(block))
+        if rc < 0:
+            _check(rc, "pa_bm_refcount")
+        return rc
+
+    def num_free(self) -> int:
+        return self._lib.pa_bm_num_free(self._h)
+
+    def free_list(self):
+        n = self._lib.pa_bm_free_list(self._h, None, 0)
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        self._lib.pa_bm_free_list(self._h, _i32p(out), n)
+        return out[:n].tolist()
+
+    def stats(self):
+        out = np.zeros(4, dtype=np.int64)
+        _check(self._lib.pa_bm_stats(self._h, _i64p(out)), "pa_bm_stats")
+        return tuple(int(x) for x in out)
+
+    def append_slots(self, seq_ids):
+        """One decode step: returns (slots int64 [n], cow_pairs int64 [P, 2])."""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = ids.shape[0]
+        slots = np.zeros(max(n, 1), dtype=np.int64)
+        pairs = np.zeros((max(n, 1), 2), dtype=np.int64)
+        num_cow, done = ctypes.c_int(), ctypes.c_int()
+        rc = self._lib.pa_bm_append_slots(self._h, _i64p(ids), n, _i64p(slots), _i64p(pairs),
+                                          ctypes.byref(num_cow), ctypes.byref(done))
+        _check(rc, "pa_bm_append_slots")
+        return slots[:n], pairs[:num_cow.value]
+
+    def build_block_tables(self, seq_ids, max_blocks: int):
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = ids.shape[0]
+        tables = np.zeros((max(n, 1), max_blocks), dtype=np.int32)
+        lens = np.zeros(max(n, 1), dtype=np.int32)
+        _check(self._lib.pa_bm_build_block_tables(self._h, _i64p(ids), n, _i32p(tables),
+                                                  int(max_blocks), _i32p(lens)),
+               "pa_bm_build_block_tables")
+        return tables[:n], lens[:n]

@@ -1,0 +1,47 @@
+// Launch of one instantiation of the persistent decode kernel.  Each element
+// type gets its own translation unit (decode_bf16.cu, decode_f32.cu) so the
+// instantiations compile in parallel.
+#pragma once
+
+#include <atomic>
+
+#include "paged_decode.cuh"
+
+namespace pa {
+
+template <bool BF16, int D, int G>
+cudaError_t run_decode_kernel(const DecodeKernelParams& kp, int grid, int device,
+                              cudaStream_t stream) {
+  using Tr = DecodeTraits<BF16, D, G>;
+  // the opt-in to more than 48 KiB of dynamic shared memory is per device
+  static std::atomic<uint64_t> configured{0};
+  const uint64_t bit = 1ull << (device & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    const cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<BF16, D, G>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               Tr::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  paged_decode_kernel<BF16, D, G>
+      <<<grid, (kConsumerWarps + 1) * 32, Tr::SMEM_BYTES, stream>>>(kp);
+  return cudaGetLastError();
+}
+
+template <bool BF16>
+cudaError_t run_decode_dispatch(int head_dim, int group, const DecodeKernelParams& kp, int grid,
+                                int device, cudaStream_t stream) {
+#define PA_CASE(D_, G_) \
+  if (head_dim == D_ && group == G_) return run_decode_kernel<BF16, D_, G_>(kp, grid, device, stream);
+  PA_CASE(64, 1) PA_CASE(64, 2) PA_CASE(64, 4) PA_CASE(64, 8)
+  PA_CASE(128, 1) PA_CASE(128, 2) PA_CASE(128, 4) PA_CASE(128, 8)
+#undef PA_CASE
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t run_decode_bf16(int head_dim, int group, const DecodeKernelParams& kp, int grid,
+                            int device, cudaStream_t stream);
+cudaError_t run_decode_f32(int head_dim, int group, const DecodeKernelParams& kp, int grid,
+                           int device, cudaStream_t stream);
+
+}  // namespace pa

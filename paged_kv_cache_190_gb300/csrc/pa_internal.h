@@ -1,0 +1,57 @@
+// Internal launcher interface between the C ABI (capi.cu) and the kernels.
+// Every launcher only enqueues on `stream` and returns a cudaError_t.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+namespace pa {
+
+// Workspace of one pa_decode call, carved from the caller's buffer.
+struct DecodeWorkspace {
+  int32_t* header;       // [0] work counter, [1] total chunks, rest reserved
+  int32_t* chunk_base;   // [num_seqs + 1] first global chunk of each sequence
+  int4* work;            // [max_chunks] {b, chunk index, length, global chunk}
+  float* part_lse;       // [max_chunks][num_q_heads] base-2 log-sum-exp of a chunk
+  float* part_out;       // [max_chunks][num_q_heads][head_dim] chunk output, normalised
+  int64_t max_chunks;
+};
+
+struct WorkspaceLayout {
+  size_t chunk_base, work, part_lse, part_out, total;
+  int64_t max_chunks;
+};
+
+WorkspaceLayout decode_workspace_layout(int num_seqs, int num_q_heads, int head_dim,
+                                        int max_context_len, int chunk_tokens);
+
+struct DecodeArgs {
+  void* out;
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  float scale;
+  int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks;
+  int max_blocks_per_seq, max_context_len, chunk_tokens;
+  int bf16;  // element type: 1 bf16, 0 f32
+  DecodeWorkspace ws;
+  int32_t* device_errors;
+  int num_sms;
+};
+
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+
+cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
+                                     const int64_t* slot_mapping, int num_tokens,
+                                     int num_kv_heads, int row_bytes, int block_size,
+                                     int num_blocks, int32_t* device_errors, cudaStream_t stream);
+
+cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int num_pairs,
+                               size_t block_bytes, int num_blocks, int32_t* device_errors,
+                               cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,542 @@
+// Paged decode attention for sm_103a: a persistent, warp-specialised kernel.
+//
+// What it computes ("PagedAttention原理" §3.4: paging leaves the attention
+// mathematics unchanged; "PagedAttentionMetal", "注意力计算优化": look the
+// physical page up in the block table, stage the K/V block in shared memory,
+// batch variable lengths without padding): for each sequence b and query head
+// i, softmax(scale * q K^T) V over the sequence's L_b tokens, read page by page
+// through block_tables[b].
+//
+// How (GB300 design, not a translation of any page's kernel):
+//   * Work item = (sequence, kv head, chunk of `chunk_tokens` tokens).  A tiny
+//     plan kernel lists the (sequence, chunk) pairs; items are handed out by an
+//     atomic counter, so lognormal lengths balance across SMs.
+//   * One CTA per SM, persistent.  Warp 8 is the producer: per item it loads the
+//     chunk's block-table slice with one coalesced read, copies the GQA group's
+//     q rows into shared memory, then streams 16-token K and V tiles (one
+//     contiguous 4 KiB run each for bf16, head_dim 128) with bulk asynchronous
+//     copies (cp.async.bulk) into a ring of S stages guarded by mbarriers.
+//   * Warps 0..7 consume: stage s always belongs to warp s % 8, so each warp
+//     keeps its own online-softmax state (running max m, sum l, accumulator) in
+//     fp32 registers for every query head of the GQA group -- one K/V read
+//     serves the whole group.  At the end of an item the 8 partial states are
+//     merged through shared memory (log-sum-exp) and the item's rows are written
+//     either straight to `out` (single-chunk sequence) or as a normalised
+//     partial plus its base-2 log-sum-exp for the split-K merge kernel.
+//   * QK: 8 lanes per token, 4 tokens per pass, 16-byte shared loads that are
+//     contiguous within each quarter warp (no bank conflicts); the 8-lane dot
+//     products are reduced by a butterfly that leaves each lane with whole sums.
+//   * PV: each lane owns head_dim / 32 output columns for every head of the group.
+//   * Every wait is bounded; on expiry the kernel reports PA_DEVERR_TIMEOUT,
+//     drains its own copies in flight and returns.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pa_device.cuh"
+#include "pa_internal.h"
+
+namespace pa {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kItemSlots = 8;        // items the producer may run ahead
+constexpr int kSmemBudget = 227 * 1024;
+constexpr unsigned kFull = 0xffffffffu;
+
+struct ItemDesc {
+  int b, h, chunk, len, gchunk, n_units, n_tokens, single;
+};
+
+template <bool BF16, int D, int G>
+struct DecodeTraits {
+  static constexpr int ELT = BF16 ? 2 : 4;
+  static constexpr int ROW_BYTES = D * ELT;
+  static constexpr int UT = ROW_BYTES >= 512 ? 8 : 16;          // tokens per stage
+  static constexpr int TILE_BYTES = UT * ROW_BYTES;            // K (or V) of one stage
+  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
+  static constexpr int Q_BYTES = G * ROW_BYTES;
+  static constexpr int CE = 16 / ELT;                          // elements per 16-byte chunk
+  static constexpr int CPR = ROW_BYTES / 16;                   // chunks per row
+  static constexpr int NCH = CPR / 8;                          // chunks per lane in QK
+  static constexpr int EPL = NCH * CE;                         // elements per lane in QK
+  static constexpr int CPL = D / 32;                           // PV columns per lane
+  static constexpr int P = UT / 4;                             // QK passes per stage
+  static constexpr int N = P * G;                              // dot products per lane
+  static constexpr int RC = N >= 8 ? N / 8 : 1;                // sums per lane after reduction
+  // butterfly levels that split the values (the rest only add): lane bits
+  // below 3 - LV hold duplicates
+  static constexpr int LV = N >= 8 ? 3 : (N >= 4 ? 2 : 1);
+  static constexpr int DUP_MASK_END = 1 << (3 - LV);
+  static_assert(CPR % 8 == 0, "head row must split into 8 lanes of 16-byte chunks");
+  static_assert(D % 32 == 0, "head_dim must split over 32 lanes");
+
+  // shared memory carve-up (bytes)
+  static constexpr int MERGE_ACC = kConsumerWarps * G * D * 4;
+  static constexpr int MERGE_ML = kConsumerWarps * G * 2 * 4;
+  static constexpr int PS = kConsumerWarps * UT * G * 4;
+  static constexpr int QBUF = kItemSlots * Q_BYTES;
+  static constexpr int DESC = kItemSlots * static_cast<int>(sizeof(ItemDesc));
+  static constexpr int FIXED = MERGE_ACC + MERGE_ML + PS + QBUF + DESC + 64 /*flags*/ +
+                               (2 * kItemSlots + 4) * 8 + 1024 /*alignment slack*/;
+  static constexpr int S_RAW = (kSmemBudget - FIXED) / (STAGE_BYTES + 2 * 8 + 4);
+  static constexpr int S_CAP = S_RAW > 32 ? 32 : S_RAW;
+  static constexpr int S = (S_CAP / kConsumerWarps) * kConsumerWarps;
+  static_assert(S >= kConsumerWarps, "at least one stage per consumer warp");
+
+  static constexpr int OFF_STAGES = 0;
+  static constexpr int OFF_QBUF = OFF_STAGES + S * STAGE_BYTES;
+  static constexpr int OFF_MACC = OFF_QBUF + QBUF;
+  static constexpr int OFF_MML = OFF_MACC + MERGE_ACC;
+  static constexpr int OFF_PS = OFF_MML + MERGE_ML;
+  static constexpr int OFF_DESC = OFF_PS + PS;
+  static constexpr int OFF_SFLAG = OFF_DESC + DESC;
+  static constexpr int OFF_ABORT = OFF_SFLAG + S * 4;
+  static constexpr int OFF_BARS = ((OFF_ABORT + 4 + 7) / 8) * 8;
+  // barriers: full[S], empty[S], item_full[NI], item_empty[NI], merge_full, merge_empty
+  static constexpr int NUM_BARS = 2 * S + 2 * kItemSlots + 2;
+  static constexpr int SMEM_BYTES = OFF_BARS + NUM_BARS * 8;
+  static_assert(SMEM_BYTES <= kSmemBudget, "shared memory over budget");
+};
+
+struct DecodeKernelParams {
+  void* out;
+  const char* q;
+  const char* k_cache;
+  const char* v_cache;
+  const int32_t* block_tables;
+  float scale_log2;                 // scale * log2(e): logits are kept in base 2
+  int num_q_heads, num_kv_heads, block_size, num_blocks, max_blocks_per_seq, chunk_tokens;
+  int32_t* header;                  // [0] item counter, [1] total chunks
+  const int4* work;
+  float* part_lse;
+  float* part_out;
+  int32_t* device_errors;
+};
+
+// Butterfly step over lane bit `mask` (within 8-lane groups): lanes with the
+// bit set keep the upper half of the values, the others the lower half, and each
+// adds its partner's copy of the half it keeps.
+template <int COUNT>
+__device__ __forceinline__ void butterfly_level(float* v, int lane, int mask) {
+  if constexpr (COUNT >= 2) {
+    constexpr int H = COUNT / 2;
+    const bool upper = (lane & mask) != 0;
+#pragma unroll
+    for (int i = 0; i < H; ++i) {
+      const float send = upper ? v[i] : v[i + H];
+      const float keep = upper ? v[i + H] : v[i];
+      v[i] = keep + __shfl_xor_sync(kFull, send, mask);
+    }
+  } else {
+    v[0] += __shfl_xor_sync(kFull, v[0], mask);
+  }
+}
+
+template <typename Tr>
+__device__ __forceinline__ void unpack_chunk(const uint4& c, float* dst) {
+  if constexpr (Tr::ELT == 2) {
+    dst[0] = bf16_lo(c.x); dst[1] = bf16_hi(c.x);
+    dst[2] = bf16_lo(c.y); dst[3] = bf16_hi(c.y);
+    dst[4] = bf16_lo(c.z); dst[5] = bf16_hi(c.z);
+    dst[6] = bf16_lo(c.w); dst[7] = bf16_hi(c.w);
+  } else {
+    dst[0] = __uint_as_float(c.x); dst[1] = __uint_as_float(c.y);
+    dst[2] = __uint_as_float(c.z); dst[3] = __uint_as_float(c.w);
+  }
+}
+
+// Load this lane's CPL value columns of row `t` as floats.
+template <typename Tr>
+__device__ __forceinline__ void load_v_cols(const char* vt, int t, int lane, float* v) {
+  const char* row = vt + t * Tr::ROW_BYTES + lane * Tr::CPL * Tr::ELT;
+  if constexpr (Tr::ELT == 2) {
+    if constexpr (Tr::CPL == 4) {
+      const uint2 w = *reinterpret_cast<const uint2*>(row);
+      v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x); v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+    } else {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(row);
+      v[0] = bf16_lo(w); v[1] = bf16_hi(w);
+    }
+  } else {
+    if constexpr (Tr::CPL == 4) {
+      const float4 w = *reinterpret_cast<const float4*>(row);
+      v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
+    } else {
+      const float2 w = *reinterpret_cast<const float2*>(row);
+      v[0] = w.x; v[1] = w.y;
+    }
+  }
+}
+
+template <bool BF16, int D, int G>
+__global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
+    paged_decode_kernel(const DecodeKernelParams p) {
+  using Tr = DecodeTraits<BF16, D, G>;
+  constexpr int S = Tr::S;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  char* stages = reinterpret_cast<char*>(smem + Tr::OFF_STAGES);
+  char* qbuf = reinterpret_cast<char*>(smem + Tr::OFF_QBUF);
+  float* macc = reinterpret_cast<float*>(smem + Tr::OFF_MACC);
+  float* mml = reinterpret_cast<float*>(smem + Tr::OFF_MML);
+  float* ps_all = reinterpret_cast<float*>(smem + Tr::OFF_PS);
+  ItemDesc* desc = reinterpret_cast<ItemDesc*>(smem + Tr::OFF_DESC);
+  volatile int* stage_bad = reinterpret_cast<volatile int*>(smem + Tr::OFF_SFLAG);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Tr::OFF_ABORT);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tr::OFF_BARS);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S;
+  uint64_t* item_full = bars + 2 * S;
+  uint64_t* item_empty = item_full + kItemSlots;
+  uint64_t* merge_full = item_empty + kItemSlots;
+  uint64_t* merge_empty = merge_full + 1;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int k = 0; k < kItemSlots; ++k) {
+      mbar_init(&item_full[k], 1);
+      mbar_init(&item_empty[k], kConsumerWarps);
+    }
+    mbar_init(merge_full, kConsumerWarps);
+    mbar_init(merge_empty, kConsumerWarps);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  const int Hkv = p.num_kv_heads;
+  const int bs = p.block_size;
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    const int total_items = p.header[1] * Hkv;
+    uint32_t unit_n = 0, item_k = 0;
+    bool ok = true;
+    for (;;) {
+      if (*abort_flag) { ok = false; break; }
+      int i = 0;
+      if (lane == 0) i = atomicAdd(&p.header[0], 1);
+      i = __shfl_sync(kFull, i, 0);
+      const int slot = item_k % kItemSlots;
+      int waited = 1;
+      if (lane == 0) waited = mbar_wait(&item_empty[slot], ((item_k / kItemSlots) & 1) ^ 1);
+      if (!__shfl_sync(kFull, waited, 0)) { ok = false; break; }
+      if (i >= total_items) {
+        if (lane == 0) {
+          desc[slot].b = -1;
+          mbar_arrive(&item_full[slot]);
+        }
+        break;
+      }
+      const int j = i / Hkv;
+      const int h = i - j * Hkv;
+      const int4 w = p.work[j];                  // {b, chunk, length, global chunk}
+      const int tok0 = w.y * p.chunk_tokens;
+      const int ntok = min(p.chunk_tokens, w.z - tok0);
+      const int n_units = (ntok + Tr::UT - 1) / Tr::UT;
+      const int page0 = tok0 / bs;
+      const int npages = (ntok + bs - 1) / bs;
+      int phys = -1;
+      if (lane < npages) {
+        phys = p.block_tables[static_cast<int64_t>(w.x) * p.max_blocks_per_seq + page0 + lane];
+        if (phys < 0 || phys >= p.num_blocks) {
+          report(p.device_errors, PA_DEVERR_BAD_BLOCK);
+          phys = -1;
+        }
+      }
+      if (lane == 0) {
+        ItemDesc d;
+        d.b = w.x; d.h = h; d.chunk = w.y; d.len = w.z; d.gchunk = w.w;
+        d.n_units = n_units; d.n_tokens = ntok; d.single = (w.z <= p.chunk_tokens);
+        desc[slot] = d;
+        mbar_arrive_expect_tx(&item_full[slot], Tr::Q_BYTES);
+        const char* qsrc =
+            p.q + (static_cast<int64_t>(w.x) * p.num_q_heads + static_cast<int64_t>(h) * G) *
+                      Tr::ROW_BYTES;
+        bulk_g2s(qbuf + slot * Tr::Q_BYTES, qsrc, Tr::Q_BYTES, &item_full[slot]);
+      }
+      for (int u = 0; u < n_units; ++u, ++unit_n) {
+        const int s = unit_n % S;
+        int got = 1;
+        if (lane == 0) got = mbar_wait(&empty[s], ((unit_n / S) & 1) ^ 1);
+        if (!__shfl_sync(kFull, got, 0)) { ok = false; break; }
+        const int tok = u * Tr::UT;
+        const int pp = __shfl_sync(kFull, phys, tok / bs);
+        if (lane == 0) {
+          if (pp >= 0) {
+            stage_bad[s] = 0;
+            mbar_arrive_expect_tx(&full[s], Tr::STAGE_BYTES);
+            const int64_t off =
+                ((static_cast<int64_t>(pp) * Hkv + h) * bs + (tok % bs)) * Tr::ROW_BYTES;
+            char* dst = stages + s * Tr::STAGE_BYTES;
+            bulk_g2s(dst, p.k_cache + off, Tr::TILE_BYTES, &full[s]);
+            bulk_g2s(dst + Tr::TILE_BYTES, p.v_cache + off, Tr::TILE_BYTES, &full[s]);
+          } else {
+            stage_bad[s] = 1;
+            mbar_arrive(&full[s]);
+          }
+        }
+      }
+      if (!ok) break;
+      ++item_k;
+    }
+    if (!ok) {
+      // Give up: tell the consumers, then wait (bounded) for our own copies.
+      if (lane == 0) {
+        report(p.device_errors, PA_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+        const uint32_t first = unit_n > static_cast<uint32_t>(S) ? unit_n - S : 0;
+        for (uint32_t n = first; n < unit_n; ++n) mbar_wait(&full[n % S], (n / S) & 1);
+        const uint32_t kfirst = item_k > kItemSlots ? item_k - kItemSlots : 0;
+        for (uint32_t k = kfirst; k < item_k; ++k)
+          mbar_wait(&item_full[k % kItemSlots], (k / kItemSlots) & 1);
+      }
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int j4 = lane >> 3;        // token within a pass
+  const int r = lane & 7;          // position within the 8-lane group
+  // After the butterfly this lane holds the sums of indices base .. base+RC-1
+  // (index = head * P + pass) -- all for one head, g_lane.
+  const int base = ((r >> 2) & 1) * (Tr::N / 2) + (Tr::N >= 4 ? ((r >> 1) & 1) * (Tr::N / 4) : 0) +
+                   (Tr::N >= 8 ? (r & 1) * (Tr::N / 8) : 0);
+  const int g_lane = base / Tr::P;
+  float* ps = ps_all + warp * Tr::UT * G;
+
+  uint32_t item_k = 0, unit_base = 0;
+  bool aborted = false;
+  for (;;) {
+    const int slot = item_k % kItemSlots;
+    if (!mbar_wait(&item_full[slot], (item_k / kItemSlots) & 1)) {
+      report(p.device_errors, PA_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+      break;
+    }
+    const ItemDesc d = desc[slot];
+    if (d.b < 0 || *abort_flag) break;
+
+    // q rows of the group, scaled so that logits come out in base 2
+    float qf[G][Tr::EPL];
+    {
+      const char* qs = qbuf + slot * Tr::Q_BYTES;
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int c = 0; c < Tr::NCH; ++c) {
+          const uint4 raw =
+              *reinterpret_cast<const uint4*>(qs + g * Tr::ROW_BYTES + (r + 8 * c) * 16);
+          unpack_chunk<Tr>(raw, &qf[g][c * Tr::CE]);
+#pragma unroll
+          for (int e = 0; e < Tr::CE; ++e) qf[g][c * Tr::CE + e] *= p.scale_log2;
+        }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&item_empty[slot]);
+
+    float m[G], acc[G][Tr::CPL];
+    float lsum = 0.f;                                  // this lane's share of l[g_lane]
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m[g] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < Tr::CPL; ++c) acc[g][c] = 0.f;
+    }
+
+    const uint32_t first =
+        unit_base + ((warp - static_cast<int>(unit_base % kConsumerWarps)) + kConsumerWarps) %
+                        kConsumerWarps;
+    for (uint32_t n = first; n < unit_base + d.n_units && !aborted; n += kConsumerWarps) {
+      const int s = n % S;
+      if (!mbar_wait(&full[s], (n / S) & 1)) {
+        report(p.device_errors, PA_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+        aborted = true;
+        break;
+      }
+      const int u = static_cast<int>(n - unit_base);
+      const int nt = min(Tr::UT, d.n_tokens - u * Tr::UT);
+      if (!stage_bad[s]) {
+        const char* kt = stages + s * Tr::STAGE_BYTES;
+        const char* vt = kt + Tr::TILE_BYTES;
+        // ---- scores: 8 lanes per token, 4 tokens per pass
+        float part[Tr::N];
+#pragma unroll
+        for (int ps_i = 0; ps_i < Tr::P; ++ps_i) {
+          const int t = 4 * ps_i + j4;
+          float kf[Tr::EPL];
+#pragma unroll
+          for (int c = 0; c < Tr::NCH; ++c) {
+            const uint4 raw =
+                *reinterpret_cast<const uint4*>(kt + t * Tr::ROW_BYTES + (r + 8 * c) * 16);
+            unpack_chunk<Tr>(raw, &kf[c * Tr::CE]);
+          }
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            float dot = 0.f;
+#pragma unroll
+            for (int e = 0; e < Tr::EPL; ++e) dot = fmaf(qf[g][e], kf[e], dot);
+            part[g * Tr::P + ps_i] = dot;
+          }
+        }
+        butterfly_level<Tr::N>(part, lane, 4);
+        butterfly_level<(Tr::N >= 4 ? Tr::N / 2 : 1)>(part, lane, 2);
+        butterfly_level<(Tr::N >= 8 ? Tr::N / 4 : 1)>(part, lane, 1);
+        // part[e], e < RC: score of head g_lane, token 4 * ((base % P) + e) + j4
+        float umax = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < Tr::RC; ++e) {
+          const int t = 4 * ((base % Tr::P) + e) + j4;
+          if (t >= nt) part[e] = -INFINITY;
+          umax = fmaxf(umax, part[e]);
+        }
+        // max over the lanes that hold the same head
+#pragma unroll
+        for (int mask = 1; mask < 8 / G; mask <<= 1)
+          umax = fmaxf(umax, __shfl_xor_sync(kFull, umax, mask));
+        umax = fmaxf(umax, __shfl_xor_sync(kFull, umax, 8));
+        umax = fmaxf(umax, __shfl_xor_sync(kFull, umax, 16));
+        float alpha[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float mu = __shfl_sync(kFull, umax, g * (8 / G));
+          const float mn = fmaxf(m[g], mu);
+          alpha[g] = fast_exp2(m[g] - mn);
+          m[g] = mn;
+        }
+        float m_lane = m[0];
+        float a_lane = alpha[0];
+#pragma unroll
+        for (int g = 1; g < G; ++g)
+          if (g_lane == g) { m_lane = m[g]; a_lane = alpha[g]; }
+        float psum = 0.f;
+#pragma unroll
+        for (int e = 0; e < Tr::RC; ++e) {
+          const int t = 4 * ((base % Tr::P) + e) + j4;
+          const float pr = fast_exp2(part[e] - m_lane);
+          psum += pr;
+          ps[t * G + g_lane] = pr;       // duplicate lanes (G == 1) store equal values
+        }
+        lsum = lsum * a_lane + psum;
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int c = 0; c < Tr::CPL; ++c) acc[g][c] *= alpha[g];
+        __syncwarp();
+        // ---- values: each lane owns CPL columns of every head
+        for (int t = 0; t < nt; ++t) {
+          float pv[G];
+          if constexpr (G % 4 == 0) {
+#pragma unroll
+            for (int g4 = 0; g4 < G; g4 += 4) {
+              const float4 w4 = *reinterpret_cast<const float4*>(ps + t * G + g4);
+              pv[g4] = w4.x; pv[g4 + 1] = w4.y; pv[g4 + 2] = w4.z; pv[g4 + 3] = w4.w;
+            }
+          } else if constexpr (G == 2) {
+            const float2 w2 = *reinterpret_cast<const float2*>(ps + t * 2);
+            pv[0] = w2.x; pv[1] = w2.y;
+          } else {
+            pv[0] = ps[t];
+          }
+          float vv[Tr::CPL];
+          load_v_cols<Tr>(vt, t, lane, vv);
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int c = 0; c < Tr::CPL; ++c) acc[g][c] = fmaf(pv[g], vv[c], acc[g][c]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+    }
+
+    // ---- merge the 8 warps' states for this item
+    // whole l for the lane's head: sum over the lanes sharing it, leaving out
+    // the low lane bits that only hold duplicates
+#pragma unroll
+    for (int mask = Tr::DUP_MASK_END; mask < 8 / G; mask <<= 1)
+      lsum += __shfl_xor_sync(kFull, lsum, mask);
+    lsum += __shfl_xor_sync(kFull, lsum, 8);
+    lsum += __shfl_xor_sync(kFull, lsum, 16);
+    if (item_k > 0 && !mbar_wait(merge_empty, (item_k - 1) & 1)) {
+      report(p.device_errors, PA_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+      aborted = true;
+    }
+    if (j4 == 0 && (r % (8 / G)) == 0) {
+      float mlane = m[0];
+#pragma unroll
+      for (int g = 1; g < G; ++g)
+        if (g_lane == g) mlane = m[g];
+      mml[(warp * G + g_lane) * 2 + 0] = mlane;
+      mml[(warp * G + g_lane) * 2 + 1] = lsum;
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float* dst = macc + (warp * G + g) * D + lane * Tr::CPL;
+      if constexpr (Tr::CPL == 4) {
+        *reinterpret_cast<float4*>(dst) = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+      } else {
+        *reinterpret_cast<float2*>(dst) = make_float2(acc[g][0], acc[g][1]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(merge_full);
+    if (!mbar_wait(merge_full, item_k & 1)) {
+      report(p.device_errors, PA_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+      aborted = true;
+    }
+    if (!aborted) {
+      const int tid = threadIdx.x;           // 0 .. 8*32-1 (consumers only)
+      for (int o2 = tid; o2 < G * D / 2; o2 += kConsumerWarps * 32) {
+        const int g = o2 / (D / 2);
+        const int dcol = (o2 - g * (D / 2)) * 2;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mml[(w * G + g) * 2]);
+        float lam = 0.f, o0 = 0.f, o1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+          const float f = fast_exp2(mml[(w * G + g) * 2] - M);
+          lam = fmaf(f, mml[(w * G + g) * 2 + 1], lam);
+          const float2 a = *reinterpret_cast<const float2*>(macc + (w * G + g) * D + dcol);
+          o0 = fmaf(f, a.x, o0);
+          o1 = fmaf(f, a.y, o1);
+        }
+        const float inv = 1.f / lam;
+        o0 *= inv;
+        o1 *= inv;
+        const int qh = d.h * G + g;
+        if (d.single) {
+          const int64_t o = (static_cast<int64_t>(d.b) * p.num_q_heads + qh) * D + dcol;
+          if constexpr (BF16) {
+            const uint32_t packed = f32_to_bf16_bits(o0) | (f32_to_bf16_bits(o1) << 16);
+            *reinterpret_cast<uint32_t*>(static_cast<char*>(p.out) + o * 2) = packed;
+          } else {
+            *reinterpret_cast<float2*>(static_cast<float*>(p.out) + o) = make_float2(o0, o1);
+          }
+        } else {
+          const int64_t row = static_cast<int64_t>(d.gchunk) * p.num_q_heads + qh;
+          *reinterpret_cast<float2*>(p.part_out + row * D + dcol) = make_float2(o0, o1);
+          if (dcol == 0) p.part_lse[row] = M + __log2f(lam);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(merge_empty);
+    unit_base += d.n_units;
+    ++item_k;
+    if (aborted) break;
+  }
+}
+
+}  // namespace pa

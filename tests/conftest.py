@@ -10,3 +10,9 @@ GOLDEN = os.path.join(ROOT, "tests", "golden")
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (runs the sm_103a library)")
+
+
+def pytest_sessionstart(session):
+    # Build (or confirm up to date) the CUDA library and the oracle's C code.
+    import __graft_entry__
+    __graft_entry__.build()

@@ -1,0 +1,179 @@
+"""The library's C++ block manager against the oracle's (CPU only): the hand
+traces, seeded random operation sequences (every result and the whole state
+compared after each step), the batched step call, and the shared-prefix script
+run to the end with every page back on the free list."""
+import pytest
+
+import numpy as np
+
+import oracle
+import pa_inputs
+import paged_kv_cache_190_gb300 as pa
+from bm_trace import check_invariants, load_trace, replay
+
+
+def _is_oom(fn):
+    try:
+        fn()
+    except pa.OutOfBlocks:
+        return True
+    return False
+
+
+@pytest.mark.parametrize("name", ["bm_teaching_trace.txt", "bm_refcount_cow_trace.txt"])
+def test_hand_trace(name):
+    header, steps = load_trace(name)
+    replay(pa.BlockManager(header["num_pages"], header["page_size"]), steps, _is_oom)
+
+
+def _state(bm, nb, live, refcount):
+    tables = {s: bm.block_table(s) for s in sorted(live)}
+    return tables, list(bm.free_list()), [refcount(p) for p in range(nb)]
+
+
+def _do(bm, op, errors):
+    kind, a, b = op
+    try:
+        if kind == "add":
+            bm.add_seq(a)
+            return "ok"
+        if kind == "append":
+            return bm.append_slot(a)
+        if kind == "fork":
+            bm.fork(a, b)
+            return "ok"
+        if kind == "free":
+            bm.free(a)
+            return "ok"
+    except errors as e:
+        return type(e).__name__
+    raise ValueError(kind)
+
+
+@pytest.mark.parametrize("seed", range(20))
+@pytest.mark.parametrize("nb,bs", [(7, 2), (12, 4), (30, 16)])
+def test_matches_oracle_on_random_operations(seed, nb, bs):
+    prod = pa.BlockManager(nb, bs, np.random.default_rng(seed).permutation(nb))
+    ref = oracle.RefBlockManager(nb, bs, np.random.default_rng(seed).permutation(nb))
+    live = set()
+    for op in pa_inputs.random_bm_ops(seed * 7 + nb, 400):
+        kind, a, b = op
+        # only issue operations whose preconditions hold; the errors compared are OOM
+        if kind == "add" and a in live:
+            continue
+        if kind in ("append", "free") and a not in live:
+            continue
+        if kind == "fork" and (a not in live or b in live):
+            continue
+        r_prod = _do(prod, op, (pa.OutOfBlocks,))
+        r_ref = _do(ref, op, (oracle.OutOfBlocks,))
+        if r_ref == "OutOfBlocks":
+            assert r_prod == "OutOfBlocks", op
+        else:
+            assert r_prod == r_ref, (op, r_prod, r_ref)
+            if kind in ("add",):
+                live.add(a)
+            elif kind == "fork":
+                live.add(b)
+            elif kind == "free":
+                live.discard(a)
+        assert _state(prod, nb, live, prod.refcount) == _state(ref, nb, live,
+                                                                lambda p: ref.refcount[p]), op
+        assert prod.stats() == ref.stats()
+    check_invariants(prod, nb, live)
+    for s in sorted(live):
+        prod.free(s)
+    assert sorted(prod.free_list()) == list(range(nb))
+    assert all(prod.refcount(p) == 0 for p in range(nb))
+
+
+def test_batched_step_equals_single_calls():
+    nb, bs = 64, 4
+    a = pa.BlockManager(nb, bs)
+    b = oracle.RefBlockManager(nb, bs)
+    for s in range(5):
+        a.add_seq(s), b.add_seq(s)
+        for _ in range(s * 3 + 1):
+            a.append_slot(s), b.append_slot(s)
+    a.fork(2, 7), b.fork(2, 7)
+    a.fork(4, 8), b.fork(4, 8)
+    ids = [0, 2, 7, 4, 8, 1]
+    slots, pairs = a.append_slots(ids)
+    want = [b.append_slot(s) for s in ids]
+    assert slots.tolist() == [w[0] for w in want]
+    assert [tuple(p) for p in pairs.tolist()] == [(w[1], w[2]) for w in want if w[1] >= 0]
+    tables, lens = a.build_block_tables(ids, 8)
+    for j, s in enumerate(ids):
+        t, L = b.block_table(s)
+        assert tables[j, :len(t)].tolist() == t and all(tables[j, len(t):] == -1)
+        assert lens[j] == L
+
+
+def test_out_of_blocks_leaves_state_unchanged():
+    bm = pa.BlockManager(3, 2)
+    bm.add_seq(0)
+    bm.fork(0, 1)                  # page 2 shared by sequences 0 and 1
+    bm.add_seq(2)
+    bm.add_seq(3)                  # free list now empty
+    before = (bm.free_list(), bm.block_table(0), bm.block_table(1), bm.stats())
+    with pytest.raises(pa.OutOfBlocks):
+        bm.append_slot(1)          # needs a copy of the shared page: none free
+    with pytest.raises(pa.OutOfBlocks):
+        bm.add_seq(9)
+    assert (bm.free_list(), bm.block_table(0), bm.block_table(1), bm.stats()) == before
+
+
+def test_unknown_and_duplicate_ids():
+    bm = pa.BlockManager(4, 2)
+    bm.add_seq(1)
+    with pytest.raises(pa.PaError):
+        bm.add_seq(1)
+    with pytest.raises(pa.PaError):
+        bm.append_slot(5)
+    with pytest.raises(pa.PaError):
+        bm.fork(1, 1)
+    with pytest.raises(pa.PaError):
+        bm.free(3)
+
+
+def _run_script(bm, script):
+    prefix_slots = pa_inputs.shared_prefix_prefill(bm, script)
+    _, children = pa_inputs.shared_prefix_ids(script)
+    trace = [[s.tolist() for s in prefix_slots]]
+    slots, pairs = bm.append_slots(children) if hasattr(bm, "append_slots") else (None, None)
+    if slots is None:
+        res = [bm.append_slot(c) for c in children]
+        slots = [r[0] for r in res]
+        pairs = [(r[1], r[2]) for r in res if r[1] >= 0]
+    trace.append((list(map(int, slots)), [tuple(map(int, p)) for p in pairs]))
+    # finish: every child generates its tail, then leaves in the scripted order
+    remaining = {c: int(script.tails[c]) for c in children}
+    step = 0
+    order = pa_inputs.shared_prefix_finish_order(script)
+    while remaining:
+        active = [c for c in children if c in remaining and remaining[c] > step]
+        if active:
+            res = [bm.append_slot(c) for c in active]
+            trace.append([tuple(map(int, r)) for r in res])
+        for c in order:
+            if c in remaining and remaining[c] == step:
+                bm.free(c)
+                del remaining[c]
+        step += 1
+    return trace
+
+
+def test_shared_prefix_script_matches_oracle_and_returns_every_page():
+    script = pa_inputs.shared_prefix_script(scale_parents=3, scale_children=5, prompt_len=100,
+                                            tail=(0, 40))
+    prod = pa.BlockManager(script.num_blocks, script.block_size, script.initial_free_order)
+    ref = oracle.RefBlockManager(script.num_blocks, script.block_size, script.initial_free_order)
+    t_prod = _run_script(prod, script)
+    t_ref = _run_script(ref, script)
+    assert t_prod == t_ref
+    # the step's copies: in each family all but the last child copy the partial page
+    cows = t_prod[1][1]
+    assert len(cows) == script.num_parents * (script.children_per_parent - 1)
+    assert prod.num_free() == script.num_blocks
+    assert sorted(prod.free_list()) == list(range(script.num_blocks))
+    assert all(prod.refcount(p) == 0 for p in range(script.num_blocks))
