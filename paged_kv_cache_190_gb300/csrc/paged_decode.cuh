@@ -16,10 +16,13 @@
 //     q rows into shared memory, then streams 16-token K and V tiles (one
 //     contiguous 4 KiB run each for bf16, head_dim 128) with bulk asynchronous
 //     copies (cp.async.bulk) into a ring of S stages guarded by mbarriers.
-//   * Warps 0..7 consume: stage s always belongs to warp s % 8, so each warp
-//     keeps its own online-softmax state (running max m, sum l, accumulator) in
-//     fp32 registers for every query head of the GQA group -- one K/V read
-//     serves the whole group.  At the end of an item the 8 partial states are
+//   * Warps 0..7 consume.  Unit u (16 tokens) of item i goes to warp
+//     (u + i) % 8, through that warp's own sub-ring of S / 8 stages (stage
+//     w + 8 k).  The split of an item between warps is therefore a function of
+//     the item alone, which makes the result bit-reproducible whatever CTA runs
+//     it.  Each warp keeps its own online-softmax state (running max m, sum l,
+//     accumulator) in fp32 registers for every query head of the GQA group --
+//     one K/V read serves the whole group.  At the end of an item the 8 partial states are
 //     merged through shared memory (log-sum-exp) and the item's rows are written
 //     either straight to `out` (single-chunk sequence) or as a normalised
 //     partial plus its base-2 log-sum-exp for the split-K merge kernel.
@@ -46,7 +49,7 @@ constexpr int kSmemBudget = 227 * 1024;
 constexpr unsigned kFull = 0xffffffffu;
 
 struct ItemDesc {
-  int b, h, chunk, len, gchunk, n_units, n_tokens, single;
+  int b, h, chunk, len, gchunk, n_units, n_tokens, single, rot;
 };
 
 template <bool BF16, int D, int G>
@@ -83,6 +86,7 @@ struct DecodeTraits {
   static constexpr int S_RAW = (kSmemBudget - FIXED) / (STAGE_BYTES + 2 * 8 + 4);
   static constexpr int S_CAP = S_RAW > 32 ? 32 : S_RAW;
   static constexpr int S = (S_CAP / kConsumerWarps) * kConsumerWarps;
+  static constexpr int SPW = S / kConsumerWarps;               // stages per consumer warp
   static_assert(S >= kConsumerWarps, "at least one stage per consumer warp");
 
   static constexpr int OFF_STAGES = 0;
@@ -217,7 +221,8 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
     const int total_items = p.header[1] * Hkv;
-    uint32_t unit_n = 0, item_k = 0;
+    // lane w < 8 counts the units handed to consumer warp w so far
+    uint32_t issued = 0, item_k = 0;
     bool ok = true;
     for (;;) {
       if (*abort_flag) { ok = false; break; }
@@ -255,6 +260,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
         ItemDesc d;
         d.b = w.x; d.h = h; d.chunk = w.y; d.len = w.z; d.gchunk = w.w;
         d.n_units = n_units; d.n_tokens = ntok; d.single = (w.z <= p.chunk_tokens);
+        d.rot = i % kConsumerWarps;
         desc[slot] = d;
         mbar_arrive_expect_tx(&item_full[slot], Tr::Q_BYTES);
         const char* qsrc =
@@ -262,10 +268,12 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
                       Tr::ROW_BYTES;
         bulk_g2s(qbuf + slot * Tr::Q_BYTES, qsrc, Tr::Q_BYTES, &item_full[slot]);
       }
-      for (int u = 0; u < n_units; ++u, ++unit_n) {
-        const int s = unit_n % S;
+      for (int u = 0; u < n_units; ++u) {
+        const int cw = (u + i) % kConsumerWarps;
+        const uint32_t c = __shfl_sync(kFull, issued, cw);
+        const int s = cw + kConsumerWarps * static_cast<int>(c % Tr::SPW);
         int got = 1;
-        if (lane == 0) got = mbar_wait(&empty[s], ((unit_n / S) & 1) ^ 1);
+        if (lane == 0) got = mbar_wait(&empty[s], ((c / Tr::SPW) & 1) ^ 1);
         if (!__shfl_sync(kFull, got, 0)) { ok = false; break; }
         const int tok = u * Tr::UT;
         const int pp = __shfl_sync(kFull, phys, tok / bs);
@@ -283,6 +291,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
             mbar_arrive(&full[s]);
           }
         }
+        if (lane == cw) ++issued;
       }
       if (!ok) break;
       ++item_k;
@@ -292,8 +301,13 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
       if (lane == 0) {
         report(p.device_errors, PA_DEVERR_TIMEOUT);
         *abort_flag = 1;
-        const uint32_t first = unit_n > static_cast<uint32_t>(S) ? unit_n - S : 0;
-        for (uint32_t n = first; n < unit_n; ++n) mbar_wait(&full[n % S], (n / S) & 1);
+      }
+      if (lane < kConsumerWarps) {     // copies still in flight on warp `lane`'s sub-ring
+        const uint32_t first = issued > static_cast<uint32_t>(Tr::SPW) ? issued - Tr::SPW : 0;
+        for (uint32_t c = first; c < issued; ++c)
+          mbar_wait(&full[lane + kConsumerWarps * (c % Tr::SPW)], (c / Tr::SPW) & 1);
+      }
+      if (lane == 0) {
         const uint32_t kfirst = item_k > kItemSlots ? item_k - kItemSlots : 0;
         for (uint32_t k = kfirst; k < item_k; ++k)
           mbar_wait(&item_full[k % kItemSlots], (k / kItemSlots) & 1);
@@ -312,7 +326,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
   const int g_lane = base / Tr::P;
   float* ps = ps_all + warp * Tr::UT * G;
 
-  uint32_t item_k = 0, unit_base = 0;
+  uint32_t item_k = 0, consumed = 0;   // items seen; units this warp consumed
   bool aborted = false;
   for (;;) {
     const int slot = item_k % kItemSlots;
@@ -351,18 +365,16 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
       for (int c = 0; c < Tr::CPL; ++c) acc[g][c] = 0.f;
     }
 
-    const uint32_t first =
-        unit_base + ((warp - static_cast<int>(unit_base % kConsumerWarps)) + kConsumerWarps) %
-                        kConsumerWarps;
-    for (uint32_t n = first; n < unit_base + d.n_units && !aborted; n += kConsumerWarps) {
-      const int s = n % S;
-      if (!mbar_wait(&full[s], (n / S) & 1)) {
+    // this warp's units of the item: u = u0, u0 + 8, ... (u + rot == warp mod 8)
+    const int u0 = (warp - d.rot + kConsumerWarps) % kConsumerWarps;
+    for (int u = u0; u < d.n_units && !aborted; u += kConsumerWarps, ++consumed) {
+      const int s = warp + kConsumerWarps * static_cast<int>(consumed % Tr::SPW);
+      if (!mbar_wait(&full[s], (consumed / Tr::SPW) & 1)) {
         report(p.device_errors, PA_DEVERR_TIMEOUT);
         *abort_flag = 1;
         aborted = true;
         break;
       }
-      const int u = static_cast<int>(n - unit_base);
       const int nt = min(Tr::UT, d.n_tokens - u * Tr::UT);
       if (!stage_bad[s]) {
         const char* kt = stages + s * Tr::STAGE_BYTES;
@@ -533,7 +545,6 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(merge_empty);
-    unit_base += d.n_units;
     ++item_k;
     if (aborted) break;
   }
