@@ -24,7 +24,7 @@ cudaError_t run_decode_kernel(const DecodeKernelParams& kp, int grid, int device
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
   paged_decode_kernel<BF16, D, G>
-      <<<grid, (kConsumerWarps + 1) * 32, Tr::SMEM_BYTES, stream>>>(kp);
+      <<<grid, kDecodeThreads, Tr::SMEM_BYTES, stream>>>(kp);
   return cudaGetLastError();
 }
 

@@ -45,6 +45,8 @@ namespace pa {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kItemSlots = 8;        // items the producer may run ahead
+constexpr int kUnitsAhead = 32;      // claimed-but-unissued units a CTA may hold
+constexpr int kDecodeThreads = (kConsumerWarps + 2) * 32;   // + producer + scheduler
 constexpr int kSmemBudget = 227 * 1024;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -81,8 +83,9 @@ struct DecodeTraits {
   static constexpr int PS = kConsumerWarps * UT * G * 4;
   static constexpr int QBUF = kItemSlots * Q_BYTES;
   static constexpr int DESC = kItemSlots * static_cast<int>(sizeof(ItemDesc));
-  static constexpr int FIXED = MERGE_ACC + MERGE_ML + PS + QBUF + DESC + 64 /*flags*/ +
-                               (2 * kItemSlots + 4) * 8 + 1024 /*alignment slack*/;
+  static constexpr int TBL = kItemSlots * 32 * 4;              // block-table slice per item
+  static constexpr int FIXED = MERGE_ACC + MERGE_ML + PS + QBUF + DESC + TBL + 64 /*flags*/ +
+                               (3 * kItemSlots + 4) * 8 + 1024 /*alignment slack*/;
   static constexpr int S_RAW = (kSmemBudget - FIXED) / (STAGE_BYTES + 2 * 8 + 4);
   static constexpr int S_CAP = S_RAW > 32 ? 32 : S_RAW;
   static constexpr int S = (S_CAP / kConsumerWarps) * kConsumerWarps;
@@ -95,11 +98,13 @@ struct DecodeTraits {
   static constexpr int OFF_MML = OFF_MACC + MERGE_ACC;
   static constexpr int OFF_PS = OFF_MML + MERGE_ML;
   static constexpr int OFF_DESC = OFF_PS + PS;
-  static constexpr int OFF_SFLAG = OFF_DESC + DESC;
-  static constexpr int OFF_ABORT = OFF_SFLAG + S * 4;
-  static constexpr int OFF_BARS = ((OFF_ABORT + 4 + 7) / 8) * 8;
-  // barriers: full[S], empty[S], item_full[NI], item_empty[NI], merge_full, merge_empty
-  static constexpr int NUM_BARS = 2 * S + 2 * kItemSlots + 2;
+  static constexpr int OFF_TBL = OFF_DESC + DESC;
+  static constexpr int OFF_SFLAG = OFF_TBL + TBL;
+  static constexpr int OFF_ABORT = OFF_SFLAG + S * 4;      // abort flag, issued-unit count
+  static constexpr int OFF_BARS = ((OFF_ABORT + 8 + 7) / 8) * 8;
+  // barriers: full[S], empty[S], item_full[NI], item_empty[NI], sched_full[NI],
+  // merge_full, merge_empty
+  static constexpr int NUM_BARS = 2 * S + 3 * kItemSlots + 2;
   static constexpr int SMEM_BYTES = OFF_BARS + NUM_BARS * 8;
   static_assert(SMEM_BYTES <= kSmemBudget, "shared memory over budget");
 };
@@ -175,7 +180,7 @@ __device__ __forceinline__ void load_v_cols(const char* vt, int t, int lane, flo
 }
 
 template <bool BF16, int D, int G>
-__global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
+__global__ void __launch_bounds__(kDecodeThreads, 1)
     paged_decode_kernel(const DecodeKernelParams p) {
   using Tr = DecodeTraits<BF16, D, G>;
   constexpr int S = Tr::S;
@@ -187,13 +192,16 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
   float* ps_all = reinterpret_cast<float*>(smem + Tr::OFF_PS);
   ItemDesc* desc = reinterpret_cast<ItemDesc*>(smem + Tr::OFF_DESC);
   volatile int* stage_bad = reinterpret_cast<volatile int*>(smem + Tr::OFF_SFLAG);
+  int* tbl_s = reinterpret_cast<int*>(smem + Tr::OFF_TBL);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Tr::OFF_ABORT);
+  volatile uint32_t* issued_units = reinterpret_cast<volatile uint32_t*>(smem + Tr::OFF_ABORT + 4);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tr::OFF_BARS);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* item_full = bars + 2 * S;
   uint64_t* item_empty = item_full + kItemSlots;
-  uint64_t* merge_full = item_empty + kItemSlots;
+  uint64_t* sched_full = item_empty + kItemSlots;
+  uint64_t* merge_full = sched_full + kItemSlots;
   uint64_t* merge_empty = merge_full + 1;
 
   const int warp = threadIdx.x >> 5;
@@ -207,10 +215,12 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
     for (int k = 0; k < kItemSlots; ++k) {
       mbar_init(&item_full[k], 1);
       mbar_init(&item_empty[k], kConsumerWarps);
+      mbar_init(&sched_full[k], 1);
     }
     mbar_init(merge_full, kConsumerWarps);
     mbar_init(merge_empty, kConsumerWarps);
     *abort_flag = 0;
+    *issued_units = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -218,25 +228,38 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
   const int Hkv = p.num_kv_heads;
   const int bs = p.block_size;
 
-  if (warp == kConsumerWarps) {
-    // ------------------------------------------------------------ producer
+  if (warp == kConsumerWarps + 1) {
+    // ----------------------------------------------------------- scheduler
+    // Claims work items and resolves them (atomic counter -> work entry ->
+    // block-table slice) into the shared item slots, so that the dependent
+    // global round trips never hold up the copy issue.  It keeps at most
+    // kUnitsAhead claimed-but-unissued units, which bounds the work one CTA
+    // holds back from the others when the queue runs dry.
     const int total_items = p.header[1] * Hkv;
-    // lane w < 8 counts the units handed to consumer warp w so far
-    uint32_t issued = 0, item_k = 0;
-    bool ok = true;
-    for (;;) {
-      if (*abort_flag) { ok = false; break; }
+    uint32_t claimed = 0;
+    for (uint32_t k = 0;; ++k) {
+      const int slot = k % kItemSlots;
+      for (uint32_t spin = 0; spin < kMaxPolls; ++spin) {
+        if (*abort_flag || static_cast<int>(claimed - *issued_units) <= kUnitsAhead) break;
+        __nanosleep(100);
+      }
+      int waited = 1;
+      if (lane == 0) waited = mbar_wait(&item_empty[slot], ((k / kItemSlots) & 1) ^ 1);
+      if (!__shfl_sync(kFull, waited, 0)) {
+        if (lane == 0) {
+          report(p.device_errors, PA_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      if (*abort_flag) break;
       int i = 0;
       if (lane == 0) i = atomicAdd(&p.header[0], 1);
       i = __shfl_sync(kFull, i, 0);
-      const int slot = item_k % kItemSlots;
-      int waited = 1;
-      if (lane == 0) waited = mbar_wait(&item_empty[slot], ((item_k / kItemSlots) & 1) ^ 1);
-      if (!__shfl_sync(kFull, waited, 0)) { ok = false; break; }
       if (i >= total_items) {
         if (lane == 0) {
           desc[slot].b = -1;
-          mbar_arrive(&item_full[slot]);
+          mbar_arrive(&sched_full[slot]);
         }
         break;
       }
@@ -256,25 +279,53 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
           phys = -1;
         }
       }
+      tbl_s[slot * 32 + lane] = phys;
       if (lane == 0) {
         ItemDesc d;
         d.b = w.x; d.h = h; d.chunk = w.y; d.len = w.z; d.gchunk = w.w;
         d.n_units = n_units; d.n_tokens = ntok; d.single = (w.z <= p.chunk_tokens);
         d.rot = i % kConsumerWarps;
         desc[slot] = d;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sched_full[slot]);
+      claimed += static_cast<uint32_t>(n_units);
+    }
+    return;
+  }
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------------------ producer
+    // lane w < 8 counts the units handed to consumer warp w so far
+    uint32_t issued = 0, issued_total = 0, q_issued = 0;
+    bool ok = true;
+    for (uint32_t k = 0;; ++k) {
+      if (*abort_flag) { ok = false; break; }
+      const int slot = k % kItemSlots;
+      int got = 1;
+      if (lane == 0) got = mbar_wait(&sched_full[slot], (k / kItemSlots) & 1);
+      if (!__shfl_sync(kFull, got, 0)) { ok = false; break; }
+      const ItemDesc d = desc[slot];
+      if (d.b < 0) {
+        if (lane == 0) mbar_arrive(&item_full[slot]);   // hand the end on to the consumers
+        break;
+      }
+      const int phys = tbl_s[slot * 32 + lane];
+      if (lane == 0) {
         mbar_arrive_expect_tx(&item_full[slot], Tr::Q_BYTES);
         const char* qsrc =
-            p.q + (static_cast<int64_t>(w.x) * p.num_q_heads + static_cast<int64_t>(h) * G) *
+            p.q + (static_cast<int64_t>(d.b) * p.num_q_heads + static_cast<int64_t>(d.h) * G) *
                       Tr::ROW_BYTES;
         bulk_g2s(qbuf + slot * Tr::Q_BYTES, qsrc, Tr::Q_BYTES, &item_full[slot]);
       }
-      for (int u = 0; u < n_units; ++u) {
-        const int cw = (u + i) % kConsumerWarps;
+      ++q_issued;
+      for (int u = 0; u < d.n_units; ++u) {
+        const int cw = (u + d.rot) % kConsumerWarps;
         const uint32_t c = __shfl_sync(kFull, issued, cw);
         const int s = cw + kConsumerWarps * static_cast<int>(c % Tr::SPW);
-        int got = 1;
-        if (lane == 0) got = mbar_wait(&empty[s], ((c / Tr::SPW) & 1) ^ 1);
-        if (!__shfl_sync(kFull, got, 0)) { ok = false; break; }
+        int got_s = 1;
+        if (lane == 0) got_s = mbar_wait(&empty[s], ((c / Tr::SPW) & 1) ^ 1);
+        if (!__shfl_sync(kFull, got_s, 0)) { ok = false; break; }
         const int tok = u * Tr::UT;
         const int pp = __shfl_sync(kFull, phys, tok / bs);
         if (lane == 0) {
@@ -282,7 +333,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
             stage_bad[s] = 0;
             mbar_arrive_expect_tx(&full[s], Tr::STAGE_BYTES);
             const int64_t off =
-                ((static_cast<int64_t>(pp) * Hkv + h) * bs + (tok % bs)) * Tr::ROW_BYTES;
+                ((static_cast<int64_t>(pp) * Hkv + d.h) * bs + (tok % bs)) * Tr::ROW_BYTES;
             char* dst = stages + s * Tr::STAGE_BYTES;
             bulk_g2s(dst, p.k_cache + off, Tr::TILE_BYTES, &full[s]);
             bulk_g2s(dst + Tr::TILE_BYTES, p.v_cache + off, Tr::TILE_BYTES, &full[s]);
@@ -290,14 +341,14 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
             stage_bad[s] = 1;
             mbar_arrive(&full[s]);
           }
+          *issued_units = ++issued_total;
         }
         if (lane == cw) ++issued;
       }
       if (!ok) break;
-      ++item_k;
     }
     if (!ok) {
-      // Give up: tell the consumers, then wait (bounded) for our own copies.
+      // Give up: tell the others, then wait (bounded) for our own copies.
       if (lane == 0) {
         report(p.device_errors, PA_DEVERR_TIMEOUT);
         *abort_flag = 1;
@@ -308,8 +359,8 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
           mbar_wait(&full[lane + kConsumerWarps * (c % Tr::SPW)], (c / Tr::SPW) & 1);
       }
       if (lane == 0) {
-        const uint32_t kfirst = item_k > kItemSlots ? item_k - kItemSlots : 0;
-        for (uint32_t k = kfirst; k < item_k; ++k)
+        const uint32_t kfirst = q_issued > kItemSlots ? q_issued - kItemSlots : 0;
+        for (uint32_t k = kfirst; k < q_issued; ++k)
           mbar_wait(&item_full[k % kItemSlots], (k / kItemSlots) & 1);
       }
     }
@@ -444,7 +495,7 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
           for (int c = 0; c < Tr::CPL; ++c) acc[g][c] *= alpha[g];
         __syncwarp();
         // ---- values: each lane owns CPL columns of every head
-        for (int t = 0; t < nt; ++t) {
+        auto pv_row = [&](int t) {
           float pv[G];
           if constexpr (G % 4 == 0) {
 #pragma unroll
@@ -464,6 +515,12 @@ __global__ void __launch_bounds__((kConsumerWarps + 1) * 32, 1)
           for (int g = 0; g < G; ++g)
 #pragma unroll
             for (int c = 0; c < Tr::CPL; ++c) acc[g][c] = fmaf(pv[g], vv[c], acc[g][c]);
+        };
+        if (nt == Tr::UT) {
+#pragma unroll
+          for (int t = 0; t < Tr::UT; ++t) pv_row(t);
+        } else {
+          for (int t = 0; t < nt; ++t) pv_row(t);
         }
       }
       __syncwarp();
