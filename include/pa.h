@@ -135,6 +135,36 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
               int chunk_tokens, void* workspace, size_t workspace_bytes,
               int32_t* device_errors, void* stream);
 
+/*
+ * Allocation-free decode.  The pages this library is built from have no
+ * counterpart: this entry point exists for callers that cannot allocate device
+ * memory (code embedded in a runtime that owns every device allocation, a
+ * process with a fixed memory pool, a decode loop that must not call cudaMalloc
+ * between steps), so they cannot provide pa_decode's workspace.
+ *
+ * Same arguments and result as pa_decode, minus the workspace: the scratch is a
+ * static device array of PA_NOALLOC_SCRATCH_BYTES (96 MiB) inside the library,
+ * allocated on every GPU that loads the library's device code and held until
+ * the process exits.  The call allocates nothing (no cudaMalloc, no allocating
+ * library routine).  Problems whose workspace (pa_decode_workspace_size with
+ * the same arguments) exceeds PA_NOALLOC_SCRATCH_BYTES are rejected with
+ * PA_ERR_WORKSPACE before anything is enqueued.
+ *
+ * The first call on a device looks the array's device address up
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  All calls share the one array: calls
+ * that may overlap on the GPU (different streams, or host threads enqueueing
+ * concurrently) race on it and must be serialised by the caller.  Each call
+ * resets what must start at zero, so the previous call's contents do no harm.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES ((size_t)96 << 20)
+int pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* context_lens, float scale,
+                      int num_kv_heads, int num_seqs, int num_q_heads, int head_dim,
+                      int block_size, int num_blocks, int max_blocks_per_seq,
+                      int max_context_len, pa_dtype dtype, int chunk_tokens,
+                      int32_t* device_errors, void* stream);
+
 /* Synchronise `stream`, copy *device_errors to *host_flags, and zero it on the
  * device when `clear` is non-zero.  This is the one call that waits. */
 int pa_read_device_errors(int32_t* device_errors, int32_t* host_flags, int clear, void* stream);

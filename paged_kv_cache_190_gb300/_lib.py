@@ -18,7 +18,7 @@ PA_DEVERR_BAD_BLOCK, PA_DEVERR_BAD_LENGTH, PA_DEVERR_BAD_SLOT, PA_DEVERR_TIMEOUT
 # Every function include/pa.h declares (checked by the tests).
 EXPORTED_SYMBOLS = [
     "pa_get_error_string", "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_chunk_tokens",
-    "pa_decode_workspace_size", "pa_decode", "pa_read_device_errors",
+    "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc", "pa_read_device_errors",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq", "pa_bm_append_slot", "pa_bm_fork",
     "pa_bm_free", "pa_bm_block_table", "pa_bm_refcount", "pa_bm_num_free", "pa_bm_free_list",
     "pa_bm_stats", "pa_bm_append_slots", "pa_bm_build_block_tables",
@@ -40,6 +40,8 @@ _SIGNATURES = {
     "pa_decode_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32]),
     "pa_decode": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _i32, _i32, _i32, _i32,
                          _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
+    "pa_decode_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _i32, _i32, _i32,
+                                 _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
     "pa_read_device_errors": (_i32, [_vp, _pi32, _i32, _vp]),
     "pa_bm_create": (_i32, [_i32, _i32, _pi32, ctypes.POINTER(_vp)]),
     "pa_bm_destroy": (None, [_vp]),
@@ -201,6 +203,35 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_k
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(device_errors),
         _stream(stream, q.device))
     _check(rc, "pa_decode")
+    return out
+
+
+PA_NOALLOC_SCRATCH_BYTES = 96 << 20
+
+
+def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
+                      max_context_len, chunk_tokens=0, device_errors=None, stream=None):
+    """pa_decode without a workspace, for callers that cannot allocate device
+    memory: the library's static scratch array (PA_NOALLOC_SCRATCH_BYTES) is used
+    instead.  Calls share that array, so calls that could overlap on the GPU must
+    be serialised; the first call on a device looks the array up and should come
+    before any stream capture."""
+    import torch
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("block_tables", block_tables), ("context_lens", context_lens)):
+        _need_cuda_contig(n, t)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    if int(Hkv) != int(num_kv_heads):
+        raise ValueError("num_kv_heads does not match the cache shape")
+    rc = library().pa_decode_noalloc(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        float(scale), int(num_kv_heads), int(B), int(Hq), int(D), int(bs), int(NB),
+        int(block_tables.shape[1]), int(max_context_len), _dtype_code(q), int(chunk_tokens),
+        _ptr(device_errors), _stream(stream, q.device))
+    _check(rc, "pa_decode_noalloc")
     return out
 
 
