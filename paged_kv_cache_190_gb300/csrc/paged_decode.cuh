@@ -310,7 +310,6 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         if (lane == 0) mbar_arrive(&item_full[slot]);   // hand the end on to the consumers
         break;
       }
-      const int phys = tbl_s[slot * 32 + lane];
       if (lane == 0) {
         mbar_arrive_expect_tx(&item_full[slot], Tr::Q_BYTES);
         const char* qsrc =
@@ -319,31 +318,42 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         bulk_g2s(qbuf + slot * Tr::Q_BYTES, qsrc, Tr::Q_BYTES, &item_full[slot]);
       }
       ++q_issued;
-      for (int u = 0; u < d.n_units; ++u) {
-        const int cw = (u + d.rot) % kConsumerWarps;
-        const uint32_t c = __shfl_sync(kFull, issued, cw);
-        const int s = cw + kConsumerWarps * static_cast<int>(c % Tr::SPW);
-        int got_s = 1;
-        if (lane == 0) got_s = mbar_wait(&empty[s], ((c / Tr::SPW) & 1) ^ 1);
-        if (!__shfl_sync(kFull, got_s, 0)) { ok = false; break; }
-        const int tok = u * Tr::UT;
-        const int pp = __shfl_sync(kFull, phys, tok / bs);
-        if (lane == 0) {
-          if (pp >= 0) {
-            stage_bad[s] = 0;
-            mbar_arrive_expect_tx(&full[s], Tr::STAGE_BYTES);
-            const int64_t off =
-                ((static_cast<int64_t>(pp) * Hkv + d.h) * bs + (tok % bs)) * Tr::ROW_BYTES;
-            char* dst = stages + s * Tr::STAGE_BYTES;
-            bulk_g2s(dst, p.k_cache + off, Tr::TILE_BYTES, &full[s]);
-            bulk_g2s(dst + Tr::TILE_BYTES, p.v_cache + off, Tr::TILE_BYTES, &full[s]);
-          } else {
-            stage_bad[s] = 1;
-            mbar_arrive(&full[s]);
+      // Hand the item's units to the consumers, eight at a time: lane w < 8 feeds
+      // consumer warp w's sub-ring (its units are u = u0, u0 + 8, ...), so eight
+      // copies are in issue at once -- one issuing thread cannot keep HBM busy.
+      const int tbl_lane = tbl_s[slot * 32 + lane];   // block id of page `lane` of the chunk
+      const int u0 = (lane - d.rot + kConsumerWarps) % kConsumerWarps;
+      const int rounds = (d.n_units + kConsumerWarps - 1) / kConsumerWarps;
+      for (int rnd = 0; rnd < rounds; ++rnd) {
+        const int u = u0 + rnd * kConsumerWarps;
+        const bool mine = lane < kConsumerWarps && u < d.n_units;
+        const int tok = mine ? u * Tr::UT : 0;
+        const int pp = __shfl_sync(kFull, tbl_lane, tok / bs);
+        int got = 1;
+        if (mine) {
+          const int s = lane + kConsumerWarps * static_cast<int>(issued % Tr::SPW);
+          got = mbar_wait(&empty[s], ((issued / Tr::SPW) & 1) ^ 1);
+          if (got) {
+            if (pp >= 0) {
+              stage_bad[s] = 0;
+              mbar_arrive_expect_tx(&full[s], Tr::STAGE_BYTES);
+              const int64_t off =
+                  ((static_cast<int64_t>(pp) * Hkv + d.h) * bs + (tok % bs)) * Tr::ROW_BYTES;
+              char* dst = stages + s * Tr::STAGE_BYTES;
+              bulk_g2s(dst, p.k_cache + off, Tr::TILE_BYTES, &full[s]);
+              bulk_g2s(dst + Tr::TILE_BYTES, p.v_cache + off, Tr::TILE_BYTES, &full[s]);
+            } else {
+              stage_bad[s] = 1;
+              mbar_arrive(&full[s]);
+            }
+            ++issued;
           }
-          *issued_units = ++issued_total;
         }
-        if (lane == cw) ++issued;
+        if (!__all_sync(kFull, got)) { ok = false; break; }
+        if (lane == 0) {
+          issued_total += static_cast<uint32_t>(min(kConsumerWarps, d.n_units - rnd * kConsumerWarps));
+          *issued_units = issued_total;
+        }
       }
       if (!ok) break;
     }
