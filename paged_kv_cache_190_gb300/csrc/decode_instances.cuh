@@ -19,12 +19,12 @@ cudaError_t run_decode_kernel(const DecodeKernelParams& kp, int grid, int device
   if (!(configured.load(std::memory_order_acquire) & bit)) {
     const cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<BF16, D, G>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               Tr::SMEM_BYTES);
+                                               Tr::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
   paged_decode_kernel<BF16, D, G>
-      <<<grid, kDecodeThreads, Tr::SMEM_BYTES, stream>>>(kp);
+      <<<grid, kDecodeThreads, Tr::SMEM_ALLOC, stream>>>(kp);
   return cudaGetLastError();
 }
 

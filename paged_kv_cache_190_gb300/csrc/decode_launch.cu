@@ -1,8 +1,12 @@
 // Orchestration of one pa_decode call: plan kernel -> persistent decode kernel
 // -> split-K merge kernel, all on the caller's stream.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <climits>
 #include <cstdint>
+#include <cstring>
 
 #include "decode_instances.cuh"
 #include "pa_device.cuh"
@@ -75,64 +79,193 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(
   }
 }
 
-__device__ __forceinline__ float block_reduce_128(float v, bool is_max, float* red) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float y = __shfl_xor_sync(0xffffffffu, v, o);
-    v = is_max ? fmaxf(v, y) : v + y;
-  }
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-  __syncthreads();
-  float r = red[0];
-#pragma unroll
-  for (int w = 1; w < 4; ++w) r = is_max ? fmaxf(r, red[w]) : r + red[w];
-  __syncthreads();
-  return r;
-}
+constexpr int kMergeWarps = 8;
 
 // Split-K merge (log-sum-exp): for sequence b, query head i with n >= 2 chunks,
 //   M = max_c lse_c,  w_c = 2^(lse_c - M),  out = sum_c w_c o_c / sum_c w_c,
 // where o_c is chunk c's normalised output and lse_c its base-2 log-sum-exp.
-template <bool BF16>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const int32_t* __restrict__ chunk_base,
-                                                           const float* __restrict__ part_lse,
-                                                           const float* __restrict__ part_out,
-                                                           void* __restrict__ out,
-                                                           int num_q_heads, int head_dim) {
-  __shared__ float red[4];
-  const int64_t row = blockIdx.x;                 // b * num_q_heads + i
+// One warp per (b, i) row; each lane owns head_dim / 32 columns; the chunk loop
+// has independent loads (the weights need only M), so several are in flight.
+template <bool BF16, int CPL>
+__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(
+    const int32_t* __restrict__ chunk_base, const float* __restrict__ part_lse,
+    const float* __restrict__ part_out, void* __restrict__ out, int num_q_heads, int64_t rows) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  constexpr int D = CPL * 32;
   const int b = static_cast<int>(row / num_q_heads);
   const int i = static_cast<int>(row - static_cast<int64_t>(b) * num_q_heads);
   const int c0 = chunk_base[b];
   const int n = chunk_base[b + 1] - c0;
   if (n < 2) return;
+  const float* lse = part_lse + static_cast<int64_t>(c0) * num_q_heads + i;   // stride num_q_heads
+  float M = -INFINITY;
+  for (int c = lane; c < n; c += 32) M = fmaxf(M, lse[static_cast<int64_t>(c) * num_q_heads]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float* po = part_out + (static_cast<int64_t>(c0) * num_q_heads + i) * D + lane * CPL;
+  const int64_t pstride = static_cast<int64_t>(num_q_heads) * D;
+  float S = 0.f, acc[CPL];
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) acc[k] = 0.f;
+#pragma unroll 8
+  for (int c = 0; c < n; ++c) {
+    const float w = fast_exp2(lse[static_cast<int64_t>(c) * num_q_heads] - M);
+    S += w;
+    if constexpr (CPL == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(po + c * pstride);
+      acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+      acc[2] = fmaf(w, v.z, acc[2]); acc[3] = fmaf(w, v.w, acc[3]);
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(po + c * pstride);
+      acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+    }
+  }
+  const float inv = 1.f / S;
+  const int64_t o = row * D + lane * CPL;
+  if constexpr (BF16) {
+    uint32_t w0 = f32_to_bf16_bits(acc[0] * inv) | (f32_to_bf16_bits(acc[1] * inv) << 16);
+    if constexpr (CPL == 4) {
+      uint32_t w1 = f32_to_bf16_bits(acc[2] * inv) | (f32_to_bf16_bits(acc[3] * inv) << 16);
+      *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(out) + o) = make_uint2(w0, w1);
+    } else {
+      *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(out) + o) = w0;
+    }
+  } else {
+    float* dst = reinterpret_cast<float*>(out) + o;
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) dst[k] = acc[k] * inv;
+  }
+}
+
+// The same merge for long chunk lists: one block per (b, i) row, its 8 warps
+// take chunks c = warp, warp + 8, ... and combine their sums in shared memory.
+template <bool BF16, int CPL>
+__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_wide_kernel(
+    const int32_t* __restrict__ chunk_base, const float* __restrict__ part_lse,
+    const float* __restrict__ part_out, void* __restrict__ out, int num_q_heads) {
+  constexpr int D = CPL * 32;
+  __shared__ float red[kMergeWarps];
+  __shared__ float sacc[kMergeWarps][D];
+  __shared__ float ssum[kMergeWarps];
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int64_t row = blockIdx.x;
+  const int b = static_cast<int>(row / num_q_heads);
+  const int i = static_cast<int>(row - static_cast<int64_t>(b) * num_q_heads);
+  const int c0 = chunk_base[b];
+  const int n = chunk_base[b + 1] - c0;
+  if (n < 2) return;                      // uniform over the block
+  const float* lse = part_lse + static_cast<int64_t>(c0) * num_q_heads + i;
   float M = -INFINITY;
   for (int c = threadIdx.x; c < n; c += blockDim.x)
-    M = fmaxf(M, part_lse[static_cast<int64_t>(c0 + c) * num_q_heads + i]);
-  M = block_reduce_128(M, true, red);
-  float S = 0.f;
-  for (int c = threadIdx.x; c < n; c += blockDim.x)
-    S += fast_exp2(part_lse[static_cast<int64_t>(c0 + c) * num_q_heads + i] - M);
-  S = block_reduce_128(S, false, red);
-  const float inv = 1.f / S;
-  for (int d = threadIdx.x; d < head_dim; d += blockDim.x) {
-    float a = 0.f;
-#pragma unroll 8
-    for (int c = 0; c < n; ++c) {
-      const int64_t prow = static_cast<int64_t>(c0 + c) * num_q_heads + i;
-      a = fmaf(fast_exp2(part_lse[prow] - M), part_out[prow * head_dim + d], a);
-    }
-    a *= inv;
-    const int64_t o = row * head_dim + d;
-    if constexpr (BF16) {
-      reinterpret_cast<uint16_t*>(out)[o] = static_cast<uint16_t>(f32_to_bf16_bits(a));
+    M = fmaxf(M, lse[static_cast<int64_t>(c) * num_q_heads]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  if (lane == 0) red[warp] = M;
+  __syncthreads();
+  M = red[0];
+#pragma unroll
+  for (int w = 1; w < kMergeWarps; ++w) M = fmaxf(M, red[w]);
+  const float* po = part_out + (static_cast<int64_t>(c0) * num_q_heads + i) * D + lane * CPL;
+  const int64_t pstride = static_cast<int64_t>(num_q_heads) * D;
+  float S = 0.f, acc[CPL];
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) acc[k] = 0.f;
+#pragma unroll 4
+  for (int c = warp; c < n; c += kMergeWarps) {
+    const float w = fast_exp2(lse[static_cast<int64_t>(c) * num_q_heads] - M);
+    S += w;
+    if constexpr (CPL == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(po + c * pstride);
+      acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+      acc[2] = fmaf(w, v.z, acc[2]); acc[3] = fmaf(w, v.w, acc[3]);
     } else {
-      reinterpret_cast<float*>(out)[o] = a;
+      const float2 v = *reinterpret_cast<const float2*>(po + c * pstride);
+      acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
     }
+  }
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) sacc[warp][lane * CPL + k] = acc[k];
+  if (lane == 0) ssum[warp] = S;
+  __syncthreads();
+  if (warp != 0) return;
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kMergeWarps; ++w) tot += ssum[w];
+  const float inv = 1.f / tot;
+  float r[CPL];
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) {
+    float a = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMergeWarps; ++w) a += sacc[w][lane * CPL + k];
+    r[k] = a * inv;
+  }
+  const int64_t o = row * D + lane * CPL;
+  if constexpr (BF16) {
+    const uint32_t w0 = f32_to_bf16_bits(r[0]) | (f32_to_bf16_bits(r[1]) << 16);
+    if constexpr (CPL == 4) {
+      const uint32_t w1 = f32_to_bf16_bits(r[2]) | (f32_to_bf16_bits(r[3]) << 16);
+      *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(out) + o) = make_uint2(w0, w1);
+    } else {
+      *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(out) + o) = w0;
+    }
+  } else {
+    float* dst = reinterpret_cast<float*>(out) + o;
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) dst[k] = r[k];
+  }
+}
+
+template <bool BF16, int CPL>
+void launch_merge(const DecodeArgs& a, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
+  const int64_t max_chunks_per_seq = (static_cast<int64_t>(a.max_context_len) + a.chunk_tokens - 1) /
+                                     a.chunk_tokens;
+  if (max_chunks_per_seq >= 32) {
+    decode_merge_wide_kernel<BF16, CPL><<<static_cast<unsigned>(rows), kMergeWarps * 32, 0, stream>>>(
+        a.ws.chunk_base, a.ws.part_lse, a.ws.part_out, a.out, a.num_q_heads);
+  } else {
+    const unsigned blocks = static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps);
+    decode_merge_kernel<BF16, CPL><<<blocks, kMergeWarps * 32, 0, stream>>>(
+        a.ws.chunk_base, a.ws.part_lse, a.ws.part_out, a.out, a.num_q_heads, rows);
   }
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }();
+  return fn;
+}
+
+// 2-D bf16 view [rows][head_dim] of a K or V pool (rows = blocks * kv heads *
+// block size), boxes of 16 rows x 64 columns (128 bytes) with 128-byte swizzle.
+cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int head_dim, int64_t rows) {
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  if (rows <= 0 || rows > INT_MAX) return cudaErrorInvalidValue;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+  const cuuint32_t box[2] = {64, 16};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims,
+                            strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
 
 }  // namespace
 
@@ -168,6 +301,14 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.ws.max_chunks == 0) return cudaSuccess;  // every length is zero
 
   DecodeKernelParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  const int group = a.num_q_heads / a.num_kv_heads;
+  if (decode_uses_tensor_cores(a.bf16 != 0, group)) {
+    const int64_t rows = static_cast<int64_t>(a.num_blocks) * a.num_kv_heads * a.block_size;
+    e = make_pool_map(&kp.tmap_k, a.k_cache, a.head_dim, rows);
+    if (e == cudaSuccess) e = make_pool_map(&kp.tmap_v, a.v_cache, a.head_dim, rows);
+    if (e != cudaSuccess) return e;
+  }
   kp.out = a.out;
   kp.q = static_cast<const char*>(a.q);
   kp.k_cache = static_cast<const char*>(a.k_cache);
@@ -190,18 +331,14 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   int device = 0;
   e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
-  const int group = a.num_q_heads / a.num_kv_heads;
   e = a.bf16 ? run_decode_bf16(a.head_dim, group, kp, grid, device, stream)
              : run_decode_f32(a.head_dim, group, kp, grid, device, stream);
   if (e != cudaSuccess) return e;
   if (a.max_context_len > a.chunk_tokens) {
-    const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
-    if (a.bf16)
-      decode_merge_kernel<true><<<static_cast<unsigned>(rows), 128, 0, stream>>>(
-          a.ws.chunk_base, a.ws.part_lse, a.ws.part_out, a.out, a.num_q_heads, a.head_dim);
-    else
-      decode_merge_kernel<false><<<static_cast<unsigned>(rows), 128, 0, stream>>>(
-          a.ws.chunk_base, a.ws.part_lse, a.ws.part_out, a.out, a.num_q_heads, a.head_dim);
+    if (a.bf16 && a.head_dim == 128) launch_merge<true, 4>(a, stream);
+    else if (a.bf16) launch_merge<true, 2>(a, stream);
+    else if (a.head_dim == 128) launch_merge<false, 4>(a, stream);
+    else launch_merge<false, 2>(a, stream);
     e = cudaGetLastError();
   }
   return e;

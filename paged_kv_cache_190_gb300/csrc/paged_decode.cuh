@@ -11,32 +11,43 @@
 //   * Work item = (sequence, kv head, chunk of `chunk_tokens` tokens).  A tiny
 //     plan kernel lists the (sequence, chunk) pairs; items are handed out by an
 //     atomic counter, so lognormal lengths balance across SMs.
-//   * One CTA per SM, persistent.  Warp 8 is the producer: per item it loads the
-//     chunk's block-table slice with one coalesced read, copies the GQA group's
-//     q rows into shared memory, then streams 16-token K and V tiles (one
-//     contiguous 4 KiB run each for bf16, head_dim 128) with bulk asynchronous
-//     copies (cp.async.bulk) into a ring of S stages guarded by mbarriers.
+//   * One CTA per SM, persistent, ten warps.  Warp 9 schedules: it claims items
+//     and resolves them (work entry, block-table slice) into shared item slots.
+//     Warp 8 produces: it copies the GQA group's q rows into shared memory and
+//     streams 16-token K and V tiles into a ring of stages guarded by
+//     mbarriers -- eight lanes issuing at once, lane w feeding consumer warp w,
+//     because a single issuing thread cannot keep HBM busy.  Tiles move with
+//     cp.async.bulk (one contiguous run per tile) or, for the tensor-core
+//     consumer, with cp.async.bulk.tensor through a 2-D tensor map with 128-byte
+//     swizzle so that ldmatrix reads them without bank conflicts.
 //   * Warps 0..7 consume.  Unit u (16 tokens) of item i goes to warp
 //     (u + i) % 8, through that warp's own sub-ring of S / 8 stages (stage
 //     w + 8 k).  The split of an item between warps is therefore a function of
 //     the item alone, which makes the result bit-reproducible whatever CTA runs
-//     it.  Each warp keeps its own online-softmax state (running max m, sum l,
+//     it.  Each warp keeps an online-softmax state (running max m, sum l,
 //     accumulator) in fp32 registers for every query head of the GQA group --
-//     one K/V read serves the whole group.  At the end of an item the 8 partial states are
-//     merged through shared memory (log-sum-exp) and the item's rows are written
-//     either straight to `out` (single-chunk sequence) or as a normalised
-//     partial plus its base-2 log-sum-exp for the split-K merge kernel.
-//   * QK: 8 lanes per token, 4 tokens per pass, 16-byte shared loads that are
-//     contiguous within each quarter warp (no bank conflicts); the 8-lane dot
-//     products are reduced by a butterfly that leaves each lane with whole sums.
-//   * PV: each lane owns head_dim / 32 output columns for every head of the group.
+//     one K/V read serves the whole group.  Two consumers:
+//       - CUDA cores (fp32 inputs, and bf16 with one query head per kv head):
+//         QK with 8 lanes per token and a butterfly reduction, PV with each
+//         lane owning head_dim / 32 output columns;
+//       - tensor cores (bf16, 2..8 query heads per kv head): mma.sync
+//         m16n8k16 with the group's q rows as the A operand (rows past the
+//         group are zero), K through ldmatrix, P re-packed from the score
+//         fragments as the next A operand, V through ldmatrix.trans.
+//   * At the end of an item the 8 partial states are merged through shared
+//     memory (log-sum-exp) and the item's rows are written either straight to
+//     `out` (single-chunk sequence) or as a normalised partial plus its base-2
+//     log-sum-exp for the split-K merge kernel.
 //   * Every wait is bounded; on expiry the kernel reports PA_DEVERR_TIMEOUT,
 //     drains its own copies in flight and returns.
 #pragma once
 
+#include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "pa_device.cuh"
 #include "pa_internal.h"
@@ -54,11 +65,19 @@ struct ItemDesc {
   int b, h, chunk, len, gchunk, n_units, n_tokens, single, rot;
 };
 
+// Tensor-core consumer: bf16 with a group of 2..8 query heads per kv head.
+constexpr bool decode_uses_tensor_cores(bool bf16, int group) { return bf16 && group >= 2; }
+
 template <bool BF16, int D, int G>
 struct DecodeTraits {
+  static constexpr int D_ = D;
+  static constexpr int G_ = G;
+  static constexpr bool TC = decode_uses_tensor_cores(BF16, G);
   static constexpr int ELT = BF16 ? 2 : 4;
   static constexpr int ROW_BYTES = D * ELT;
   static constexpr int UT = ROW_BYTES >= 512 ? 8 : 16;          // tokens per stage
+  static constexpr int BOXES = ROW_BYTES / 128;                // 128-byte tensor-map boxes per row
+  static constexpr int BOX_BYTES = UT * 128;
   static constexpr int TILE_BYTES = UT * ROW_BYTES;            // K (or V) of one stage
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
   static constexpr int Q_BYTES = G * ROW_BYTES;
@@ -89,6 +108,7 @@ struct DecodeTraits {
   static constexpr int S_RAW = (kSmemBudget - FIXED) / (STAGE_BYTES + 2 * 8 + 4);
   static constexpr int S_CAP = S_RAW > 32 ? 32 : S_RAW;
   static constexpr int S = (S_CAP / kConsumerWarps) * kConsumerWarps;
+  static_assert(!TC || (UT == 16 && STAGE_BYTES % 1024 == 0), "swizzled stages need 1 KiB alignment");
   static constexpr int SPW = S / kConsumerWarps;               // stages per consumer warp
   static_assert(S >= kConsumerWarps, "at least one stage per consumer warp");
 
@@ -106,10 +126,13 @@ struct DecodeTraits {
   // merge_full, merge_empty
   static constexpr int NUM_BARS = 2 * S + 3 * kItemSlots + 2;
   static constexpr int SMEM_BYTES = OFF_BARS + NUM_BARS * 8;
-  static_assert(SMEM_BYTES <= kSmemBudget, "shared memory over budget");
+  static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;        // room to align the base to 1 KiB
+  static_assert(SMEM_ALLOC <= kSmemBudget, "shared memory over budget");
 };
 
 struct DecodeKernelParams {
+  CUtensorMap tmap_k;               // 2-D views [rows = NB*Hkv*bs][head_dim] of the pools
+  CUtensorMap tmap_v;               // (tensor-core consumer only)
   void* out;
   const char* q;
   const char* k_cache;
@@ -179,12 +202,340 @@ __device__ __forceinline__ void load_v_cols(const char* vt, int t, int lane, flo
   }
 }
 
+// ------------------------------------------------------------------ tensor-core helpers
+
+// 2-D tensor-map copy of one box (rows y.., columns x..) into shared memory.
+__device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Byte offset of (row, 16-byte chunk) inside a tile stored as 128-byte-wide boxes
+// with the tensor map's 128-byte swizzle: chunk index XOR (row mod 8).
+template <typename Tr>
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return static_cast<uint32_t>((chunk >> 3) * Tr::BOX_BYTES + row * 128 +
+                               (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D = A * B + D for one m16n8k16 bf16 tile with fp32 accumulation.  A rows 8..15
+// (a1, a3) are zero here: the group has at most 8 query heads.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// ------------------------------------------------------------------ consumers
+// Both consumers hold one warp's online-softmax state for the item in flight:
+//   begin(q rows)  -> reset the state, load the group's q
+//   unit(K, V, nt) -> fold 16 tokens (nt valid) into the state
+//   store(...)     -> hand (m, l, unnormalised accumulator) to the merge
+
+// CUDA-core consumer.  QK: 8 lanes per token (16-byte chunks contiguous within a
+// quarter warp), 4 tokens per pass, butterfly reduction; PV: each lane owns
+// head_dim / 32 output columns of every head.
+template <typename Tr>
+struct CoreConsumer {
+  static constexpr int G = Tr::G_, D = Tr::D_;
+  float qf[G][Tr::EPL];
+  float m[G], acc[G][Tr::CPL];
+  float lsum;                       // this lane's share of l[g_lane]
+  int lane, j4, r, base, g_lane;
+  float* ps;                        // this warp's probabilities [UT][G]
+
+  __device__ __forceinline__ void init(int lane_, float* ps_) {
+    lane = lane_;
+    j4 = lane >> 3;
+    r = lane & 7;
+    // after the butterfly this lane holds the sums of indices base .. base+RC-1
+    // (index = head * P + pass) -- all for one head, g_lane
+    base = ((r >> 2) & 1) * (Tr::N / 2) + (Tr::N >= 4 ? ((r >> 1) & 1) * (Tr::N / 4) : 0) +
+           (Tr::N >= 8 ? (r & 1) * (Tr::N / 8) : 0);
+    g_lane = base / Tr::P;
+    ps = ps_;
+  }
+
+  __device__ __forceinline__ void begin(const char* qs, float scale_log2) {
+    // q scaled so that logits come out in base 2
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int c = 0; c < Tr::NCH; ++c) {
+        const uint4 raw =
+            *reinterpret_cast<const uint4*>(qs + g * Tr::ROW_BYTES + (r + 8 * c) * 16);
+        unpack_chunk<Tr>(raw, &qf[g][c * Tr::CE]);
+#pragma unroll
+        for (int e = 0; e < Tr::CE; ++e) qf[g][c * Tr::CE + e] *= scale_log2;
+      }
+    lsum = 0.f;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m[g] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < Tr::CPL; ++c) acc[g][c] = 0.f;
+    }
+  }
+
+  __device__ __forceinline__ void unit(const char* kt, const char* vt, int nt, float) {
+    // ---- scores: 8 lanes per token, 4 tokens per pass
+    float part[Tr::N];
+#pragma unroll
+    for (int pi = 0; pi < Tr::P; ++pi) {
+      const int t = 4 * pi + j4;
+      float kf[Tr::EPL];
+#pragma unroll
+      for (int c = 0; c < Tr::NCH; ++c) {
+        const uint4 raw =
+            *reinterpret_cast<const uint4*>(kt + t * Tr::ROW_BYTES + (r + 8 * c) * 16);
+        unpack_chunk<Tr>(raw, &kf[c * Tr::CE]);
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float dot = 0.f;
+#pragma unroll
+        for (int e = 0; e < Tr::EPL; ++e) dot = fmaf(qf[g][e], kf[e], dot);
+        part[g * Tr::P + pi] = dot;
+      }
+    }
+    butterfly_level<Tr::N>(part, lane, 4);
+    butterfly_level<(Tr::N >= 4 ? Tr::N / 2 : 1)>(part, lane, 2);
+    butterfly_level<(Tr::N >= 8 ? Tr::N / 4 : 1)>(part, lane, 1);
+    // part[e], e < RC: score of head g_lane, token 4 * ((base % P) + e) + j4
+    float umax = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < Tr::RC; ++e) {
+      const int t = 4 * ((base % Tr::P) + e) + j4;
+      if (t >= nt) part[e] = -INFINITY;
+      umax = fmaxf(umax, part[e]);
+    }
+    // max over the lanes that hold the same head
+#pragma unroll
+    for (int mask = 1; mask < 8 / G; mask <<= 1)
+      umax = fmaxf(umax, __shfl_xor_sync(kFull, umax, mask));
+    umax = fmaxf(umax, __shfl_xor_sync(kFull, umax, 8));
+    umax = fmaxf(umax, __shfl_xor_sync(kFull, umax, 16));
+    float alpha[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float mu = __shfl_sync(kFull, umax, g * (8 / G));
+      const float mn = fmaxf(m[g], mu);
+      alpha[g] = fast_exp2(m[g] - mn);
+      m[g] = mn;
+    }
+    float m_lane = m[0];
+    float a_lane = alpha[0];
+#pragma unroll
+    for (int g = 1; g < G; ++g)
+      if (g_lane == g) { m_lane = m[g]; a_lane = alpha[g]; }
+    float psum = 0.f;
+#pragma unroll
+    for (int e = 0; e < Tr::RC; ++e) {
+      const int t = 4 * ((base % Tr::P) + e) + j4;
+      const float pr = fast_exp2(part[e] - m_lane);
+      psum += pr;
+      ps[t * G + g_lane] = pr;       // duplicate lanes (G == 1) store equal values
+    }
+    lsum = lsum * a_lane + psum;
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int c = 0; c < Tr::CPL; ++c) acc[g][c] *= alpha[g];
+    __syncwarp();
+    // ---- values: each lane owns CPL columns of every head
+    auto pv_row = [&](int t) {
+      float pv[G];
+      if constexpr (G % 4 == 0) {
+#pragma unroll
+        for (int g4 = 0; g4 < G; g4 += 4) {
+          const float4 w4 = *reinterpret_cast<const float4*>(ps + t * G + g4);
+          pv[g4] = w4.x; pv[g4 + 1] = w4.y; pv[g4 + 2] = w4.z; pv[g4 + 3] = w4.w;
+        }
+      } else if constexpr (G == 2) {
+        const float2 w2 = *reinterpret_cast<const float2*>(ps + t * 2);
+        pv[0] = w2.x; pv[1] = w2.y;
+      } else {
+        pv[0] = ps[t];
+      }
+      float vv[Tr::CPL];
+      load_v_cols<Tr>(vt, t, lane, vv);
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int c = 0; c < Tr::CPL; ++c) acc[g][c] = fmaf(pv[g], vv[c], acc[g][c]);
+    };
+    if (nt == Tr::UT) {
+#pragma unroll
+      for (int t = 0; t < Tr::UT; ++t) pv_row(t);
+    } else {
+      for (int t = 0; t < nt; ++t) pv_row(t);
+    }
+  }
+
+  // macc_w: this warp's [G][D] accumulator slot; mml_w: its [G][2] (m, l) slot.
+  __device__ __forceinline__ void store(float* macc_w, float* mml_w) {
+    // whole l for the lane's head: sum over the lanes sharing it, leaving out
+    // the low lane bits that only hold duplicates
+#pragma unroll
+    for (int mask = Tr::DUP_MASK_END; mask < 8 / G; mask <<= 1)
+      lsum += __shfl_xor_sync(kFull, lsum, mask);
+    lsum += __shfl_xor_sync(kFull, lsum, 8);
+    lsum += __shfl_xor_sync(kFull, lsum, 16);
+    if (j4 == 0 && (r % (8 / G)) == 0) {
+      float mlane = m[0];
+#pragma unroll
+      for (int g = 1; g < G; ++g)
+        if (g_lane == g) mlane = m[g];
+      mml_w[g_lane * 2 + 0] = mlane;
+      mml_w[g_lane * 2 + 1] = lsum;
+    }
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float* dst = macc_w + g * D + lane * Tr::CPL;
+      if constexpr (Tr::CPL == 4) {
+        *reinterpret_cast<float4*>(dst) = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+      } else {
+        *reinterpret_cast<float2*>(dst) = make_float2(acc[g][0], acc[g][1]);
+      }
+    }
+  }
+};
+
+// Tensor-core consumer (bf16, G in 2..8).  m16n8k16 tiles: rows = query heads
+// of the group (rows >= G carry zero q and are never stored), columns = 8
+// tokens (scores) or 8 head_dim columns (output).  Lane t holds row t / 4 of
+// every fragment; the four lanes of a row own its columns 2 (t % 4) + {0, 1}.
+template <typename Tr>
+struct TensorConsumer {
+  static constexpr int G = Tr::G_, D = Tr::D_;
+  static constexpr int KS = D / 16;     // k-steps over head_dim (scores)
+  static constexpr int NT = D / 8;      // output n-tiles
+  uint32_t qa[KS][2];                   // A fragments of q (row t/4, k lo / k hi)
+  float o[NT][4];                       // output fragments; [.][2..3] are rows >= 8
+  float m, l;                           // this row's running max (base 2) and sum share
+  int lane;
+
+  __device__ __forceinline__ void init(int lane_, float*) { lane = lane_; }
+
+  __device__ __forceinline__ void begin(const char* qs, float) {
+    const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qa[ks][0] = 0u;
+      qa[ks][1] = 0u;
+      if (g < G) {
+        qa[ks][0] = *reinterpret_cast<const uint32_t*>(qs + g * Tr::ROW_BYTES + (16 * ks + 2 * c) * 2);
+        qa[ks][1] =
+            *reinterpret_cast<const uint32_t*>(qs + g * Tr::ROW_BYTES + (16 * ks + 8 + 2 * c) * 2);
+      }
+    }
+    m = -INFINITY;
+    l = 0.f;
+#pragma unroll
+    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  }
+
+  __device__ __forceinline__ void unit(const char* kt, const char* vt, int nt, float scale_log2) {
+    const uint32_t kb = smem_addr(kt), vb = smem_addr(vt);
+    const int mi = lane >> 3, r8 = lane & 7, c = lane & 3;
+    // ---- scores S[g][token] = q_g . K_token, two 8-token n-tiles
+    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+    const int krow = (mi >> 1) * 8 + r8;          // ldmatrix row this lane addresses
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(kb + swz<Tr>(krow, 2 * ks + (mi & 1)), b0, b1, b2, b3);
+      mma_bf16(s0, qa[ks][0], qa[ks][1], b0, b1);
+      mma_bf16(s1, qa[ks][0], qa[ks][1], b2, b3);
+    }
+    // this lane's scores: tokens 2c, 2c+1 (n-tile 0) and 8+2c, 9+2c (n-tile 1)
+    float sv[4] = {s0[0], s0[1], s1[0], s1[1]};
+    const int tk[4] = {2 * c, 2 * c + 1, 8 + 2 * c, 9 + 2 * c};
+    float mx = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      sv[e] = tk[e] < nt ? sv[e] * scale_log2 : -INFINITY;
+      mx = fmaxf(mx, sv[e]);
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+    const float mn = fmaxf(m, mx);
+    const float alpha = fast_exp2(m - mn);
+    m = mn;
+    float pr[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pr[e] = fast_exp2(sv[e] - mn);
+    l = l * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+    // P as the A operand of the value product (k = the 16 tokens)
+    const uint32_t pa_lo = pack_bf16x2(pr[0], pr[1]);
+    const uint32_t pa_hi = pack_bf16x2(pr[2], pr[3]);
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      o[n][0] *= alpha;
+      o[n][1] *= alpha;
+    }
+    // ---- O[g][d] += sum_token P[g][token] V[token][d], two n-tiles per ldmatrix
+    const int vrow = (mi & 1) * 8 + r8;
+#pragma unroll
+    for (int np = 0; np < NT / 2; ++np) {
+      uint32_t v0, v1, v2, v3;
+      ldsm_x4_trans(vb + swz<Tr>(vrow, 2 * np + (mi >> 1)), v0, v1, v2, v3);
+      mma_bf16(o[2 * np], pa_lo, pa_hi, v0, v1);
+      mma_bf16(o[2 * np + 1], pa_lo, pa_hi, v2, v3);
+    }
+  }
+
+  __device__ __forceinline__ void store(float* macc_w, float* mml_w) {
+    float lt = l + __shfl_xor_sync(kFull, l, 1);
+    lt += __shfl_xor_sync(kFull, lt, 2);
+    const int g = lane >> 2, c = lane & 3;
+    if (g < G) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+        *reinterpret_cast<float2*>(macc_w + g * D + n * 8 + 2 * c) = make_float2(o[n][0], o[n][1]);
+      if (c == 0) {
+        mml_w[g * 2 + 0] = m;
+        mml_w[g * 2 + 1] = lt;
+      }
+    }
+  }
+};
+
 template <bool BF16, int D, int G>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
-    paged_decode_kernel(const DecodeKernelParams p) {
+    paged_decode_kernel(const __grid_constant__ DecodeKernelParams p) {
   using Tr = DecodeTraits<BF16, D, G>;
+  using Consumer = typename std::conditional<Tr::TC, TensorConsumer<Tr>, CoreConsumer<Tr>>::type;
   constexpr int S = Tr::S;
-  extern __shared__ __align__(1024) unsigned char smem[];
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // swizzled tensor-map copies need 1 KiB-aligned stages
+  unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   char* stages = reinterpret_cast<char*>(smem + Tr::OFF_STAGES);
   char* qbuf = reinterpret_cast<char*>(smem + Tr::OFF_QBUF);
   float* macc = reinterpret_cast<float*>(smem + Tr::OFF_MACC);
@@ -337,11 +688,21 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             if (pp >= 0) {
               stage_bad[s] = 0;
               mbar_arrive_expect_tx(&full[s], Tr::STAGE_BYTES);
-              const int64_t off =
-                  ((static_cast<int64_t>(pp) * Hkv + d.h) * bs + (tok % bs)) * Tr::ROW_BYTES;
               char* dst = stages + s * Tr::STAGE_BYTES;
-              bulk_g2s(dst, p.k_cache + off, Tr::TILE_BYTES, &full[s]);
-              bulk_g2s(dst + Tr::TILE_BYTES, p.v_cache + off, Tr::TILE_BYTES, &full[s]);
+              const int64_t row = (static_cast<int64_t>(pp) * Hkv + d.h) * bs + (tok % bs);
+              if constexpr (Tr::TC) {
+#pragma unroll
+                for (int bx = 0; bx < Tr::BOXES; ++bx) {
+                  tma_load_2d(dst + bx * Tr::BOX_BYTES, &p.tmap_k, bx * 64, static_cast<int>(row),
+                              &full[s]);
+                  tma_load_2d(dst + Tr::TILE_BYTES + bx * Tr::BOX_BYTES, &p.tmap_v, bx * 64,
+                              static_cast<int>(row), &full[s]);
+                }
+              } else {
+                const int64_t off = row * Tr::ROW_BYTES;
+                bulk_g2s(dst, p.k_cache + off, Tr::TILE_BYTES, &full[s]);
+                bulk_g2s(dst + Tr::TILE_BYTES, p.v_cache + off, Tr::TILE_BYTES, &full[s]);
+              }
             } else {
               stage_bad[s] = 1;
               mbar_arrive(&full[s]);
@@ -378,14 +739,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   }
 
   // -------------------------------------------------------------- consumers
-  const int j4 = lane >> 3;        // token within a pass
-  const int r = lane & 7;          // position within the 8-lane group
-  // After the butterfly this lane holds the sums of indices base .. base+RC-1
-  // (index = head * P + pass) -- all for one head, g_lane.
-  const int base = ((r >> 2) & 1) * (Tr::N / 2) + (Tr::N >= 4 ? ((r >> 1) & 1) * (Tr::N / 4) : 0) +
-                   (Tr::N >= 8 ? (r & 1) * (Tr::N / 8) : 0);
-  const int g_lane = base / Tr::P;
-  float* ps = ps_all + warp * Tr::UT * G;
+  Consumer cs;
+  cs.init(lane, ps_all + warp * Tr::UT * G);
 
   uint32_t item_k = 0, consumed = 0;   // items seen; units this warp consumed
   bool aborted = false;
@@ -398,33 +753,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     const ItemDesc d = desc[slot];
     if (d.b < 0 || *abort_flag) break;
-
-    // q rows of the group, scaled so that logits come out in base 2
-    float qf[G][Tr::EPL];
-    {
-      const char* qs = qbuf + slot * Tr::Q_BYTES;
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int c = 0; c < Tr::NCH; ++c) {
-          const uint4 raw =
-              *reinterpret_cast<const uint4*>(qs + g * Tr::ROW_BYTES + (r + 8 * c) * 16);
-          unpack_chunk<Tr>(raw, &qf[g][c * Tr::CE]);
-#pragma unroll
-          for (int e = 0; e < Tr::CE; ++e) qf[g][c * Tr::CE + e] *= p.scale_log2;
-        }
-    }
+    cs.begin(qbuf + slot * Tr::Q_BYTES, p.scale_log2);
     __syncwarp();
     if (lane == 0) mbar_arrive(&item_empty[slot]);
-
-    float m[G], acc[G][Tr::CPL];
-    float lsum = 0.f;                                  // this lane's share of l[g_lane]
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      m[g] = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < Tr::CPL; ++c) acc[g][c] = 0.f;
-    }
 
     // this warp's units of the item: u = u0, u0 + 8, ... (u + rot == warp mod 8)
     const int u0 = (warp - d.rot + kConsumerWarps) % kConsumerWarps;
@@ -438,99 +769,25 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       }
       const int nt = min(Tr::UT, d.n_tokens - u * Tr::UT);
       if (!stage_bad[s]) {
-        const char* kt = stages + s * Tr::STAGE_BYTES;
-        const char* vt = kt + Tr::TILE_BYTES;
-        // ---- scores: 8 lanes per token, 4 tokens per pass
-        float part[Tr::N];
-#pragma unroll
-        for (int ps_i = 0; ps_i < Tr::P; ++ps_i) {
-          const int t = 4 * ps_i + j4;
-          float kf[Tr::EPL];
-#pragma unroll
-          for (int c = 0; c < Tr::NCH; ++c) {
-            const uint4 raw =
-                *reinterpret_cast<const uint4*>(kt + t * Tr::ROW_BYTES + (r + 8 * c) * 16);
-            unpack_chunk<Tr>(raw, &kf[c * Tr::CE]);
-          }
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            float dot = 0.f;
-#pragma unroll
-            for (int e = 0; e < Tr::EPL; ++e) dot = fmaf(qf[g][e], kf[e], dot);
-            part[g * Tr::P + ps_i] = dot;
-          }
-        }
-        butterfly_level<Tr::N>(part, lane, 4);
-        butterfly_level<(Tr::N >= 4 ? Tr::N / 2 : 1)>(part, lane, 2);
-        butterfly_level<(Tr::N >= 8 ? Tr::N / 4 : 1)>(part, lane, 1);
-        // part[e], e < RC: score of head g_lane, token 4 * ((base % P) + e) + j4
-        float umax = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < Tr::RC; ++e) {
-          const int t = 4 * ((base % Tr::P) + e) + j4;
-          if (t >= nt) part[e] = -INFINITY;
-          umax = fmaxf(umax, part[e]);
-        }
-        // max over the lanes that hold the same head
-#pragma unroll
-        for (int mask = 1; mask < 8 / G; mask <<= 1)
-          umax = fmaxf(umax, __shfl_xor_sync(kFull, umax, mask));
-        umax = fmaxf(umax, __shfl_xor_sync(kFull, umax, 8));
-        umax = fmaxf(umax, __shfl_xor_sync(kFull, umax, 16));
-        float alpha[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float mu = __shfl_sync(kFull, umax, g * (8 / G));
-          const float mn = fmaxf(m[g], mu);
-          alpha[g] = fast_exp2(m[g] - mn);
-          m[g] = mn;
-        }
-        float m_lane = m[0];
-        float a_lane = alpha[0];
-#pragma unroll
-        for (int g = 1; g < G; ++g)
-          if (g_lane == g) { m_lane = m[g]; a_lane = alpha[g]; }
-        float psum = 0.f;
-#pragma unroll
-        for (int e = 0; e < Tr::RC; ++e) {
-          const int t = 4 * ((base % Tr::P) + e) + j4;
-          const float pr = fast_exp2(part[e] - m_lane);
-          psum += pr;
-          ps[t * G + g_lane] = pr;       // duplicate lanes (G == 1) store equal values
-        }
-        lsum = lsum * a_lane + psum;
-#pragma unroll
-        for (int g = 0; g < G; ++g)
-#pragma unroll
-          for (int c = 0; c < Tr::CPL; ++c) acc[g][c] *= alpha[g];
-        __syncwarp();
-        // ---- values: each lane owns CPL columns of every head
-        auto pv_row = [&](int t) {
-          float pv[G];
-          if constexpr (G % 4 == 0) {
-#pragma unroll
-            for (int g4 = 0; g4 < G; g4 += 4) {
-              const float4 w4 = *reinterpret_cast<const float4*>(ps + t * G + g4);
-              pv[g4] = w4.x; pv[g4 + 1] = w4.y; pv[g4 + 2] = w4.z; pv[g4 + 3] = w4.w;
+        char* kt = stages + s * Tr::STAGE_BYTES;
+        char* vt = kt + Tr::TILE_BYTES;
+        if constexpr (Tr::TC) {
+          // The tensor cores multiply every one of the 16 rows, so value rows past
+          // the sequence (stale or never-written slots) must not hold NaN or Inf.
+          if (nt < Tr::UT) {
+            for (int i = lane; i < (Tr::UT - nt) * Tr::BOXES * 8; i += 32) {
+              const int row = nt + i / (Tr::BOXES * 8);
+              const int rest = i % (Tr::BOXES * 8);
+              *reinterpret_cast<uint4*>(vt + (rest >> 3) * Tr::BOX_BYTES + row * 128 +
+                                        (rest & 7) * 16) = make_uint4(0, 0, 0, 0);
             }
-          } else if constexpr (G == 2) {
-            const float2 w2 = *reinterpret_cast<const float2*>(ps + t * 2);
-            pv[0] = w2.x; pv[1] = w2.y;
-          } else {
-            pv[0] = ps[t];
+            __syncwarp();
           }
-          float vv[Tr::CPL];
-          load_v_cols<Tr>(vt, t, lane, vv);
-#pragma unroll
-          for (int g = 0; g < G; ++g)
-#pragma unroll
-            for (int c = 0; c < Tr::CPL; ++c) acc[g][c] = fmaf(pv[g], vv[c], acc[g][c]);
-        };
-        if (nt == Tr::UT) {
-#pragma unroll
-          for (int t = 0; t < Tr::UT; ++t) pv_row(t);
-        } else {
-          for (int t = 0; t < nt; ++t) pv_row(t);
+        }
+        cs.unit(kt, vt, nt, p.scale_log2);
+        if constexpr (Tr::TC) {
+          // order this warp's generic-proxy writes before the next tensor copy here
+          if (nt < Tr::UT) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         }
       }
       __syncwarp();
@@ -538,35 +795,12 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
 
     // ---- merge the 8 warps' states for this item
-    // whole l for the lane's head: sum over the lanes sharing it, leaving out
-    // the low lane bits that only hold duplicates
-#pragma unroll
-    for (int mask = Tr::DUP_MASK_END; mask < 8 / G; mask <<= 1)
-      lsum += __shfl_xor_sync(kFull, lsum, mask);
-    lsum += __shfl_xor_sync(kFull, lsum, 8);
-    lsum += __shfl_xor_sync(kFull, lsum, 16);
     if (item_k > 0 && !mbar_wait(merge_empty, (item_k - 1) & 1)) {
       report(p.device_errors, PA_DEVERR_TIMEOUT);
       *abort_flag = 1;
       aborted = true;
     }
-    if (j4 == 0 && (r % (8 / G)) == 0) {
-      float mlane = m[0];
-#pragma unroll
-      for (int g = 1; g < G; ++g)
-        if (g_lane == g) mlane = m[g];
-      mml[(warp * G + g_lane) * 2 + 0] = mlane;
-      mml[(warp * G + g_lane) * 2 + 1] = lsum;
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float* dst = macc + (warp * G + g) * D + lane * Tr::CPL;
-      if constexpr (Tr::CPL == 4) {
-        *reinterpret_cast<float4*>(dst) = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
-      } else {
-        *reinterpret_cast<float2*>(dst) = make_float2(acc[g][0], acc[g][1]);
-      }
-    }
+    cs.store(macc + warp * G * D, mml + warp * G * 2);
     __syncwarp();
     if (lane == 0) mbar_arrive(merge_full);
     if (!mbar_wait(merge_full, item_k & 1)) {
