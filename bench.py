@@ -167,8 +167,9 @@ def dist_env():
 class GpuStep:
     """Device-resident inputs of one workload and the step that runs on them."""
 
-    def __init__(self, name: str, device, torch, pa):
+    def __init__(self, name: str, device, torch, pa, chunk_tokens: int = 0):
         self.torch, self.pa, self.device = torch, pa, device
+        self.chunk_tokens = chunk_tokens
         self.name = name
         if name == "shared_prefix_bf16":
             self._init_shared_prefix()
@@ -237,12 +238,13 @@ class GpuStep:
         torch, pa = self.torch, self.pa
         c = self.case
         self.ws_bytes = pa.pa_decode_workspace_size(c.num_seqs, c.num_q_heads, c.num_kv_heads,
-                                                    c.head_dim, c.block_size, self.max_len)
+                                                    c.head_dim, c.block_size, self.max_len,
+                                                    self.chunk_tokens)
         self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8,
                                      device=self.device)
         self.errs = torch.zeros(1, dtype=torch.int32, device=self.device)
-        self.chunk = pa.pa_decode_chunk_tokens(c.num_seqs, c.num_kv_heads, c.block_size,
-                                               self.max_len)
+        self.chunk = self.chunk_tokens or pa.pa_decode_chunk_tokens(
+            c.num_seqs, c.num_kv_heads, c.block_size, self.max_len)
         # kernels of ours per step: [copy_blocks] + reshape + plan + decode [+ merge]
         self.launches_per_step = (1 if self.pairs is not None else 0) + 3 + (
             1 if self.max_len > self.chunk else 0)
@@ -257,7 +259,7 @@ class GpuStep:
     def decode(self):
         self.pa.pa_decode(self.out, self.q, self.k_cache, self.v_cache, self.tables, self.lens,
                           self.scale, self.Hkv, self.max_len, workspace=self.workspace,
-                          device_errors=self.errs)
+                          chunk_tokens=self.chunk_tokens, device_errors=self.errs)
 
     def step(self):
         self.write()
@@ -273,7 +275,7 @@ def run_gpu(args, world, rank, local):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
-    ws = GpuStep(args.workload, device, torch, pa)
+    ws = GpuStep(args.workload, device, torch, pa, args.chunk_tokens)
     stream = torch.cuda.current_stream(device)
 
     def barrier():
@@ -509,6 +511,8 @@ def main(argv=None):
                     choices=list(pa_inputs.WORKLOADS) + ["shared_prefix_bf16"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--chunk-tokens", type=int, default=0,
+                    help="split size for pa_decode (0: the library's automatic choice)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")

@@ -99,7 +99,7 @@ struct DecodeTraits {
   // shared memory carve-up (bytes)
   static constexpr int MERGE_ACC = kConsumerWarps * G * D * 4;
   static constexpr int MERGE_ML = kConsumerWarps * G * 2 * 4;
-  static constexpr int PS = kConsumerWarps * UT * G * 4;
+  static constexpr int PS = TC ? 0 : kConsumerWarps * UT * G * 4;   // CUDA-core probabilities
   static constexpr int QBUF = kItemSlots * Q_BYTES;
   static constexpr int DESC = kItemSlots * static_cast<int>(sizeof(ItemDesc));
   static constexpr int TBL = kItemSlots * 32 * 4;              // block-table slice per item
@@ -120,11 +120,11 @@ struct DecodeTraits {
   static constexpr int OFF_DESC = OFF_PS + PS;
   static constexpr int OFF_TBL = OFF_DESC + DESC;
   static constexpr int OFF_SFLAG = OFF_TBL + TBL;
-  static constexpr int OFF_ABORT = OFF_SFLAG + S * 4;      // abort flag, issued-unit count
-  static constexpr int OFF_BARS = ((OFF_ABORT + 8 + 7) / 8) * 8;
-  // barriers: full[S], empty[S], item_full[NI], item_empty[NI], sched_full[NI],
-  // merge_full, merge_empty
-  static constexpr int NUM_BARS = 2 * S + 3 * kItemSlots + 2;
+  // abort flag, merge arrival counter, units issued per producer lane [8]
+  static constexpr int OFF_ABORT = OFF_SFLAG + S * 4;
+  static constexpr int OFF_BARS = ((OFF_ABORT + 8 + 4 * kConsumerWarps + 7) / 8) * 8;
+  // barriers: full[S], empty[S], item_full[NI], item_empty[NI], sched_full[NI], merge_free
+  static constexpr int NUM_BARS = 2 * S + 3 * kItemSlots + 1;
   static constexpr int SMEM_BYTES = OFF_BARS + NUM_BARS * 8;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;        // room to align the base to 1 KiB
   static_assert(SMEM_ALLOC <= kSmemBudget, "shared memory over budget");
@@ -247,6 +247,16 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a2
       : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
 }
 
+// D = A * B + D for one m16n8k16 bf16 tile, all four A registers given.
+__device__ __forceinline__ void mma_bf16_full(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                              uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -303,7 +313,9 @@ struct CoreConsumer {
     }
   }
 
-  __device__ __forceinline__ void unit(const char* kt, const char* vt, int nt, float) {
+  template <typename Release>
+  __device__ __forceinline__ void unit(const char* kt, const char* vt, int nt, float,
+                                       Release release) {
     // ---- scores: 8 lanes per token, 4 tokens per pass
     float part[Tr::N];
 #pragma unroll
@@ -396,6 +408,7 @@ struct CoreConsumer {
     } else {
       for (int t = 0; t < nt; ++t) pv_row(t);
     }
+    release();
   }
 
   // macc_w: this warp's [G][D] accumulator slot; mml_w: its [G][2] (m, l) slot.
@@ -427,18 +440,23 @@ struct CoreConsumer {
   }
 };
 
-// Tensor-core consumer (bf16, G in 2..8).  m16n8k16 tiles: rows = query heads
-// of the group (rows >= G carry zero q and are never stored), columns = 8
-// tokens (scores) or 8 head_dim columns (output).  Lane t holds row t / 4 of
-// every fragment; the four lanes of a row own its columns 2 (t % 4) + {0, 1}.
+// Tensor-core consumer (bf16, G in 2..8), mma.sync m16n8k16 with fp32 accumulation.
+//   Scores  S = Q K^T : rows = the group's query heads (rows >= G carry zero q),
+//                       columns = 8 tokens per n-tile, k = head_dim.
+//   Values  O^T = V^T P^T : rows = 16 head_dim columns per m-tile, columns = the
+//                       heads (8 per tile; heads >= G are never stored), k = tokens.
+// The score fragment of lane t (head t / 4, tokens 2 (t % 4) + {0, 1, 8, 9}) is
+// exactly the B fragment P^T needs, so P never leaves registers.  The whole
+// stage is read into registers first (K via ldmatrix, V^T via ldmatrix.trans)
+// and handed back to the producer before the arithmetic starts.
 template <typename Tr>
 struct TensorConsumer {
   static constexpr int G = Tr::G_, D = Tr::D_;
   static constexpr int KS = D / 16;     // k-steps over head_dim (scores)
-  static constexpr int NT = D / 8;      // output n-tiles
+  static constexpr int MT = D / 16;     // m-tiles of O^T (16 head_dim columns each)
   uint32_t qa[KS][2];                   // A fragments of q (row t/4, k lo / k hi)
-  float o[NT][4];                       // output fragments; [.][2..3] are rows >= 8
-  float m, l;                           // this row's running max (base 2) and sum share
+  float o[MT][4];                       // O^T fragments: d = 16 mt + t/4 (+8), heads 2(t%4) + {0,1}
+  float m, l;                           // head t/4: running max (base 2) and this lane's sum share
   int lane;
 
   __device__ __forceinline__ void init(int lane_, float*) { lane = lane_; }
@@ -458,23 +476,32 @@ struct TensorConsumer {
     m = -INFINITY;
     l = 0.f;
 #pragma unroll
-    for (int n = 0; n < NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   }
 
-  __device__ __forceinline__ void unit(const char* kt, const char* vt, int nt, float scale_log2) {
+  template <typename Release>
+  __device__ __forceinline__ void unit(const char* kt, const char* vt, int nt, float scale_log2,
+                                       Release release) {
     const uint32_t kb = smem_addr(kt), vb = smem_addr(vt);
     const int mi = lane >> 3, r8 = lane & 7, c = lane & 3;
-    // ---- scores S[g][token] = q_g . K_token, two 8-token n-tiles
+    const int frow = (mi >> 1) * 8 + r8;          // token row this lane addresses
+    uint32_t kf[KS][4], vf[MT][4];
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+      ldsm_x4(kb + swz<Tr>(frow, 2 * ks + (mi & 1)), kf[ks][0], kf[ks][1], kf[ks][2], kf[ks][3]);
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt)
+      ldsm_x4_trans(vb + swz<Tr>(frow, 2 * mt + (mi & 1)), vf[mt][0], vf[mt][1], vf[mt][2],
+                    vf[mt][3]);
+    release();                                    // the stage's bytes are all in registers
+    // ---- scores, two 8-token n-tiles
     float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
-    const int krow = (mi >> 1) * 8 + r8;          // ldmatrix row this lane addresses
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      uint32_t b0, b1, b2, b3;
-      ldsm_x4(kb + swz<Tr>(krow, 2 * ks + (mi & 1)), b0, b1, b2, b3);
-      mma_bf16(s0, qa[ks][0], qa[ks][1], b0, b1);
-      mma_bf16(s1, qa[ks][0], qa[ks][1], b2, b3);
+      mma_bf16(s0, qa[ks][0], qa[ks][1], kf[ks][0], kf[ks][1]);
+      mma_bf16(s1, qa[ks][0], qa[ks][1], kf[ks][2], kf[ks][3]);
     }
-    // this lane's scores: tokens 2c, 2c+1 (n-tile 0) and 8+2c, 9+2c (n-tile 1)
+    // this lane's scores: head t/4, tokens 2c, 2c+1 (n-tile 0) and 8+2c, 9+2c (n-tile 1)
     float sv[4] = {s0[0], s0[1], s1[0], s1[1]};
     const int tk[4] = {2 * c, 2 * c + 1, 8 + 2 * c, 9 + 2 * c};
     float mx = -INFINITY;
@@ -492,22 +519,19 @@ struct TensorConsumer {
 #pragma unroll
     for (int e = 0; e < 4; ++e) pr[e] = fast_exp2(sv[e] - mn);
     l = l * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
-    // P as the A operand of the value product (k = the 16 tokens)
-    const uint32_t pa_lo = pack_bf16x2(pr[0], pr[1]);
-    const uint32_t pa_hi = pack_bf16x2(pr[2], pr[3]);
+    // P^T as the B operand: k = tokens 2c, 2c+1 (b0) and 8+2c, 9+2c (b1), n = head t/4
+    const uint32_t pb0 = pack_bf16x2(pr[0], pr[1]);
+    const uint32_t pb1 = pack_bf16x2(pr[2], pr[3]);
+    // rescale: this lane's O^T columns are heads 2c and 2c+1 (alpha lives in lanes 4h..4h+3)
+    const float a_even = __shfl_sync(kFull, alpha, 8 * c);
+    const float a_odd = __shfl_sync(kFull, alpha, 8 * c + 4);
 #pragma unroll
-    for (int n = 0; n < NT; ++n) {
-      o[n][0] *= alpha;
-      o[n][1] *= alpha;
-    }
-    // ---- O[g][d] += sum_token P[g][token] V[token][d], two n-tiles per ldmatrix
-    const int vrow = (mi & 1) * 8 + r8;
-#pragma unroll
-    for (int np = 0; np < NT / 2; ++np) {
-      uint32_t v0, v1, v2, v3;
-      ldsm_x4_trans(vb + swz<Tr>(vrow, 2 * np + (mi >> 1)), v0, v1, v2, v3);
-      mma_bf16(o[2 * np], pa_lo, pa_hi, v0, v1);
-      mma_bf16(o[2 * np + 1], pa_lo, pa_hi, v2, v3);
+    for (int mt = 0; mt < MT; ++mt) {
+      o[mt][0] *= a_even;
+      o[mt][1] *= a_odd;
+      o[mt][2] *= a_even;
+      o[mt][3] *= a_odd;
+      mma_bf16_full(o[mt], vf[mt][0], vf[mt][1], vf[mt][2], vf[mt][3], pb0, pb1);
     }
   }
 
@@ -515,13 +539,21 @@ struct TensorConsumer {
     float lt = l + __shfl_xor_sync(kFull, l, 1);
     lt += __shfl_xor_sync(kFull, lt, 2);
     const int g = lane >> 2, c = lane & 3;
-    if (g < G) {
+    if (g < G && c == 0) {
+      mml_w[g * 2 + 0] = m;
+      mml_w[g * 2 + 1] = lt;
+    }
+    const int h0 = 2 * c, h1 = 2 * c + 1;
 #pragma unroll
-      for (int n = 0; n < NT; ++n)
-        *reinterpret_cast<float2*>(macc_w + g * D + n * 8 + 2 * c) = make_float2(o[n][0], o[n][1]);
-      if (c == 0) {
-        mml_w[g * 2 + 0] = m;
-        mml_w[g * 2 + 1] = lt;
+    for (int mt = 0; mt < MT; ++mt) {
+      const int d0 = 16 * mt + g, d1 = d0 + 8;
+      if (h0 < G) {
+        macc_w[h0 * D + d0] = o[mt][0];
+        macc_w[h0 * D + d1] = o[mt][2];
+      }
+      if (h1 < G) {
+        macc_w[h1 * D + d0] = o[mt][1];
+        macc_w[h1 * D + d1] = o[mt][3];
       }
     }
   }
@@ -545,15 +577,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   volatile int* stage_bad = reinterpret_cast<volatile int*>(smem + Tr::OFF_SFLAG);
   int* tbl_s = reinterpret_cast<int*>(smem + Tr::OFF_TBL);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Tr::OFF_ABORT);
-  volatile uint32_t* issued_units = reinterpret_cast<volatile uint32_t*>(smem + Tr::OFF_ABORT + 4);
+  int* merge_cnt = reinterpret_cast<int*>(smem + Tr::OFF_ABORT + 4);
+  volatile uint32_t* issued_by = reinterpret_cast<volatile uint32_t*>(smem + Tr::OFF_ABORT + 8);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tr::OFF_BARS);
   uint64_t* full = bars;
   uint64_t* empty = bars + S;
   uint64_t* item_full = bars + 2 * S;
   uint64_t* item_empty = item_full + kItemSlots;
   uint64_t* sched_full = item_empty + kItemSlots;
-  uint64_t* merge_full = sched_full + kItemSlots;
-  uint64_t* merge_empty = merge_full + 1;
+  uint64_t* merge_free = sched_full + kItemSlots;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -565,13 +597,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     for (int k = 0; k < kItemSlots; ++k) {
       mbar_init(&item_full[k], 1);
-      mbar_init(&item_empty[k], kConsumerWarps);
+      // released by the 8 producer lanes (done issuing) and the 8 consumer warps (q read)
+      mbar_init(&item_empty[k], 2 * kConsumerWarps);
       mbar_init(&sched_full[k], 1);
     }
-    mbar_init(merge_full, kConsumerWarps);
-    mbar_init(merge_empty, kConsumerWarps);
+    mbar_init(merge_free, 1);
     *abort_flag = 0;
-    *issued_units = 0;
+    *merge_cnt = 0;
+    for (int w = 0; w < kConsumerWarps; ++w) issued_by[w] = 0;
     fence_mbar_init();
   }
   __syncthreads();
@@ -582,16 +615,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   if (warp == kConsumerWarps + 1) {
     // ----------------------------------------------------------- scheduler
     // Claims work items and resolves them (atomic counter -> work entry ->
-    // block-table slice) into the shared item slots, so that the dependent
-    // global round trips never hold up the copy issue.  It keeps at most
-    // kUnitsAhead claimed-but-unissued units, which bounds the work one CTA
-    // holds back from the others when the queue runs dry.
+    // block-table slice) into the shared item slots, then starts the copy of
+    // the item's q rows.  The dependent global round trips never hold up the
+    // K/V copies.  It keeps at most kUnitsAhead claimed-but-unissued units,
+    // which bounds the work one CTA holds back when the queue runs dry.
     const int total_items = p.header[1] * Hkv;
     uint32_t claimed = 0;
     for (uint32_t k = 0;; ++k) {
       const int slot = k % kItemSlots;
       for (uint32_t spin = 0; spin < kMaxPolls; ++spin) {
-        if (*abort_flag || static_cast<int>(claimed - *issued_units) <= kUnitsAhead) break;
+        uint32_t issued = 0;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) issued += issued_by[w];
+        if (*abort_flag || static_cast<int>(claimed - issued) <= kUnitsAhead) break;
         __nanosleep(100);
       }
       int waited = 1;
@@ -609,8 +645,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       i = __shfl_sync(kFull, i, 0);
       if (i >= total_items) {
         if (lane == 0) {
-          desc[slot].b = -1;
+          desc[slot].b = -1;                     // the end: producer lanes and consumers stop
           mbar_arrive(&sched_full[slot]);
+          mbar_arrive(&item_full[slot]);
         }
         break;
       }
@@ -639,7 +676,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         desc[slot] = d;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sched_full[slot]);
+      if (lane == 0) {
+        mbar_arrive(&sched_full[slot]);
+        mbar_arrive_expect_tx(&item_full[slot], Tr::Q_BYTES);
+        const char* qsrc =
+            p.q + (static_cast<int64_t>(w.x) * p.num_q_heads + static_cast<int64_t>(h) * G) *
+                      Tr::ROW_BYTES;
+        bulk_g2s(qbuf + slot * Tr::Q_BYTES, qsrc, Tr::Q_BYTES, &item_full[slot]);
+      }
       claimed += static_cast<uint32_t>(n_units);
     }
     return;
@@ -647,49 +691,50 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
   if (warp == kConsumerWarps) {
     // ------------------------------------------------------------ producer
-    // lane w < 8 counts the units handed to consumer warp w so far
-    uint32_t issued = 0, issued_total = 0, q_issued = 0;
+    // Lane w < 8 feeds consumer warp w's sub-ring: the units u of every item
+    // with (u + rot) % 8 == w, in order.  Eight copies are in issue at once (one
+    // issuing thread cannot keep HBM busy), and the lanes advance independently
+    // -- each polls its own barriers without blocking -- so a consumer that is
+    // busy merging only holds back its own sub-ring.
+    const bool mine = lane < kConsumerWarps;
+    bool active = mine;
+    uint32_t k = 0;          // item this lane is in
+    uint32_t c = 0;          // units this lane has issued
+    int u = -1;              // next unit of item k for this lane; -1: descriptor not read yet
+    int n_units = 0, h = 0;
+    uint32_t idle = 0;
     bool ok = true;
-    for (uint32_t k = 0;; ++k) {
-      if (*abort_flag) { ok = false; break; }
-      const int slot = k % kItemSlots;
-      int got = 1;
-      if (lane == 0) got = mbar_wait(&sched_full[slot], (k / kItemSlots) & 1);
-      if (!__shfl_sync(kFull, got, 0)) { ok = false; break; }
-      const ItemDesc d = desc[slot];
-      if (d.b < 0) {
-        if (lane == 0) mbar_arrive(&item_full[slot]);   // hand the end on to the consumers
-        break;
-      }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&item_full[slot], Tr::Q_BYTES);
-        const char* qsrc =
-            p.q + (static_cast<int64_t>(d.b) * p.num_q_heads + static_cast<int64_t>(d.h) * G) *
-                      Tr::ROW_BYTES;
-        bulk_g2s(qbuf + slot * Tr::Q_BYTES, qsrc, Tr::Q_BYTES, &item_full[slot]);
-      }
-      ++q_issued;
-      // Hand the item's units to the consumers, eight at a time: lane w < 8 feeds
-      // consumer warp w's sub-ring (its units are u = u0, u0 + 8, ...), so eight
-      // copies are in issue at once -- one issuing thread cannot keep HBM busy.
-      const int tbl_lane = tbl_s[slot * 32 + lane];   // block id of page `lane` of the chunk
-      const int u0 = (lane - d.rot + kConsumerWarps) % kConsumerWarps;
-      const int rounds = (d.n_units + kConsumerWarps - 1) / kConsumerWarps;
-      for (int rnd = 0; rnd < rounds; ++rnd) {
-        const int u = u0 + rnd * kConsumerWarps;
-        const bool mine = lane < kConsumerWarps && u < d.n_units;
-        const int tok = mine ? u * Tr::UT : 0;
-        const int pp = __shfl_sync(kFull, tbl_lane, tok / bs);
-        int got = 1;
-        if (mine) {
-          const int s = lane + kConsumerWarps * static_cast<int>(issued % Tr::SPW);
-          got = mbar_wait(&empty[s], ((issued / Tr::SPW) & 1) ^ 1);
-          if (got) {
+    while (__any_sync(kFull, active)) {
+      bool progressed = false;
+      if (active) {
+        const int slot = k % kItemSlots;
+        if (u < 0) {
+          if (mbar_test(&sched_full[slot], (k / kItemSlots) & 1)) {
+            const ItemDesc d = desc[slot];
+            progressed = true;
+            if (d.b < 0) {
+              active = false;
+            } else {
+              n_units = d.n_units;
+              h = d.h;
+              u = (lane - d.rot + kConsumerWarps) % kConsumerWarps;
+              if (u >= n_units) {                // no unit of this item for this lane
+                mbar_arrive(&item_empty[slot]);
+                ++k;
+                u = -1;
+              }
+            }
+          }
+        } else {
+          const int s = lane + kConsumerWarps * static_cast<int>(c % Tr::SPW);
+          if (mbar_test(&empty[s], ((c / Tr::SPW) & 1) ^ 1)) {
+            const int tok = u * Tr::UT;
+            const int pp = tbl_s[slot * 32 + tok / bs];
             if (pp >= 0) {
               stage_bad[s] = 0;
               mbar_arrive_expect_tx(&full[s], Tr::STAGE_BYTES);
               char* dst = stages + s * Tr::STAGE_BYTES;
-              const int64_t row = (static_cast<int64_t>(pp) * Hkv + d.h) * bs + (tok % bs);
+              const int64_t row = (static_cast<int64_t>(pp) * Hkv + h) * bs + (tok % bs);
               if constexpr (Tr::TC) {
 #pragma unroll
                 for (int bx = 0; bx < Tr::BOXES; ++bx) {
@@ -707,16 +752,24 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               stage_bad[s] = 1;
               mbar_arrive(&full[s]);
             }
-            ++issued;
+            ++c;
+            issued_by[lane] = c;
+            progressed = true;
+            u += kConsumerWarps;
+            if (u >= n_units) {                  // done with this item
+              mbar_arrive(&item_empty[slot]);
+              ++k;
+              u = -1;
+            }
           }
         }
-        if (!__all_sync(kFull, got)) { ok = false; break; }
-        if (lane == 0) {
-          issued_total += static_cast<uint32_t>(min(kConsumerWarps, d.n_units - rnd * kConsumerWarps));
-          *issued_units = issued_total;
-        }
       }
-      if (!ok) break;
+      if (__any_sync(kFull, progressed)) {
+        idle = 0;
+      } else {
+        if (++idle > kMaxPolls || *abort_flag) { ok = false; break; }
+        __nanosleep(20);
+      }
     }
     if (!ok) {
       // Give up: tell the others, then wait (bounded) for our own copies.
@@ -724,15 +777,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         report(p.device_errors, PA_DEVERR_TIMEOUT);
         *abort_flag = 1;
       }
-      if (lane < kConsumerWarps) {     // copies still in flight on warp `lane`'s sub-ring
-        const uint32_t first = issued > static_cast<uint32_t>(Tr::SPW) ? issued - Tr::SPW : 0;
-        for (uint32_t c = first; c < issued; ++c)
-          mbar_wait(&full[lane + kConsumerWarps * (c % Tr::SPW)], (c / Tr::SPW) & 1);
-      }
-      if (lane == 0) {
-        const uint32_t kfirst = q_issued > kItemSlots ? q_issued - kItemSlots : 0;
-        for (uint32_t k = kfirst; k < q_issued; ++k)
-          mbar_wait(&item_full[k % kItemSlots], (k / kItemSlots) & 1);
+      if (mine) {                      // copies still in flight on warp `lane`'s sub-ring
+        const uint32_t first = c > static_cast<uint32_t>(Tr::SPW) ? c - Tr::SPW : 0;
+        for (uint32_t cc = first; cc < c; ++cc)
+          mbar_wait(&full[lane + kConsumerWarps * (cc % Tr::SPW)], (cc / Tr::SPW) & 1);
       }
     }
     return;
@@ -784,68 +832,83 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             __syncwarp();
           }
         }
-        cs.unit(kt, vt, nt, p.scale_log2);
-        if constexpr (Tr::TC) {
-          // order this warp's generic-proxy writes before the next tensor copy here
-          if (nt < Tr::UT) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        }
+        cs.unit(kt, vt, nt, p.scale_log2, [&] {
+          if constexpr (Tr::TC) {
+            // order this warp's generic-proxy writes before the next tensor copy here
+            if (nt < Tr::UT) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+        });
+      } else {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[s]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[s]);
     }
 
-    // ---- merge the 8 warps' states for this item
-    if (item_k > 0 && !mbar_wait(merge_empty, (item_k - 1) & 1)) {
+    // ---- hand this warp's state to the merge; the last of the 8 warps to
+    // arrive merges while the others go on with their next item
+    if (item_k > 0 && !mbar_wait(merge_free, (item_k - 1) & 1)) {
       report(p.device_errors, PA_DEVERR_TIMEOUT);
       *abort_flag = 1;
       aborted = true;
     }
     cs.store(macc + warp * G * D, mml + warp * G * 2);
     __syncwarp();
-    if (lane == 0) mbar_arrive(merge_full);
-    if (!mbar_wait(merge_full, item_k & 1)) {
-      report(p.device_errors, PA_DEVERR_TIMEOUT);
-      *abort_flag = 1;
-      aborted = true;
+    int last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      last = atomicAdd(merge_cnt, 1) == kConsumerWarps - 1;
+      __threadfence_block();
     }
-    if (!aborted) {
-      const int tid = threadIdx.x;           // 0 .. 8*32-1 (consumers only)
-      for (int o2 = tid; o2 < G * D / 2; o2 += kConsumerWarps * 32) {
-        const int g = o2 / (D / 2);
-        const int dcol = (o2 - g * (D / 2)) * 2;
+    last = __shfl_sync(kFull, last, 0);
+    if (last) {
+      if (lane == 0) *merge_cnt = 0;
+      // out[g] = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w over the 8 warps
+#pragma unroll 1
+      for (int g = 0; g < G; ++g) {
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mml[(w * G + g) * 2]);
-        float lam = 0.f, o0 = 0.f, o1 = 0.f;
+        float f[kConsumerWarps];
+        float lam = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
-          const float f = fast_exp2(mml[(w * G + g) * 2] - M);
-          lam = fmaf(f, mml[(w * G + g) * 2 + 1], lam);
-          const float2 a = *reinterpret_cast<const float2*>(macc + (w * G + g) * D + dcol);
-          o0 = fmaf(f, a.x, o0);
-          o1 = fmaf(f, a.y, o1);
+          f[w] = fast_exp2(mml[(w * G + g) * 2] - M);
+          lam = fmaf(f[w], mml[(w * G + g) * 2 + 1], lam);
         }
         const float inv = 1.f / lam;
-        o0 *= inv;
-        o1 *= inv;
         const int qh = d.h * G + g;
-        if (d.single) {
-          const int64_t o = (static_cast<int64_t>(d.b) * p.num_q_heads + qh) * D + dcol;
-          if constexpr (BF16) {
-            const uint32_t packed = f32_to_bf16_bits(o0) | (f32_to_bf16_bits(o1) << 16);
-            *reinterpret_cast<uint32_t*>(static_cast<char*>(p.out) + o * 2) = packed;
-          } else {
-            *reinterpret_cast<float2*>(static_cast<float*>(p.out) + o) = make_float2(o0, o1);
+#pragma unroll
+        for (int cp = lane; cp < D / 2; cp += 32) {
+          const int dcol = 2 * cp;
+          float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+          for (int w = 0; w < kConsumerWarps; ++w) {
+            const float2 a = *reinterpret_cast<const float2*>(macc + (w * G + g) * D + dcol);
+            o0 = fmaf(f[w], a.x, o0);
+            o1 = fmaf(f[w], a.y, o1);
           }
-        } else {
-          const int64_t row = static_cast<int64_t>(d.gchunk) * p.num_q_heads + qh;
-          *reinterpret_cast<float2*>(p.part_out + row * D + dcol) = make_float2(o0, o1);
-          if (dcol == 0) p.part_lse[row] = M + __log2f(lam);
+          o0 *= inv;
+          o1 *= inv;
+          if (d.single) {
+            const int64_t o = (static_cast<int64_t>(d.b) * p.num_q_heads + qh) * D + dcol;
+            if constexpr (BF16) {
+              const uint32_t packed = f32_to_bf16_bits(o0) | (f32_to_bf16_bits(o1) << 16);
+              *reinterpret_cast<uint32_t*>(static_cast<char*>(p.out) + o * 2) = packed;
+            } else {
+              *reinterpret_cast<float2*>(static_cast<float*>(p.out) + o) = make_float2(o0, o1);
+            }
+          } else {
+            const int64_t row = static_cast<int64_t>(d.gchunk) * p.num_q_heads + qh;
+            *reinterpret_cast<float2*>(p.part_out + row * D + dcol) = make_float2(o0, o1);
+            if (dcol == 0) p.part_lse[row] = M + __log2f(lam);
+          }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(merge_free);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(merge_empty);
     ++item_k;
     if (aborted) break;
   }
