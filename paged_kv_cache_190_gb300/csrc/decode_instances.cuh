@@ -23,9 +23,19 @@ cudaError_t run_decode_kernel(const DecodeKernelParams& kp, int grid, int device
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  paged_decode_kernel<BF16, D, G>
-      <<<grid, kDecodeThreads, Tr::SMEM_ALLOC, stream>>>(kp);
-  return cudaGetLastError();
+  // programmatic dependent launch: the CTAs become resident while the plan
+  // kernel finishes and wait for it on the device
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.dynamicSmemBytes = Tr::SMEM_ALLOC;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, paged_decode_kernel<BF16, D, G>, kp);
 }
 
 template <bool BF16>

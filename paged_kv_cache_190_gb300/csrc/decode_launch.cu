@@ -19,15 +19,20 @@ constexpr int kPlanThreads = 1024;
 
 // Lists every (sequence, chunk) pair in sequence order, records where each
 // sequence's chunks start, resets the work counter and writes zero rows for
-// empty sequences.  One block; sequences are scanned 1024 at a time.
+// empty sequences.  One block; sequences are taken 1024 at a time: a block scan
+// gives each sequence's first chunk, then all threads fill the tile's entries
+// together (entry -> sequence by binary search over the tile's offsets).
 __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(
     const int32_t* __restrict__ context_lens, int num_seqs, int chunk_tokens, int max_len,
     int32_t* __restrict__ header, int32_t* __restrict__ chunk_base, int4* __restrict__ work,
     uint4* __restrict__ out, int64_t row_chunks, int32_t* device_errors) {
   __shared__ int warp_sums[kPlanThreads / 32];
+  __shared__ int first_s[kPlanThreads + 1];     // tile-local exclusive offsets (+ total)
+  __shared__ int len_s[kPlanThreads];
   __shared__ int carry_s;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
+  allow_next_grid();                      // the decode kernel may start its prologue
   if (threadIdx.x == 0) carry_s = 0;
   __syncthreads();
   for (int base = 0; base < num_seqs; base += kPlanThreads) {
@@ -61,15 +66,26 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(
     __syncthreads();
     const int excl = x - n + (warp > 0 ? warp_sums[warp - 1] : 0);
     const int carry = carry_s;
+    first_s[threadIdx.x] = excl;
+    len_s[threadIdx.x] = L;
+    if (threadIdx.x == kPlanThreads - 1) first_s[kPlanThreads] = excl + n;
     if (b < num_seqs) {
-      const int first = carry + excl;
-      chunk_base[b] = first;
-      for (int c = 0; c < n; ++c) work[first + c] = make_int4(b, c, L, first + c);
+      chunk_base[b] = carry + excl;
       if (L == 0)
         for (int64_t k = 0; k < row_chunks; ++k) out[b * row_chunks + k] = make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
-    if (threadIdx.x == kPlanThreads - 1) carry_s = carry + excl + n;
+    const int tile_total = first_s[kPlanThreads];
+    for (int e = threadIdx.x; e < tile_total; e += kPlanThreads) {
+      int lo = 0, hi = kPlanThreads - 1;          // last t with first_s[t] <= e
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (first_s[mid] <= e) lo = mid; else hi = mid - 1;
+      }
+      work[carry + e] = make_int4(base + lo, e - first_s[lo], len_s[lo], carry + e);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) carry_s = carry + tile_total;
     __syncthreads();
   }
   if (threadIdx.x == 0) {
@@ -80,130 +96,38 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(
 }
 
 constexpr int kMergeWarps = 8;
+constexpr int kWideMergeWarps = 16;
 
-// Split-K merge (log-sum-exp): for sequence b, query head i with n >= 2 chunks,
-//   M = max_c lse_c,  w_c = 2^(lse_c - M),  out = sum_c w_c o_c / sum_c w_c,
-// where o_c is chunk c's normalised output and lse_c its base-2 log-sum-exp.
-// One warp per (b, i) row; each lane owns head_dim / 32 columns; the chunk loop
-// has independent loads (the weights need only M), so several are in flight.
-template <bool BF16, int CPL>
-__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(
-    const int32_t* __restrict__ chunk_base, const float* __restrict__ part_lse,
-    const float* __restrict__ part_out, void* __restrict__ out, int num_q_heads, int64_t rows) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
-  if (row >= rows) return;
-  constexpr int D = CPL * 32;
-  const int b = static_cast<int>(row / num_q_heads);
-  const int i = static_cast<int>(row - static_cast<int64_t>(b) * num_q_heads);
-  const int c0 = chunk_base[b];
-  const int n = chunk_base[b + 1] - c0;
-  if (n < 2) return;
-  const float* lse = part_lse + static_cast<int64_t>(c0) * num_q_heads + i;   // stride num_q_heads
-  float M = -INFINITY;
-  for (int c = lane; c < n; c += 32) M = fmaxf(M, lse[static_cast<int64_t>(c) * num_q_heads]);
+// Running log-sum-exp state of one output row over some chunks (base 2):
+//   M = max lse_c, S = sum 2^(lse_c - M), acc = sum 2^(lse_c - M) o_c.
+template <int CPL>
+struct LseAcc {
+  float M = -INFINITY, S = 0.f, acc[CPL] = {};
+
+  __device__ __forceinline__ void add(float lse, const float* v) {
+    const float Mn = fmaxf(M, lse);
+    const float sc = fast_exp2(M - Mn);     // 0 on the first chunk (M = -inf)
+    const float w = fast_exp2(lse - Mn);
+    S = fmaf(S, sc, w);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  const float* po = part_out + (static_cast<int64_t>(c0) * num_q_heads + i) * D + lane * CPL;
-  const int64_t pstride = static_cast<int64_t>(num_q_heads) * D;
-  float S = 0.f, acc[CPL];
-#pragma unroll
-  for (int k = 0; k < CPL; ++k) acc[k] = 0.f;
-#pragma unroll 8
-  for (int c = 0; c < n; ++c) {
-    const float w = fast_exp2(lse[static_cast<int64_t>(c) * num_q_heads] - M);
-    S += w;
-    if constexpr (CPL == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(po + c * pstride);
-      acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
-      acc[2] = fmaf(w, v.z, acc[2]); acc[3] = fmaf(w, v.w, acc[3]);
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(po + c * pstride);
-      acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
-    }
+    for (int k = 0; k < CPL; ++k) acc[k] = fmaf(acc[k], sc, w * v[k]);
+    M = Mn;
   }
-  const float inv = 1.f / S;
-  const int64_t o = row * D + lane * CPL;
-  if constexpr (BF16) {
-    uint32_t w0 = f32_to_bf16_bits(acc[0] * inv) | (f32_to_bf16_bits(acc[1] * inv) << 16);
-    if constexpr (CPL == 4) {
-      uint32_t w1 = f32_to_bf16_bits(acc[2] * inv) | (f32_to_bf16_bits(acc[3] * inv) << 16);
-      *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(out) + o) = make_uint2(w0, w1);
-    } else {
-      *reinterpret_cast<uint32_t*>(reinterpret_cast<uint16_t*>(out) + o) = w0;
-    }
+};
+
+template <int CPL>
+__device__ __forceinline__ void load_cols(const float* p, float* v) {
+  if constexpr (CPL == 4) {
+    const float4 t = *reinterpret_cast<const float4*>(p);
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
   } else {
-    float* dst = reinterpret_cast<float*>(out) + o;
-#pragma unroll
-    for (int k = 0; k < CPL; ++k) dst[k] = acc[k] * inv;
+    const float2 t = *reinterpret_cast<const float2*>(p);
+    v[0] = t.x; v[1] = t.y;
   }
 }
 
-// The same merge for long chunk lists: one block per (b, i) row, its 8 warps
-// take chunks c = warp, warp + 8, ... and combine their sums in shared memory.
 template <bool BF16, int CPL>
-__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_wide_kernel(
-    const int32_t* __restrict__ chunk_base, const float* __restrict__ part_lse,
-    const float* __restrict__ part_out, void* __restrict__ out, int num_q_heads) {
-  constexpr int D = CPL * 32;
-  __shared__ float red[kMergeWarps];
-  __shared__ float sacc[kMergeWarps][D];
-  __shared__ float ssum[kMergeWarps];
-  const int lane = threadIdx.x & 31;
-  const int warp = threadIdx.x >> 5;
-  const int64_t row = blockIdx.x;
-  const int b = static_cast<int>(row / num_q_heads);
-  const int i = static_cast<int>(row - static_cast<int64_t>(b) * num_q_heads);
-  const int c0 = chunk_base[b];
-  const int n = chunk_base[b + 1] - c0;
-  if (n < 2) return;                      // uniform over the block
-  const float* lse = part_lse + static_cast<int64_t>(c0) * num_q_heads + i;
-  float M = -INFINITY;
-  for (int c = threadIdx.x; c < n; c += blockDim.x)
-    M = fmaxf(M, lse[static_cast<int64_t>(c) * num_q_heads]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if (lane == 0) red[warp] = M;
-  __syncthreads();
-  M = red[0];
-#pragma unroll
-  for (int w = 1; w < kMergeWarps; ++w) M = fmaxf(M, red[w]);
-  const float* po = part_out + (static_cast<int64_t>(c0) * num_q_heads + i) * D + lane * CPL;
-  const int64_t pstride = static_cast<int64_t>(num_q_heads) * D;
-  float S = 0.f, acc[CPL];
-#pragma unroll
-  for (int k = 0; k < CPL; ++k) acc[k] = 0.f;
-#pragma unroll 4
-  for (int c = warp; c < n; c += kMergeWarps) {
-    const float w = fast_exp2(lse[static_cast<int64_t>(c) * num_q_heads] - M);
-    S += w;
-    if constexpr (CPL == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(po + c * pstride);
-      acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
-      acc[2] = fmaf(w, v.z, acc[2]); acc[3] = fmaf(w, v.w, acc[3]);
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(po + c * pstride);
-      acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
-    }
-  }
-#pragma unroll
-  for (int k = 0; k < CPL; ++k) sacc[warp][lane * CPL + k] = acc[k];
-  if (lane == 0) ssum[warp] = S;
-  __syncthreads();
-  if (warp != 0) return;
-  float tot = 0.f;
-#pragma unroll
-  for (int w = 0; w < kMergeWarps; ++w) tot += ssum[w];
-  const float inv = 1.f / tot;
-  float r[CPL];
-#pragma unroll
-  for (int k = 0; k < CPL; ++k) {
-    float a = 0.f;
-#pragma unroll
-    for (int w = 0; w < kMergeWarps; ++w) a += sacc[w][lane * CPL + k];
-    r[k] = a * inv;
-  }
-  const int64_t o = row * D + lane * CPL;
+__device__ __forceinline__ void store_row(void* out, int64_t o, const float* r) {
   if constexpr (BF16) {
     const uint32_t w0 = f32_to_bf16_bits(r[0]) | (f32_to_bf16_bits(r[1]) << 16);
     if constexpr (CPL == 4) {
@@ -219,19 +143,128 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_wide_kernel(
   }
 }
 
+// Split-K merge (log-sum-exp): for sequence b, query head i with n >= 2 chunks,
+//   out = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M),  M = max_c lse_c,
+// where o_c is chunk c's normalised output and lse_c its base-2 log-sum-exp.
+// One warp per (b, i) row, each lane owning head_dim / 32 columns; one pass with
+// a running maximum, so every chunk's loads can be in flight together.
 template <bool BF16, int CPL>
-void launch_merge(const DecodeArgs& a, cudaStream_t stream) {
+__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(
+    const int32_t* __restrict__ chunk_base, const float* __restrict__ part_lse,
+    const float* __restrict__ part_out, void* __restrict__ out, int num_q_heads, int64_t rows) {
+  constexpr int D = CPL * 32;
+  wait_prior_grids();                     // the decode kernel's partials
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int b = static_cast<int>(row / num_q_heads);
+  const int i = static_cast<int>(row - static_cast<int64_t>(b) * num_q_heads);
+  const int c0 = chunk_base[b];
+  const int n = chunk_base[b + 1] - c0;
+  if (n < 2) return;
+  const int64_t prow0 = static_cast<int64_t>(c0) * num_q_heads + i;
+  LseAcc<CPL> st;
+#pragma unroll 8
+  for (int c = 0; c < n; ++c) {
+    const int64_t prow = prow0 + static_cast<int64_t>(c) * num_q_heads;
+    float v[CPL];
+    load_cols<CPL>(part_out + prow * D + lane * CPL, v);
+    st.add(part_lse[prow], v);
+  }
+  float r[CPL];
+  const float inv = 1.f / st.S;
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) r[k] = st.acc[k] * inv;
+  store_row<BF16, CPL>(out, row * D + lane * CPL, r);
+}
+
+// The same merge for long chunk lists: one block per (b, i) row; its 16 warps
+// take chunks c = warp, warp + 16, ... and their states are combined in
+// shared memory.
+template <bool BF16, int CPL>
+__global__ void __launch_bounds__(kWideMergeWarps * 32) decode_merge_wide_kernel(
+    const int32_t* __restrict__ chunk_base, const float* __restrict__ part_lse,
+    const float* __restrict__ part_out, void* __restrict__ out, int num_q_heads) {
+  constexpr int D = CPL * 32;
+  __shared__ float sM[kWideMergeWarps], sS[kWideMergeWarps];
+  __shared__ float sacc[kWideMergeWarps][D];
+  wait_prior_grids();                     // the decode kernel's partials
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int64_t row = blockIdx.x;
+  const int b = static_cast<int>(row / num_q_heads);
+  const int i = static_cast<int>(row - static_cast<int64_t>(b) * num_q_heads);
+  const int c0 = chunk_base[b];
+  const int n = chunk_base[b + 1] - c0;
+  if (n < 2) return;                      // uniform over the block
+  const int64_t prow0 = static_cast<int64_t>(c0) * num_q_heads + i;
+  LseAcc<CPL> st;
+#pragma unroll 8
+  for (int c = warp; c < n; c += kWideMergeWarps) {
+    const int64_t prow = prow0 + static_cast<int64_t>(c) * num_q_heads;
+    float v[CPL];
+    load_cols<CPL>(part_out + prow * D + lane * CPL, v);
+    st.add(part_lse[prow], v);
+  }
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) sacc[warp][lane * CPL + k] = st.acc[k];
+  if (lane == 0) {
+    sM[warp] = st.M;
+    sS[warp] = st.S;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  float M = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < kWideMergeWarps; ++w) M = fmaxf(M, sM[w]);
+  float S = 0.f, r[CPL] = {};
+#pragma unroll
+  for (int w = 0; w < kWideMergeWarps; ++w) {
+    const float f = fast_exp2(sM[w] - M);   // warps without chunks: S = 0, acc = 0
+    S = fmaf(f, sS[w], S);
+#pragma unroll
+    for (int k = 0; k < CPL; ++k) r[k] = fmaf(f, sacc[w][lane * CPL + k], r[k]);
+  }
+  const float inv = 1.f / S;
+#pragma unroll
+  for (int k = 0; k < CPL; ++k) r[k] *= inv;
+  store_row<BF16, CPL>(out, row * D + lane * CPL, r);
+}
+
+// Launch as a programmatic dependent of the decode kernel (its blocks wait for
+// the decode kernel on the device), which hides the launch gap.
+template <typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Args...), unsigned blocks, unsigned threads,
+                             cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+template <bool BF16, int CPL>
+cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
   const int64_t max_chunks_per_seq = (static_cast<int64_t>(a.max_context_len) + a.chunk_tokens - 1) /
                                      a.chunk_tokens;
-  if (max_chunks_per_seq >= 32) {
-    decode_merge_wide_kernel<BF16, CPL><<<static_cast<unsigned>(rows), kMergeWarps * 32, 0, stream>>>(
-        a.ws.chunk_base, a.ws.part_lse, a.ws.part_out, a.out, a.num_q_heads);
-  } else {
-    const unsigned blocks = static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps);
-    decode_merge_kernel<BF16, CPL><<<blocks, kMergeWarps * 32, 0, stream>>>(
-        a.ws.chunk_base, a.ws.part_lse, a.ws.part_out, a.out, a.num_q_heads, rows);
-  }
+  if (max_chunks_per_seq >= 32)
+    return launch_dependent(decode_merge_wide_kernel<BF16, CPL>, static_cast<unsigned>(rows),
+                            kWideMergeWarps * 32, stream,
+                            static_cast<const int32_t*>(a.ws.chunk_base),
+                            static_cast<const float*>(a.ws.part_lse),
+                            static_cast<const float*>(a.ws.part_out), a.out, a.num_q_heads);
+  const unsigned blocks = static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps);
+  return launch_dependent(decode_merge_kernel<BF16, CPL>, blocks, kMergeWarps * 32, stream,
+                          static_cast<const int32_t*>(a.ws.chunk_base),
+                          static_cast<const float*>(a.ws.part_lse),
+                          static_cast<const float*>(a.ws.part_out), a.out, a.num_q_heads, rows);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -335,11 +368,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
              : run_decode_f32(a.head_dim, group, kp, grid, device, stream);
   if (e != cudaSuccess) return e;
   if (a.max_context_len > a.chunk_tokens) {
-    if (a.bf16 && a.head_dim == 128) launch_merge<true, 4>(a, stream);
-    else if (a.bf16) launch_merge<true, 2>(a, stream);
-    else if (a.head_dim == 128) launch_merge<false, 4>(a, stream);
-    else launch_merge<false, 2>(a, stream);
-    e = cudaGetLastError();
+    if (a.bf16 && a.head_dim == 128) e = launch_merge<true, 4>(a, stream);
+    else if (a.bf16) e = launch_merge<true, 2>(a, stream);
+    else if (a.head_dim == 128) e = launch_merge<false, 4>(a, stream);
+    else e = launch_merge<false, 2>(a, stream);
   }
   return e;
 }

@@ -81,6 +81,16 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
       : "memory");
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on have
+// completed (their writes visible); let the grid queued after this one start
+// launching.
+__device__ __forceinline__ void wait_prior_grids() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_next_grid() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void report(int32_t* device_errors, int32_t bits) {
   if (device_errors) atomicOr(device_errors, bits);
 }

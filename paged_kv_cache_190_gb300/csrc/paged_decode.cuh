@@ -607,6 +607,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     for (int w = 0; w < kConsumerWarps; ++w) issued_by[w] = 0;
     fence_mbar_init();
   }
+  // launched as a programmatic dependent of the plan kernel: everything above
+  // overlaps its tail; the work list is only read after it has completed
+  wait_prior_grids();
+  allow_next_grid();
   __syncthreads();
 
   const int Hkv = p.num_kv_heads;
