@@ -156,6 +156,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(x: float, device, world: int) -> float:
+    """The slowest rank's value (every rank gets it); `device` is where the
+    process group's backend reduces (a CUDA device for NCCL, the CPU for gloo)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step_per_rank: int, world: int, seconds_per_step: float) -> float:
+    """Whole-job throughput: every rank's bytes over the slowest rank's time."""
+    return world * bytes_per_step_per_rank / seconds_per_step / 1e9
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -313,11 +330,7 @@ def run_gpu(args, world, rank, local):
     total_ms = t_start.elapsed_time(t_end)
     decode_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
     write_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    ms_per_step = total_ms / K
-    if world > 1:
-        t = torch.tensor([ms_per_step], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_per_step = float(t.item())
+    ms_per_step = max_over_ranks(total_ms / K, device, world)
     flags = pa.pa_read_device_errors(ws.errs)
     if flags:
         raise RuntimeError(f"device error bits {flags} during the timed steps")
@@ -329,7 +342,7 @@ def run_gpu(args, world, rank, local):
         return None
     peak, peak_src = hbm_peak()
     b = ws.bytes
-    value = world * b["step"] / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(b["step"], world, ms_per_step * 1e-3)
     dec_avg_ms = statistics.mean(decode_ms)
     achieved = b["decode"] / (dec_avg_ms * 1e-3) / 1e9
     traffic = ncu_traffic(args.workload)
@@ -406,12 +419,8 @@ def run_e2e(ws, args, torch, pa, device, stream, barrier, world):
         one()
     t1 = time.perf_counter()
     barrier()
-    sec = (t1 - t0) / n
-    if world > 1:
-        t = torch.tensor([sec], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        sec = float(t.item())
-    return {"value": round(world * ws.bytes["step"] / sec / 1e9, 2), "unit": "GB/s",
+    sec = max_over_ranks((t1 - t0) / n, device, world)
+    return {"value": round(whole_job_gbs(ws.bytes["step"], world, sec), 2), "unit": "GB/s",
             "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "us_per_step": round(sec * 1e6, 2), "steps": n}
 
