@@ -375,6 +375,7 @@ def run_gpu(args, world, rank, local):
             "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json hbm' if peak_src == 'measured' else 'profiling recipe fallback 6.8 TB/s'})",
         },
         "write_avg_us": round(statistics.mean(write_ms) * 1e3, 2),
+        "host_block_manager": host_block_manager_time(ws.case, pa),
         "e2e": e2e,
         "gpu_launches": ws.launches_per_step * K,
         "clocks": clocks.summary(),
@@ -382,6 +383,43 @@ def run_gpu(args, world, rank, local):
     if not args.no_cpu_baseline and world == 1:
         result["cpu_baseline"] = cpu_baseline(ws.case, budget_s=args.cpu_budget)
     return result
+
+
+def host_block_manager_time(case, pa, repeats: int = 100):
+    """Host cost of the block manager for this batch, after the sequences have
+    been grown to the workload's lengths: one decode step (every sequence takes
+    its next slot -- a new page at page boundaries -- and the step's tables and
+    lengths are exported), and a fork plus a free of every sequence (the
+    shared-prefix and finish paths).  Medians over `repeats`."""
+    B, bs = case.num_seqs, case.block_size
+    lens = case.context_lens.astype(np.int64)
+    pages = (lens + bs - 1) // bs
+    mb = int(pages.max()) + repeats // bs + 2
+    bm = pa.BlockManager(int(pages.sum()) + B * (repeats // bs + 3), bs)
+    ids = np.arange(B, dtype=np.int64)
+    for b in range(B):
+        bm.add_seq(b)
+    for t in range(int(lens.max())):
+        active = ids[lens > t]
+        if active.size:
+            bm.append_slots(active)
+    step_us, fork_free_us = [], []
+    for _ in range(repeats):
+        t0 = time.perf_counter()
+        bm.append_slots(ids)
+        bm.build_block_tables(ids, mb)
+        step_us.append((time.perf_counter() - t0) * 1e6)
+    for _ in range(max(3, repeats // 10)):
+        t0 = time.perf_counter()
+        for b in range(B):
+            bm.fork(b, B + b)
+        for b in range(B):
+            bm.free(B + b)
+        fork_free_us.append((time.perf_counter() - t0) * 1e6)
+    bm.close()
+    return {"step_append_slots_and_tables_us": round(statistics.median(step_us), 1),
+            "fork_and_free_all_us": round(statistics.median(fork_free_us), 1),
+            "num_seqs": B, "note": "host C++ block manager via ctypes; outside the device timing"}
 
 
 def run_e2e(ws, args, torch, pa, device, stream, barrier, world):

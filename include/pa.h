@@ -165,6 +165,16 @@ int pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void*
                       int max_context_len, pa_dtype dtype, int chunk_tokens,
                       int32_t* device_errors, void* stream);
 
+/*
+ * Test hook for the failure path.  Every pipeline wait of the decode kernels
+ * enqueued after this call gives up after `polls` polls (0: at once) and
+ * reports PA_DEVERR_TIMEOUT; the kernel then waits for its own copies in flight
+ * (with the normal bound) and returns, leaving the context usable.  polls < 0
+ * restores the normal bound (well over a second).  Process-wide; meant for
+ * tests, not for concurrent use.
+ */
+int pa_debug_set_wait_limit(int polls);
+
 /* Synchronise `stream`, copy *device_errors to *host_flags, and zero it on the
  * device when `clear` is non-zero.  This is the one call that waits. */
 int pa_read_device_errors(int32_t* device_errors, int32_t* host_flags, int clear, void* stream);

@@ -120,7 +120,7 @@ static int decode_row(double* out_row, const void* q, const void* k_cache, const
 }
 
 /* rows: NULL for every (b, i) row, else num_rows pairs {b, i}.  Returns 0, or
- * the first negative status of any row.  `threads` <= 0 leaves OpenMP's default. */
+ * the first negative status of any row.  `threads` <= 0 uses every processor. */
 int oracle_decode_f64(double* out, const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* block_tables, const int32_t* context_lens, double scale,
                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
@@ -131,8 +131,8 @@ int oracle_decode_f64(double* out, const void* q, const void* k_cache, const voi
   const long n = rows ? (long)num_rows : (long)num_seqs * num_q_heads;
   int status = 0;
 #ifdef _OPENMP
-  if (threads > 0) omp_set_num_threads(threads);
-#pragma omp parallel for schedule(dynamic, 1)
+  const int nthreads = threads > 0 ? threads : omp_get_num_procs();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
 #endif
   for (long r = 0; r < n; ++r) {
     const int b = rows ? rows[2 * r] : (int)(r / num_q_heads);
@@ -154,7 +154,7 @@ int oracle_decode_f64(double* out, const void* q, const void* k_cache, const voi
 
 int oracle_max_threads(void) {
 #ifdef _OPENMP
-  return omp_get_max_threads();
+  return omp_get_num_procs();
 #else
   return 1;
 #endif

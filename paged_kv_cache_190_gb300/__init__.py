@@ -13,5 +13,5 @@ from ._lib import (  # noqa: F401
     PA_BF16, PA_F32, PA_DEVERR_BAD_BLOCK, PA_DEVERR_BAD_LENGTH, PA_DEVERR_BAD_SLOT,
     PA_DEVERR_TIMEOUT, BlockManager, OutOfBlocks, PaError, library, library_path,
     pa_copy_blocks, pa_decode, pa_decode_chunk_tokens, pa_decode_noalloc, PA_NOALLOC_SCRATCH_BYTES, pa_decode_workspace_size,
-    pa_get_error_string, pa_read_device_errors, pa_reshape_and_cache, EXPORTED_SYMBOLS,
+    pa_get_error_string, pa_read_device_errors, pa_debug_set_wait_limit, pa_reshape_and_cache, EXPORTED_SYMBOLS,
 )

@@ -18,7 +18,8 @@ PA_DEVERR_BAD_BLOCK, PA_DEVERR_BAD_LENGTH, PA_DEVERR_BAD_SLOT, PA_DEVERR_TIMEOUT
 # Every function include/pa.h declares (checked by the tests).
 EXPORTED_SYMBOLS = [
     "pa_get_error_string", "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_chunk_tokens",
-    "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc", "pa_read_device_errors",
+    "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc", "pa_debug_set_wait_limit",
+    "pa_read_device_errors",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq", "pa_bm_append_slot", "pa_bm_fork",
     "pa_bm_free", "pa_bm_block_table", "pa_bm_refcount", "pa_bm_num_free", "pa_bm_free_list",
     "pa_bm_stats", "pa_bm_append_slots", "pa_bm_build_block_tables",
@@ -42,6 +43,7 @@ _SIGNATURES = {
                          _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
     "pa_decode_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _i32, _i32, _i32,
                                  _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "pa_debug_set_wait_limit": (_i32, [_i32]),
     "pa_read_device_errors": (_i32, [_vp, _pi32, _i32, _vp]),
     "pa_bm_create": (_i32, [_i32, _i32, _pi32, ctypes.POINTER(_vp)]),
     "pa_bm_destroy": (None, [_vp]),
@@ -233,6 +235,11 @@ def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scal
         _ptr(device_errors), _stream(stream, q.device))
     _check(rc, "pa_decode_noalloc")
     return out
+
+
+def pa_debug_set_wait_limit(polls: int) -> None:
+    """Test hook: bound every decode pipeline wait to `polls` polls (< 0: normal)."""
+    _check(library().pa_debug_set_wait_limit(int(polls)), "pa_debug_set_wait_limit")
 
 
 def pa_read_device_errors(device_errors, clear=True, stream=None) -> int:

@@ -12,6 +12,9 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Bound on each decode pipeline wait, in polls (< 0: the kernels' default).
+std::atomic<int64_t> g_wait_limit{-1};
+
 bool supported_shape(int head_dim, int block_size) {
   return (head_dim == 64 || head_dim == 128) && (block_size == 16 || block_size == 32);
 }
@@ -180,8 +183,14 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   a.ws.max_chunks = lay.max_chunks;
   a.device_errors = device_errors;
   a.num_sms = sms;
+  a.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
   const cudaError_t e = pa::launch_decode(a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_debug_set_wait_limit(int polls) {
+  g_wait_limit.store(polls < 0 ? -1 : polls, std::memory_order_relaxed);
+  return PA_OK;
 }
 
 int pa_read_device_errors(int32_t* device_errors, int32_t* host_flags, int clear, void* stream) {

@@ -359,6 +359,7 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   kp.part_lse = a.ws.part_lse;
   kp.part_out = a.ws.part_out;
   kp.device_errors = a.device_errors;
+  kp.wait_limit = a.wait_limit < 0 ? kMaxPolls : static_cast<uint32_t>(a.wait_limit);
   const int64_t items_upper = a.ws.max_chunks * a.num_kv_heads;
   const int grid = static_cast<int>(items_upper < a.num_sms ? items_upper : a.num_sms);
   int device = 0;

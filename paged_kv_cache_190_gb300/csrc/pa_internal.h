@@ -41,6 +41,7 @@ struct DecodeArgs {
   DecodeWorkspace ws;
   int32_t* device_errors;
   int num_sms;
+  int64_t wait_limit;  // polls before a pipeline wait gives up; < 0: the default bound
 };
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);

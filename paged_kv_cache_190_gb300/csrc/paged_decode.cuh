@@ -145,6 +145,7 @@ struct DecodeKernelParams {
   float* part_lse;
   float* part_out;
   int32_t* device_errors;
+  uint32_t wait_limit;              // polls before a pipeline wait gives up (drains use kMaxPolls)
 };
 
 // Butterfly step over lane bit `mask` (within 8-lane groups): lanes with the
@@ -624,10 +625,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     // K/V copies.  It keeps at most kUnitsAhead claimed-but-unissued units,
     // which bounds the work one CTA holds back when the queue runs dry.
     const int total_items = p.header[1] * Hkv;
-    uint32_t claimed = 0;
+    uint32_t claimed = 0, q_issued = 0;
+    bool ended = false;                          // published the end marker
     for (uint32_t k = 0;; ++k) {
       const int slot = k % kItemSlots;
-      for (uint32_t spin = 0; spin < kMaxPolls; ++spin) {
+      for (uint32_t spin = 0; spin < p.wait_limit; ++spin) {
         uint32_t issued = 0;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) issued += issued_by[w];
@@ -635,7 +637,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         __nanosleep(100);
       }
       int waited = 1;
-      if (lane == 0) waited = mbar_wait(&item_empty[slot], ((k / kItemSlots) & 1) ^ 1);
+      if (lane == 0) waited = mbar_wait(&item_empty[slot], ((k / kItemSlots) & 1) ^ 1, p.wait_limit);
       if (!__shfl_sync(kFull, waited, 0)) {
         if (lane == 0) {
           report(p.device_errors, PA_DEVERR_TIMEOUT);
@@ -653,6 +655,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           mbar_arrive(&sched_full[slot]);
           mbar_arrive(&item_full[slot]);
         }
+        ended = true;
         break;
       }
       const int j = i / Hkv;
@@ -688,7 +691,17 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
                       Tr::ROW_BYTES;
         bulk_g2s(qbuf + slot * Tr::Q_BYTES, qsrc, Tr::Q_BYTES, &item_full[slot]);
       }
+      ++q_issued;
       claimed += static_cast<uint32_t>(n_units);
+    }
+    // Wait (bounded) for our q copies that may still be in flight: item k's slot
+    // was reused for item k + NI only after every consumer had read it, so only
+    // the last NI items can be outstanding -- NI - 1 once the end marker has
+    // taken the oldest one's slot.
+    if (lane == 0) {
+      const uint32_t span = ended ? kItemSlots - 1 : kItemSlots;
+      for (uint32_t k = q_issued > span ? q_issued - span : 0; k < q_issued; ++k)
+        mbar_wait(&item_full[k % kItemSlots], (k / kItemSlots) & 1);
     }
     return;
   }
@@ -771,21 +784,20 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       if (__any_sync(kFull, progressed)) {
         idle = 0;
       } else {
-        if (++idle > kMaxPolls || *abort_flag) { ok = false; break; }
+        if (++idle > p.wait_limit || *abort_flag) { ok = false; break; }
         __nanosleep(20);
       }
     }
-    if (!ok) {
-      // Give up: tell the others, then wait (bounded) for our own copies.
-      if (lane == 0) {
-        report(p.device_errors, PA_DEVERR_TIMEOUT);
-        *abort_flag = 1;
-      }
-      if (mine) {                      // copies still in flight on warp `lane`'s sub-ring
-        const uint32_t first = c > static_cast<uint32_t>(Tr::SPW) ? c - Tr::SPW : 0;
-        for (uint32_t cc = first; cc < c; ++cc)
-          mbar_wait(&full[lane + kConsumerWarps * (cc % Tr::SPW)], (cc / Tr::SPW) & 1);
-      }
+    if (!ok && lane == 0) {            // give up: tell the others
+      report(p.device_errors, PA_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+    // Wait (bounded) for copies still in flight on warp `lane`'s sub-ring: only
+    // the last SPW can be (immediate when the consumers took them all).
+    if (mine) {
+      const uint32_t first = c > static_cast<uint32_t>(Tr::SPW) ? c - Tr::SPW : 0;
+      for (uint32_t cc = first; cc < c; ++cc)
+        mbar_wait(&full[lane + kConsumerWarps * (cc % Tr::SPW)], (cc / Tr::SPW) & 1);
     }
     return;
   }
@@ -798,7 +810,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   bool aborted = false;
   for (;;) {
     const int slot = item_k % kItemSlots;
-    if (!mbar_wait(&item_full[slot], (item_k / kItemSlots) & 1)) {
+    if (!mbar_wait(&item_full[slot], (item_k / kItemSlots) & 1, p.wait_limit)) {
       report(p.device_errors, PA_DEVERR_TIMEOUT);
       *abort_flag = 1;
       break;
@@ -813,7 +825,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     const int u0 = (warp - d.rot + kConsumerWarps) % kConsumerWarps;
     for (int u = u0; u < d.n_units && !aborted; u += kConsumerWarps, ++consumed) {
       const int s = warp + kConsumerWarps * static_cast<int>(consumed % Tr::SPW);
-      if (!mbar_wait(&full[s], (consumed / Tr::SPW) & 1)) {
+      if (!mbar_wait(&full[s], (consumed / Tr::SPW) & 1, p.wait_limit)) {
         report(p.device_errors, PA_DEVERR_TIMEOUT);
         *abort_flag = 1;
         aborted = true;
@@ -852,7 +864,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
 
     // ---- hand this warp's state to the merge; the last of the 8 warps to
     // arrive merges while the others go on with their next item
-    if (item_k > 0 && !mbar_wait(merge_free, (item_k - 1) & 1)) {
+    if (item_k > 0 && !mbar_wait(merge_free, (item_k - 1) & 1, p.wait_limit)) {
       report(p.device_errors, PA_DEVERR_TIMEOUT);
       *abort_flag = 1;
       aborted = true;
