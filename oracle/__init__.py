@@ -9,14 +9,18 @@ Contents, each written from the pages (cited in the modules):
   * ``decode_f64``         -- fp64 gather-then-attend over the block table (plain C).
   * ``reshape_and_cache``  -- byte copy of each new token's K/V into its slot.
   * ``copy_blocks``        -- byte copy of whole pages for copy-on-write.
+  * ``e4m3_encode`` / ``decode_kv8_f64`` / ``reshape_and_cache_fp8`` -- the same
+                              path with float8 e4m3 pools and per-kv-head scales.
   * ``RefBlockManager``    -- the teaching allocator of "PagedAttention原理" §3.3.4
                               with the reference counts of §3.3.3 and copy-on-write.
 """
-from ._decode import build, decode_f64, library_path, max_threads, widen
-from ._cache_ops import copy_blocks, reshape_and_cache
+from ._decode import build, decode_f64, decode_kv8_f64, library_path, max_threads, widen
+from ._cache_ops import (copy_blocks, e4m3_encode, e4m3_value, reshape_and_cache,
+                         reshape_and_cache_fp8)
 from .ref_block_manager import OutOfBlocks, RefBlockManager
 
 __all__ = [
-    "build", "decode_f64", "library_path", "max_threads", "widen",
-    "copy_blocks", "reshape_and_cache", "OutOfBlocks", "RefBlockManager",
+    "build", "decode_f64", "decode_kv8_f64", "library_path", "max_threads", "widen",
+    "copy_blocks", "e4m3_encode", "e4m3_value", "reshape_and_cache", "reshape_and_cache_fp8",
+    "OutOfBlocks", "RefBlockManager",
 ]

@@ -49,3 +49,51 @@ def copy_blocks(k_cache, v_cache, src_dst_pairs) -> None:
             raise ValueError(f"pair ({src}, {dst}) is outside the pool")
         k_cache[dst] = k_cache[src]
         v_cache[dst] = v_cache[src]
+
+
+# ------------------------------------------------------------------ float8 e4m3
+def e4m3_value(code: int) -> float:
+    """Value of an e4m3 code: 1 sign bit, 4 exponent bits (bias 7), 3 fraction
+    bits; exponent 0 is subnormal (fraction * 2^-9); 0x7F / 0xFF are NaN."""
+    sign = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 15, code & 7
+    if e == 15 and m == 7:
+        return float("nan")
+    if e == 0:
+        return sign * m * 2.0 ** -9
+    return sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+
+
+_E4M3_POS = np.array([e4m3_value(c) for c in range(0x7F)])     # codes 0..126, increasing
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """float32 values -> e4m3 codes: the nearest representable value, ties to
+    the even code; magnitudes past the largest finite value (448) saturate to
+    it; NaN -> 0x7F.  The sign bit follows the input's sign."""
+    x = np.asarray(x, dtype=np.float32)
+    a = np.abs(x.astype(np.float64))
+    hi = np.clip(np.searchsorted(_E4M3_POS, a, side="left"), 0, 126)
+    lo = np.clip(hi - 1, 0, 126)
+    d_lo = a - _E4M3_POS[lo]
+    d_hi = _E4M3_POS[hi] - a
+    code = np.where(d_hi < d_lo, hi, lo)
+    tie = d_hi == d_lo
+    code = np.where(tie & (hi != lo), np.where(hi % 2 == 0, hi, lo), code)
+    code = np.where(a >= _E4M3_POS[126], 126, code)            # saturate (incl. +-inf)
+    code = code.astype(np.uint8) | np.where(np.signbit(x), 0x80, 0).astype(np.uint8)
+    return np.where(np.isnan(x), np.uint8(0x7F), code).astype(np.uint8)
+
+
+def reshape_and_cache_fp8(k, v, k_cache, v_cache, slot_mapping, k_scale, v_scale) -> None:
+    """The cache write with float8 e4m3 pools: each element of token t, kv head
+    h is stored as e4m3(k / k_scale[h]) (the division in float32), likewise v.
+    k, v: bf16 bits (uint16) [T, Hkv, D]; caches uint8 [NB, Hkv, bs, D]."""
+    from ._decode import widen
+    T = k.shape[0]
+    NB, Hkv, bs, D = k_cache.shape
+    ks = np.asarray(k_scale, dtype=np.float32).reshape(1, Hkv, 1)
+    vs = np.asarray(v_scale, dtype=np.float32).reshape(1, Hkv, 1)
+    kq = e4m3_encode(widen(k, "bf16").astype(np.float32) / ks)
+    vq = e4m3_encode(widen(v, "bf16").astype(np.float32) / vs)
+    reshape_and_cache(kq, vq, k_cache, v_cache, slot_mapping)

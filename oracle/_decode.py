@@ -20,7 +20,7 @@ _LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-DTYPE_CODES = {"f32": 0, "bf16": 1}
+DTYPE_CODES = {"f32": 0, "bf16": 1, "fp8": 2}
 
 
 def library_path() -> str:
@@ -52,6 +52,11 @@ def _load():
                 vp, vp, vp, vp, i32p, i32p, ctypes.c_double,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int]
+            lib.oracle_decode_kv8_f64.restype = ctypes.c_int
+            lib.oracle_decode_kv8_f64.argtypes = [
+                vp, vp, vp, vp, i32p, i32p, ctypes.c_double, vp, vp,
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int, ctypes.c_int]
             lib.oracle_widen.restype = None
             lib.oracle_widen.argtypes = [vp, vp, ctypes.c_long, ctypes.c_int]
             lib.oracle_max_threads.restype = ctypes.c_int
@@ -65,7 +70,7 @@ def max_threads() -> int:
 
 
 def _storage(a: np.ndarray, dtype: str) -> np.ndarray:
-    want = np.uint16 if dtype == "bf16" else np.float32
+    want = {"bf16": np.uint16, "f32": np.float32, "fp8": np.uint8}[dtype]
     if a.dtype != want:
         raise TypeError(f"{dtype} data must be stored as {want.__name__}, got {a.dtype}")
     return np.ascontiguousarray(a)
@@ -113,4 +118,37 @@ def decode_f64(q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_he
         rows_arr.ctypes.data_as(i32p) if rows_arr is not None else None, nrows, int(threads))
     if rc != 0:
         raise ValueError(f"oracle_decode_f64 refused the input (status {rc})")
+    return out
+
+
+def decode_kv8_f64(q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale,
+                   rows=None, threads: int = 0) -> np.ndarray:
+    """fp64 paged decode with float8 e4m3 caches: K = code * k_scale[h],
+    V = code * v_scale[h] for kv head h; q is bf16 (uint16 bits)."""
+    q = _storage(q, "bf16")
+    k_cache = _storage(k_cache, "fp8")
+    v_cache = _storage(v_cache, "fp8")
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B, Hq, D = q.shape
+    NB, Hkv, bs, D2 = k_cache.shape
+    ks = np.ascontiguousarray(k_scale, dtype=np.float64)
+    vs = np.ascontiguousarray(v_scale, dtype=np.float64)
+    if D2 != D or v_cache.shape != k_cache.shape or ks.shape != (Hkv,) or vs.shape != (Hkv,):
+        raise ValueError("shape mismatch")
+    if rows is None:
+        out = np.zeros((B, Hq, D), dtype=np.float64)
+        rows_arr, nrows = None, 0
+    else:
+        rows_arr = np.ascontiguousarray(rows, dtype=np.int32).reshape(-1, 2)
+        nrows = rows_arr.shape[0]
+        out = np.zeros((nrows, D), dtype=np.float64)
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    rc = _load().oracle_decode_kv8_f64(
+        out.ctypes.data, q.ctypes.data, k_cache.ctypes.data, v_cache.ctypes.data,
+        bt.ctypes.data_as(i32p), cl.ctypes.data_as(i32p), float(scale), ks.ctypes.data,
+        vs.ctypes.data, B, Hq, Hkv, D, bs, bt.shape[1], NB,
+        rows_arr.ctypes.data_as(i32p) if rows_arr is not None else None, nrows, int(threads))
+    if rc != 0:
+        raise ValueError(f"oracle_decode_kv8_f64 refused the input (status {rc})")
     return out

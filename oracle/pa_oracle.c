@@ -24,7 +24,7 @@
  *   3. out[b][i][d] = sum_t p_t * V_b[t][d].
  *   L_b == 0 gives a zero row.
  *
- * Layouts (row-major, element type f32 or bf16 given by `dtype`):
+ * Layouts (row-major, element type f32, bf16, or float8 e4m3 for the caches):
  *   q       [num_seqs][num_q_heads][head_dim]
  *   k_cache [num_blocks][num_kv_heads][block_size][head_dim]   (v_cache alike)
  *   block_tables int32 [num_seqs][max_blocks_per_seq], context_lens int32 [num_seqs]
@@ -39,7 +39,7 @@
 #include <omp.h>
 #endif
 
-enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_FP8_E4M3 = 2 };
 
 /* bfloat16 is the upper half of an IEEE binary32: widen by a 16-bit shift. */
 static double bf16_bits_to_double(uint16_t bits) {
@@ -49,8 +49,21 @@ static double bf16_bits_to_double(uint16_t bits) {
   return (double)f;
 }
 
+/* float8 e4m3 ("fn" variant): 1 sign bit, 4 exponent bits with bias 7, 3 fraction
+ * bits; no infinities; exponent and fraction all ones is NaN; exponent 0 is
+ * subnormal (fraction * 2^-9). */
+static double e4m3_bits_to_double(uint8_t bits) {
+  const int sign = bits >> 7, e = (bits >> 3) & 15, m = bits & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) v = ldexp((double)m, -9);
+  else v = ldexp(1.0 + m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
 static double load_elem(const void* base, size_t index, int dtype) {
   if (dtype == ORACLE_BF16) return bf16_bits_to_double(((const uint16_t*)base)[index]);
+  if (dtype == ORACLE_FP8_E4M3) return e4m3_bits_to_double(((const uint8_t*)base)[index]);
   return (double)((const float*)base)[index];
 }
 
@@ -64,11 +77,14 @@ void oracle_widen(double* dst, const void* src, long n, int dtype) {
 static int decode_row(double* out_row, const void* q, const void* k_cache, const void* v_cache,
                       const int32_t* block_tables, const int32_t* context_lens, double scale,
                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                      int max_blocks_per_seq, int num_blocks, int dtype, int b, int i) {
+                      int max_blocks_per_seq, int num_blocks, int q_dtype, int kv_dtype,
+                      const double* k_scale, const double* v_scale, int b, int i) {
   const int D = head_dim;
   const int G = num_q_heads / num_kv_heads;
   const int h = i / G;
   const int L = context_lens[b];
+  /* stored K/V codes times the kv head's scale (1 when none is given) */
+  const double ks = k_scale ? k_scale[h] : 1.0, vs = v_scale ? v_scale[h] : 1.0;
   if (L < 0 || (long)L > (long)max_blocks_per_seq * block_size) return -1;
   for (int d = 0; d < D; ++d) out_row[d] = 0.0;
   if (L == 0) return 0;
@@ -90,8 +106,8 @@ static int decode_row(double* out_row, const void* q, const void* k_cache, const
     if (phys < 0 || phys >= num_blocks) { rc = -1; break; }
     const size_t base = (((size_t)phys * num_kv_heads + h) * block_size + offset) * D;
     for (int d = 0; d < D; ++d) {
-      K[(size_t)t * D + d] = load_elem(k_cache, base + d, dtype);
-      V[(size_t)t * D + d] = load_elem(v_cache, base + d, dtype);
+      K[(size_t)t * D + d] = load_elem(k_cache, base + d, kv_dtype) * ks;
+      V[(size_t)t * D + d] = load_elem(v_cache, base + d, kv_dtype) * vs;
     }
   }
 
@@ -101,7 +117,7 @@ static int decode_row(double* out_row, const void* q, const void* k_cache, const
     double smax = -INFINITY;
     for (int t = 0; t < L; ++t) {
       double dot = 0.0;
-      for (int d = 0; d < D; ++d) dot += load_elem(q, qbase + d, dtype) * K[(size_t)t * D + d];
+      for (int d = 0; d < D; ++d) dot += load_elem(q, qbase + d, q_dtype) * K[(size_t)t * D + d];
       s[t] = scale * dot;
       if (s[t] > smax) smax = s[t];
     }
@@ -119,13 +135,12 @@ static int decode_row(double* out_row, const void* q, const void* k_cache, const
   return rc;
 }
 
-/* rows: NULL for every (b, i) row, else num_rows pairs {b, i}.  Returns 0, or
- * the first negative status of any row.  `threads` <= 0 uses every processor. */
-int oracle_decode_f64(double* out, const void* q, const void* k_cache, const void* v_cache,
-                      const int32_t* block_tables, const int32_t* context_lens, double scale,
-                      int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                      int block_size, int max_blocks_per_seq, int num_blocks, int dtype,
-                      const int32_t* rows, int num_rows, int threads) {
+static int decode_rows(double* out, const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, const int32_t* context_lens, double scale,
+                       int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                       int block_size, int max_blocks_per_seq, int num_blocks, int q_dtype,
+                       int kv_dtype, const double* k_scale, const double* v_scale,
+                       const int32_t* rows, int num_rows, int threads) {
   if (num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0)
     return -3;
   const long n = rows ? (long)num_rows : (long)num_seqs * num_q_heads;
@@ -141,7 +156,7 @@ int oracle_decode_f64(double* out, const void* q, const void* k_cache, const voi
     if (b >= 0 && b < num_seqs && i >= 0 && i < num_q_heads)
       rc = decode_row(out + (size_t)r * head_dim, q, k_cache, v_cache, block_tables, context_lens,
                       scale, num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
-                      num_blocks, dtype, b, i);
+                      num_blocks, q_dtype, kv_dtype, k_scale, v_scale, b, i);
     if (rc != 0) {
 #ifdef _OPENMP
 #pragma omp critical
@@ -150,6 +165,33 @@ int oracle_decode_f64(double* out, const void* q, const void* k_cache, const voi
     }
   }
   return status;
+}
+
+/* rows: NULL for every (b, i) row, else num_rows pairs {b, i}.  Returns 0, or
+ * the first negative status of any row.  `threads` <= 0 uses every processor.
+ * q, k_cache and v_cache share `dtype`. */
+int oracle_decode_f64(double* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* context_lens, double scale,
+                      int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                      int block_size, int max_blocks_per_seq, int num_blocks, int dtype,
+                      const int32_t* rows, int num_rows, int threads) {
+  return decode_rows(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                     num_blocks, dtype, dtype, NULL, NULL, rows, num_rows, threads);
+}
+
+/* The same with float8 e4m3 caches: K = code * k_scale[h], V = code * v_scale[h]
+ * for kv head h; q is bf16. */
+int oracle_decode_kv8_f64(double* out, const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, const int32_t* context_lens, double scale,
+                          const double* k_scale, const double* v_scale, int num_seqs,
+                          int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                          int max_blocks_per_seq, int num_blocks, const int32_t* rows,
+                          int num_rows, int threads) {
+  return decode_rows(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_seqs,
+                     num_q_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq,
+                     num_blocks, ORACLE_BF16, ORACLE_FP8_E4M3, k_scale, v_scale, rows, num_rows,
+                     threads);
 }
 
 int oracle_max_threads(void) {

@@ -38,28 +38,50 @@ WORKLOADS = {
                           head_dim=128, block_size=32, lens=("fixed", 131072), std=0.5),
 }
 
+# The same decode workloads with float8 e4m3 K/V pools (q and the new token bf16).
+for _name in ("mha_bf16", "gqa_bf16", "long128k_bf16"):
+    WORKLOADS[_name.replace("bf16", "fp8")] = dict(WORKLOADS[_name], dtype="fp8")
+
 SHARED_PREFIX = dict(seed=1005, dtype="bf16", num_parents=8, children_per_parent=16,
                      prompt_len=2048, parent_extra=(1, 15), tail=(0, 512), num_q_heads=32,
                      num_kv_heads=8, head_dim=128, block_size=16, std=1.0)
 
 
-def to_storage(x: np.ndarray, dtype: str) -> np.ndarray:
-    """float32 samples -> stored form (float32, or bf16 bits as uint16, RNE)."""
+def to_storage(x: np.ndarray, dtype: str, scale=None) -> np.ndarray:
+    """float32 samples -> stored form: float32; bf16 bits as uint16 (RNE); or,
+    for "fp8", e4m3 codes of x / scale[h] (scale per kv head, axis 1 of x),
+    through torch's float8_e4m3fn cast on values kept inside +-448."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     if dtype == "f32":
         return x
     import torch
+    if dtype == "fp8":
+        sc = np.asarray(scale, dtype=np.float32).reshape((1, -1) + (1,) * (x.ndim - 2))
+        y = np.clip(x / sc, -448.0, 448.0)
+        return torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
     return torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
 
 
 def storage_dtype(dtype: str):
-    return np.uint16 if dtype == "bf16" else np.float32
+    return {"bf16": np.uint16, "f32": np.float32, "fp8": np.uint8}[dtype]
+
+
+FP8_NAN = np.uint8(0x7F)
 
 
 def nan_fill(shape, dtype: str) -> np.ndarray:
     if dtype == "bf16":
         return np.full(shape, BF16_NAN, dtype=np.uint16)
+    if dtype == "fp8":
+        return np.full(shape, FP8_NAN, dtype=np.uint8)
     return np.full(shape, np.nan, dtype=np.float32)
+
+
+def fp8_scales(num_kv_heads: int, std: float) -> np.ndarray:
+    """Per-kv-head dequantisation scales of the fp8 workloads: 8 standard
+    deviations map to 448, slightly different for every head."""
+    h = np.arange(num_kv_heads, dtype=np.float64)
+    return (std * 8.0 / 448.0 * (1.0 + h / 16.0)).astype(np.float32)
 
 
 def draw_lengths(rng: np.random.Generator, spec, num_seqs: int) -> np.ndarray:
@@ -111,7 +133,7 @@ class DecodeCase:
 
     def kv_bytes(self) -> int:
         """Bytes of K and V of the valid tokens (what one decode step must read)."""
-        elt = 2 if self.dtype == "bf16" else 4
+        elt = {"bf16": 2, "f32": 4, "fp8": 1}[self.dtype]
         return int(self.context_lens.astype(np.int64).sum()) * 2 * self.num_kv_heads * self.head_dim * elt
 
 
@@ -128,6 +150,10 @@ def make_decode_case(name="custom", *, seed, dtype, num_seqs, num_q_heads, num_k
     """Build a seeded decode case; ``lens`` is a length spec (see ``draw_lengths``)."""
     rng = np.random.Generator(np.random.PCG64(seed))
     B, Hq, Hkv, D, bs = num_seqs, num_q_heads, num_kv_heads, head_dim, block_size
+    # fp8 cases: e4m3 pools with per-kv-head scales; q and the new token in bf16
+    kv_dtype, act_dtype = dtype, ("bf16" if dtype == "fp8" else dtype)
+    ksc = fp8_scales(Hkv, std) if dtype == "fp8" else None
+    vsc = ksc * np.float32(1.25) if dtype == "fp8" else None
     L = draw_lengths(rng, lens, B)
     pages = [(int(l) + bs - 1) // bs for l in L]
     need = int(sum(pages))
@@ -143,19 +169,19 @@ def make_decode_case(name="custom", *, seed, dtype, num_seqs, num_q_heads, num_k
         tables[b, :pages[b]] = perm[cursor - pages[b]:cursor][::-1]
         cursor -= pages[b]
 
-    k_cache = nan_fill((NB, Hkv, bs, D), dtype)
-    v_cache = nan_fill((NB, Hkv, bs, D), dtype)
+    k_cache = nan_fill((NB, Hkv, bs, D), kv_dtype)
+    v_cache = nan_fill((NB, Hkv, bs, D), kv_dtype)
     for b in range(B):
         n_old = max(int(L[b]) - 1, 0)
         if n_old == 0:
             continue
-        kb = to_storage(_draw_normal(rng, (n_old, Hkv, D), std), dtype)
-        vb = to_storage(_draw_normal(rng, (n_old, Hkv, D), std), dtype)
+        kb = to_storage(_draw_normal(rng, (n_old, Hkv, D), std), kv_dtype, ksc)
+        vb = to_storage(_draw_normal(rng, (n_old, Hkv, D), std), kv_dtype, vsc)
         _lay_out_prefix(k_cache, tables[b], kb, bs)
         _lay_out_prefix(v_cache, tables[b], vb, bs)
-    k_new = to_storage(_draw_normal(rng, (B, Hkv, D), std), dtype)
-    v_new = to_storage(_draw_normal(rng, (B, Hkv, D), std), dtype)
-    q = to_storage(_draw_normal(rng, (B, Hq, D), std), dtype)
+    k_new = to_storage(_draw_normal(rng, (B, Hkv, D), std), act_dtype)
+    v_new = to_storage(_draw_normal(rng, (B, Hkv, D), std), act_dtype)
+    q = to_storage(_draw_normal(rng, (B, Hq, D), std), act_dtype)
     slots = np.full(B, -1, dtype=np.int64)
     for b in range(B):
         if L[b] > 0:
@@ -165,7 +191,8 @@ def make_decode_case(name="custom", *, seed, dtype, num_seqs, num_q_heads, num_k
                       head_dim=D, block_size=bs, num_blocks=NB,
                       scale=float(scale) if scale is not None else 1.0 / math.sqrt(D),
                       context_lens=L, block_tables=tables, slot_mapping=slots,
-                      k_cache=k_cache, v_cache=v_cache, k_new=k_new, v_new=v_new, q=q)
+                      k_cache=k_cache, v_cache=v_cache, k_new=k_new, v_new=v_new, q=q,
+                      extra={} if ksc is None else {"k_scale": ksc, "v_scale": vsc})
 
 
 def _lay_out_prefix(pool, table_row, rows, bs):
