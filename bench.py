@@ -42,17 +42,24 @@ DECODE_SOURCES = ["paged_decode.cuh", "decode_launch.cu", "decode_instances.cuh"
 
 
 # ------------------------------------------------------------------ helpers
+def element_sizes(case):
+    """(cache element bytes, q / out / new-token element bytes)."""
+    return {"f32": (4, 4), "bf16": (2, 2), "fp8": (1, 2)}[case.dtype]
+
+
 def algorithmic_bytes(case) -> dict:
-    elt = 2 if case.dtype == "bf16" else 4
+    kv_elt, act_elt = element_sizes(case)
     L = case.context_lens.astype(np.int64)
     B, Hq, Hkv, D, bs = (case.num_seqs, case.num_q_heads, case.num_kv_heads, case.head_dim,
                          case.block_size)
-    kv = int(L.sum()) * 2 * Hkv * D * elt
-    q = B * Hq * D * elt
-    out = B * Hq * D * elt
+    kv = int(L.sum()) * 2 * Hkv * D * kv_elt
+    q = B * Hq * D * act_elt
+    out = B * Hq * D * act_elt
     tables = 4 * (int(((L + bs - 1) // bs).sum()) + B)
-    decode = kv + q + out + tables
-    write = 2 * 2 * B * Hkv * D * elt + 8 * B            # read new k/v, write them, slots
+    scales = 2 * 4 * Hkv if case.dtype == "fp8" else 0
+    decode = kv + q + out + tables + scales
+    # read the new k/v, write them into the pool, the slots (and the scales)
+    write = 2 * B * Hkv * D * (act_elt + kv_elt) + 8 * B + scales
     return dict(kv=kv, decode=decode, write=write, step=decode + write)
 
 
@@ -201,9 +208,14 @@ class GpuStep:
 
     def _init_decode(self, case):
         torch = self.torch
-        bf = case.dtype == "bf16"
+        self.fp8 = case.dtype == "fp8"            # e4m3 pools; q, new token, out bf16
+        bf = case.dtype in ("bf16", "fp8")
         self.case = case
-        self.k_cache, self.v_cache = self._t(case.k_cache, bf), self._t(case.v_cache, bf)
+        self.k_cache = self._t(case.k_cache, bf and not self.fp8)
+        self.v_cache = self._t(case.v_cache, bf and not self.fp8)
+        if self.fp8:
+            self.k_scale = self._t(case.extra["k_scale"])
+            self.v_scale = self._t(case.extra["v_scale"])
         self.k_new, self.v_new = self._t(case.k_new, bf), self._t(case.v_new, bf)
         self.q = self._t(case.q, bf)
         self.slots = self._t(case.slot_mapping)
@@ -270,10 +282,21 @@ class GpuStep:
         pa = self.pa
         if self.pairs is not None:
             pa.pa_copy_blocks(self.k_cache, self.v_cache, self.pairs, device_errors=self.errs)
+        if self.fp8:
+            pa.pa_reshape_and_cache_fp8(self.k_new, self.v_new, self.k_cache, self.v_cache,
+                                        self.slots, self.k_scale, self.v_scale,
+                                        device_errors=self.errs)
+            return
         pa.pa_reshape_and_cache(self.k_new, self.v_new, self.k_cache, self.v_cache, self.slots,
                                 device_errors=self.errs)
 
     def decode(self):
+        if self.fp8:
+            self.pa.pa_decode_fp8(self.out, self.q, self.k_cache, self.v_cache, self.tables,
+                                  self.lens, self.scale, self.k_scale, self.v_scale, self.Hkv,
+                                  self.max_len, workspace=self.workspace,
+                                  chunk_tokens=self.chunk_tokens, device_errors=self.errs)
+            return
         self.pa.pa_decode(self.out, self.q, self.k_cache, self.v_cache, self.tables, self.lens,
                           self.scale, self.Hkv, self.max_len, workspace=self.workspace,
                           chunk_tokens=self.chunk_tokens, device_errors=self.errs)
@@ -352,8 +375,9 @@ def run_gpu(args, world, rank, local):
         "us_per_step": round(ms_per_step * 1e3, 2),
         "steps_per_s": round(world * 1e3 / ms_per_step, 1),
         "hbm_frac_step": round(value / world / peak, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
-        if ws.bf16 else "f32", "data": "synthetic (seeded pa_inputs; no dataset or weights)",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": ("e4m3 K/V (f16 MMA, fp32 accumulate), bf16 q/out" if ws.fp8
+                  else "bf16" if ws.bf16 else "f32"), "data": "synthetic (seeded pa_inputs; no dataset or weights)",
         "config": {
             "workload": args.workload, "num_seqs": ws.case.num_seqs,
             "num_q_heads": ws.case.num_q_heads, "num_kv_heads": ws.case.num_kv_heads,
@@ -467,14 +491,33 @@ def run_e2e(ws, args, torch, pa, device, stream, barrier, world):
 def _oracle_sample(case, n_rows, rng):
     rows = [(int(rng.integers(case.num_seqs)), int(rng.integers(case.num_q_heads)))
             for _ in range(n_rows)]
-    elt = 2 if case.dtype == "bf16" else 4
+    elt, act_elt = element_sizes(case)
     D = case.head_dim
     # bytes the sampled rows stand for: each row reads its sequence's K and V for
     # one head (shared by the GQA group, counted once per group member here is
     # avoided by dividing by the group size), plus its q and out row
     G = case.num_q_heads // case.num_kv_heads
-    nbytes = sum(int(case.context_lens[b]) * 2 * D * elt / G + 2 * D * elt for b, _ in rows)
+    nbytes = sum(int(case.context_lens[b]) * 2 * D * elt / G + 2 * D * act_elt for b, _ in rows)
     return rows, nbytes
+
+
+def _oracle_write(case, kc, vc):
+    import oracle
+    if case.dtype == "fp8":
+        oracle.reshape_and_cache_fp8(case.k_new, case.v_new, kc, vc, case.slot_mapping,
+                                     case.extra["k_scale"], case.extra["v_scale"])
+    else:
+        oracle.reshape_and_cache(case.k_new, case.v_new, kc, vc, case.slot_mapping)
+
+
+def _oracle_decode(case, kc, vc, rows=None):
+    import oracle
+    if case.dtype == "fp8":
+        return oracle.decode_kv8_f64(case.q, kc, vc, case.block_tables, case.context_lens,
+                                     case.scale, case.extra["k_scale"], case.extra["v_scale"],
+                                     rows=rows)
+    return oracle.decode_f64(case.q, kc, vc, case.block_tables, case.context_lens, case.scale,
+                             case.num_kv_heads, case.dtype, rows=rows)
 
 
 def cpu_baseline(case, budget_s=15.0, kind="oracle"):
@@ -490,17 +533,15 @@ def cpu_baseline(case, budget_s=15.0, kind="oracle"):
     # calibrate on a few rows
     rows, _ = _oracle_sample(case, 8, rng)
     t0 = time.perf_counter()
-    oracle.decode_f64(case.q, kc, vc, case.block_tables, case.context_lens, case.scale,
-                      case.num_kv_heads, case.dtype, rows=rows)
+    _oracle_decode(case, kc, vc, rows=rows)
     per_row = (time.perf_counter() - t0) / 8
     step_bytes = algorithmic_bytes(case)["step"]
     if per_row * all_rows <= budget_s:
         steps, elapsed = 0, 0.0
         while steps == 0 or elapsed < budget_s:
             t0 = time.perf_counter()
-            oracle.reshape_and_cache(case.k_new, case.v_new, kc, vc, case.slot_mapping)
-            oracle.decode_f64(case.q, kc, vc, case.block_tables, case.context_lens, case.scale,
-                              case.num_kv_heads, case.dtype)
+            _oracle_write(case, kc, vc)
+            _oracle_decode(case, kc, vc)
             elapsed += time.perf_counter() - t0
             steps += 1
         nbytes, sample = steps * step_bytes, f"{steps} whole {case.name} steps"
@@ -508,8 +549,7 @@ def cpu_baseline(case, budget_s=15.0, kind="oracle"):
         n = int(max(8, budget_s / max(per_row, 1e-9)))
         rows, nbytes = _oracle_sample(case, n, rng)
         t0 = time.perf_counter()
-        oracle.decode_f64(case.q, kc, vc, case.block_tables, case.context_lens, case.scale,
-                          case.num_kv_heads, case.dtype, rows=rows)
+        _oracle_decode(case, kc, vc, rows=rows)
         elapsed = time.perf_counter() - t0
         sample = f"{n} random (sequence, query head) rows of the {case.name} step"
     return {"value": round(nbytes / elapsed / 1e9, 4), "unit": "GB/s", "cores": threads,
@@ -533,8 +573,7 @@ def run_reference(args, world, rank):
     # size a step so K + W steps take about two minutes
     rows, _ = _oracle_sample(case, 4, rng)
     t0 = time.perf_counter()
-    oracle.decode_f64(case.q, kc, vc, case.block_tables, case.context_lens, case.scale,
-                      case.num_kv_heads, case.dtype, rows=rows)
+    _oracle_decode(case, kc, vc, rows=rows)
     per_row = (time.perf_counter() - t0) / 4
     total_steps = args.steps + args.warmup
     n_rows = int(max(1, min(4 * threads, 120.0 / max(total_steps, 1) / max(per_row, 1e-6))))
@@ -542,9 +581,8 @@ def run_reference(args, world, rank):
     elapsed, nbytes_total = 0.0, 0.0
     for i, (rows, nbytes) in enumerate(samples):
         t0 = time.perf_counter()
-        oracle.reshape_and_cache(case.k_new, case.v_new, kc, vc, case.slot_mapping)
-        oracle.decode_f64(case.q, kc, vc, case.block_tables, case.context_lens, case.scale,
-                          case.num_kv_heads, case.dtype, rows=rows)
+        _oracle_write(case, kc, vc)
+        _oracle_decode(case, kc, vc, rows=rows)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             elapsed += dt

@@ -166,6 +166,39 @@ int pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void*
                       int32_t* device_errors, void* stream);
 
 /*
+ * float8 e4m3 KV pools.  "mlx-paged-attention" (future plans) names
+ * quantization as the next optimisation; the pages give no format, so this is
+ * the plainest one: the pools hold one-byte e4m3 codes (1 sign, 4 exponent bits
+ * with bias 7, 3 fraction bits, no infinities, 0x7F/0xFF NaN) and every kv head
+ * h has a fixed dequantisation scale, so the stored K element is
+ * code * k_scale[h] (and V: code * v_scale[h]).  Only head_dim 128 (one
+ * 128-byte row per token) is supported; q, k, v and out are bf16.
+ * k_scale, v_scale: device float32 [num_kv_heads], positive and finite.
+ *
+ * pa_reshape_and_cache_fp8: the cache write of pa_reshape_and_cache, where each
+ * element x of kv head h is stored as e4m3(x / scale[h]): IEEE float32
+ * division, round to nearest (ties to the even code), magnitudes above 448
+ * (and infinities) saturate to +-448, NaN stores a NaN code.
+ *
+ * pa_decode_fp8: pa_decode over such pools, with the same arguments and
+ * workspace (pa_decode_workspace_size with the same sizes).  The kernel uses
+ * the codes as they are and applies K's scale to the logits and V's to the
+ * output; products are computed with q and the probabilities rounded to f16
+ * (every e4m3 value is exactly an f16) and fp32 accumulation.
+ */
+int pa_reshape_and_cache_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
+                             const int64_t* slot_mapping, const float* k_scale,
+                             const float* v_scale, int num_tokens, int num_kv_heads,
+                             int head_dim, int block_size, int num_blocks,
+                             int32_t* device_errors, void* stream);
+int pa_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* context_lens, float scale,
+                  const float* k_scale, const float* v_scale, int num_kv_heads, int num_seqs,
+                  int num_q_heads, int head_dim, int block_size, int num_blocks,
+                  int max_blocks_per_seq, int max_context_len, int chunk_tokens, void* workspace,
+                  size_t workspace_bytes, int32_t* device_errors, void* stream);
+
+/*
  * Test hook for the failure path.  Every pipeline wait of the decode kernels
  * enqueued after this call gives up after `polls` polls (0: at once) and
  * reports PA_DEVERR_TIMEOUT; the kernel then waits for its own copies in flight

@@ -19,7 +19,7 @@ PA_DEVERR_BAD_BLOCK, PA_DEVERR_BAD_LENGTH, PA_DEVERR_BAD_SLOT, PA_DEVERR_TIMEOUT
 EXPORTED_SYMBOLS = [
     "pa_get_error_string", "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_chunk_tokens",
     "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc", "pa_debug_set_wait_limit",
-    "pa_read_device_errors",
+    "pa_read_device_errors", "pa_reshape_and_cache_fp8", "pa_decode_fp8",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq", "pa_bm_append_slot", "pa_bm_fork",
     "pa_bm_free", "pa_bm_block_table", "pa_bm_refcount", "pa_bm_num_free", "pa_bm_free_list",
     "pa_bm_stats", "pa_bm_append_slots", "pa_bm_build_block_tables",
@@ -43,6 +43,10 @@ _SIGNATURES = {
                          _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
     "pa_decode_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _i32, _i32, _i32,
                                  _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _vp]),
+    "pa_reshape_and_cache_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32,
+                                        _i32, _i32, _vp, _vp]),
+    "pa_decode_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _i32, _i32,
+                             _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
     "pa_debug_set_wait_limit": (_i32, [_i32]),
     "pa_read_device_errors": (_i32, [_vp, _pi32, _i32, _vp]),
     "pa_bm_create": (_i32, [_i32, _i32, _pi32, ctypes.POINTER(_vp)]),
@@ -234,6 +238,75 @@ def pa_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens, scal
         int(block_tables.shape[1]), int(max_context_len), _dtype_code(q), int(chunk_tokens),
         _ptr(device_errors), _stream(stream, q.device))
     _check(rc, "pa_decode_noalloc")
+    return out
+
+
+def _need_fp8_pool(name, t):
+    _need_cuda_contig(name, t)
+    if t.element_size() != 1:
+        raise TypeError(f"{name} must hold one-byte e4m3 codes (uint8 or float8_e4m3fn)")
+
+
+def _need_scales(k_scale, v_scale, num_kv_heads):
+    import torch
+    for n, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        _need_cuda_contig(n, t)
+        if t.dtype != torch.float32 or t.numel() != num_kv_heads:
+            raise TypeError(f"{n} must be float32 [num_kv_heads]")
+
+
+def pa_reshape_and_cache_fp8(k, v, k_cache, v_cache, slot_mapping, k_scale, v_scale,
+                             device_errors=None, stream=None):
+    """k, v bf16 [T, Hkv, 128]; caches one-byte e4m3 [NB, Hkv, bs, 128];
+    k_scale, v_scale float32 [Hkv] (see pa.h)."""
+    import torch
+    for n, t in (("k", k), ("v", v), ("slot_mapping", slot_mapping)):
+        _need_cuda_contig(n, t)
+    _need_fp8_pool("k_cache", k_cache)
+    _need_fp8_pool("v_cache", v_cache)
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    if k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise TypeError("k and v must be bf16")
+    NB, Hkv, bs, D = k_cache.shape
+    _need_scales(k_scale, v_scale, Hkv)
+    rc = library().pa_reshape_and_cache_fp8(
+        _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), _ptr(k_scale),
+        _ptr(v_scale), int(k.shape[0]), int(Hkv), int(D), int(bs), int(NB), _ptr(device_errors),
+        _stream(stream, k_cache.device))
+    _check(rc, "pa_reshape_and_cache_fp8")
+
+
+def pa_decode_fp8(out, q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale,
+                  num_kv_heads, max_context_len, workspace=None, chunk_tokens=0,
+                  device_errors=None, stream=None):
+    """pa_decode over e4m3 pools: out, q bf16 [B, Hq, 128]; caches one-byte
+    [NB, Hkv, bs, 128]; k_scale, v_scale float32 [Hkv] (see pa.h)."""
+    import torch
+    for n, t in (("out", out), ("q", q), ("block_tables", block_tables),
+                 ("context_lens", context_lens)):
+        _need_cuda_contig(n, t)
+    _need_fp8_pool("k_cache", k_cache)
+    _need_fp8_pool("v_cache", v_cache)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    if q.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise TypeError("q and out must be bf16")
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    if int(Hkv) != int(num_kv_heads):
+        raise ValueError("num_kv_heads does not match the cache shape")
+    _need_scales(k_scale, v_scale, Hkv)
+    if workspace is None:
+        nbytes = pa_decode_workspace_size(B, Hq, Hkv, D, bs, max_context_len, chunk_tokens)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    rc = library().pa_decode_fp8(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        float(scale), _ptr(k_scale), _ptr(v_scale), int(num_kv_heads), int(B), int(Hq), int(D),
+        int(bs), int(NB), int(block_tables.shape[1]), int(max_context_len), int(chunk_tokens),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(device_errors),
+        _stream(stream, q.device))
+    _check(rc, "pa_decode_fp8")
     return out
 
 

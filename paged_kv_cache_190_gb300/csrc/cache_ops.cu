@@ -2,6 +2,7 @@
 // page copy.  Both are byte moves in 16-byte vectors: one thread per 16-byte
 // chunk of a head row, consecutive threads on consecutive chunks so every warp
 // moves contiguous 512-byte runs.
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -38,6 +39,48 @@ __global__ void __launch_bounds__(256) reshape_and_cache_kernel(
     const int64_t dst = ((page * num_kv_heads + h) * block_size + offset) * chunks_per_row + c;
     k_cache[dst] = k[i];
     v_cache[dst] = v[i];
+  }
+}
+
+// Two quotients x / s (IEEE division) -> two e4m3 codes, round to nearest even,
+// magnitudes past 448 (and infinities) saturated to 448.
+__device__ __forceinline__ uint32_t e4m3x2_div(uint32_t two_bf16, float s) {
+  const float2 f = make_float2(__fdiv_rn(bf16_lo(two_bf16), s), __fdiv_rn(bf16_hi(two_bf16), s));
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(f, __NV_SATFINITE, __NV_E4M3));
+}
+
+// The cache write for float8 e4m3 pools: token t's bf16 row for kv head h is
+// divided by that head's scale and stored as e4m3 codes in the same slot as the
+// bf16 write.  One thread per 8 elements (16 bytes in, 8 bytes out).
+__global__ void __launch_bounds__(256) reshape_and_cache_fp8_kernel(
+    const uint4* __restrict__ k, const uint4* __restrict__ v, uint2* __restrict__ k_cache,
+    uint2* __restrict__ v_cache, const int64_t* __restrict__ slot_mapping,
+    const float* __restrict__ k_scale, const float* __restrict__ v_scale, int num_tokens,
+    int num_kv_heads, int groups_per_row, int block_size, int64_t num_slots,
+    int32_t* device_errors) {
+  const int64_t per_token = static_cast<int64_t>(num_kv_heads) * groups_per_row;
+  const int64_t total = per_token * num_tokens;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = i / per_token;
+    const int64_t rem = i - t * per_token;        // h * groups_per_row + c
+    const int64_t slot = slot_mapping[t];
+    if (slot < 0) continue;                       // padding token
+    if (slot >= num_slots) {
+      if (rem == 0) report(device_errors, PA_DEVERR_BAD_SLOT);
+      continue;
+    }
+    const int64_t page = slot / block_size;
+    const int64_t offset = slot - page * block_size;
+    const int64_t h = rem / groups_per_row;
+    const int64_t c = rem - h * groups_per_row;
+    const int64_t dst = ((page * num_kv_heads + h) * block_size + offset) * groups_per_row + c;
+    const float ks = k_scale[h], vs = v_scale[h];
+    const uint4 a = k[i], b = v[i];
+    k_cache[dst] = make_uint2(e4m3x2_div(a.x, ks) | (e4m3x2_div(a.y, ks) << 16),
+                              e4m3x2_div(a.z, ks) | (e4m3x2_div(a.w, ks) << 16));
+    v_cache[dst] = make_uint2(e4m3x2_div(b.x, vs) | (e4m3x2_div(b.y, vs) << 16),
+                              e4m3x2_div(b.z, vs) | (e4m3x2_div(b.w, vs) << 16));
   }
 }
 
@@ -84,6 +127,25 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache
       static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint4*>(k_cache),
       static_cast<uint4*>(v_cache), slot_mapping, num_tokens, num_kv_heads, chunks_per_row,
       block_size, static_cast<int64_t>(num_blocks) * block_size, device_errors);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reshape_and_cache_fp8(const void* k, const void* v, void* k_cache,
+                                         void* v_cache, const int64_t* slot_mapping,
+                                         const float* k_scale, const float* v_scale,
+                                         int num_tokens, int num_kv_heads, int head_dim,
+                                         int block_size, int num_blocks, int32_t* device_errors,
+                                         cudaStream_t stream) {
+  const int groups_per_row = head_dim / 8;
+  const int64_t total = static_cast<int64_t>(num_tokens) * num_kv_heads * groups_per_row;
+  if (total == 0) return cudaSuccess;
+  const int threads = 256;
+  int64_t blocks = (total + threads - 1) / threads;
+  if (blocks > 65535) blocks = 65535;
+  reshape_and_cache_fp8_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), static_cast<uint2*>(k_cache),
+      static_cast<uint2*>(v_cache), slot_mapping, k_scale, v_scale, num_tokens, num_kv_heads,
+      groups_per_row, block_size, static_cast<int64_t>(num_blocks) * block_size, device_errors);
   return cudaGetLastError();
 }
 

@@ -122,14 +122,18 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
   return pa::decode_workspace_layout(num_seqs, num_q_heads, head_dim, max_context_len, chunk).total;
 }
 
-int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
-              const int32_t* block_tables, const int32_t* context_lens, float scale,
-              int num_kv_heads, int num_seqs, int num_q_heads, int head_dim, int block_size,
-              int num_blocks, int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
-              int chunk_tokens, void* workspace, size_t workspace_bytes,
-              int32_t* device_errors, void* stream) {
-  const int elt = elt_size(dtype);
-  if (!elt || !supported_shape(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
+}  // extern "C"
+
+namespace {
+
+// Shared body of pa_decode and pa_decode_fp8 (kv8: e4m3 caches, bf16 q / out).
+int decode_common(void* out, const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* context_lens, float scale,
+                  int num_kv_heads, int num_seqs, int num_q_heads, int head_dim, int block_size,
+                  int num_blocks, int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
+                  bool kv8, const float* k_scale, const float* v_scale, int chunk_tokens,
+                  void* workspace, size_t workspace_bytes, int32_t* device_errors,
+                  void* stream) {
   if (num_kv_heads <= 0 || num_q_heads <= 0 || num_seqs < 0 || num_blocks <= 0 ||
       max_blocks_per_seq <= 0 || max_context_len < 0)
     return PA_ERR_INVALID_ARG;
@@ -141,6 +145,7 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   if (num_seqs == 0) return PA_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
     return PA_ERR_INVALID_ARG;
+  if (kv8 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
   if (!aligned16(out) || !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
     return PA_ERR_INVALID_ARG;
   const int sms = current_sm_count();
@@ -175,6 +180,9 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   a.max_context_len = max_context_len;
   a.chunk_tokens = chunk;
   a.bf16 = dtype == PA_BF16;
+  a.kv8 = kv8 ? 1 : 0;
+  a.k_scale = kv8 ? k_scale : nullptr;
+  a.v_scale = kv8 ? v_scale : nullptr;
   a.ws.header = reinterpret_cast<int32_t*>(ws);
   a.ws.chunk_base = reinterpret_cast<int32_t*>(ws + lay.chunk_base);
   a.ws.work = reinterpret_cast<int4*>(ws + lay.work);
@@ -185,6 +193,54 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   a.num_sms = sms;
   a.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
   const cudaError_t e = pa::launch_decode(a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache,
+              const int32_t* block_tables, const int32_t* context_lens, float scale,
+              int num_kv_heads, int num_seqs, int num_q_heads, int head_dim, int block_size,
+              int num_blocks, int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
+              int chunk_tokens, void* workspace, size_t workspace_bytes,
+              int32_t* device_errors, void* stream) {
+  if (!elt_size(dtype) || !supported_shape(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
+  return decode_common(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
+                       num_seqs, num_q_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_context_len, dtype, false, nullptr, nullptr,
+                       chunk_tokens, workspace, workspace_bytes, device_errors, stream);
+}
+
+int pa_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* block_tables, const int32_t* context_lens, float scale,
+                  const float* k_scale, const float* v_scale, int num_kv_heads, int num_seqs,
+                  int num_q_heads, int head_dim, int block_size, int num_blocks,
+                  int max_blocks_per_seq, int max_context_len, int chunk_tokens, void* workspace,
+                  size_t workspace_bytes, int32_t* device_errors, void* stream) {
+  if (head_dim != 128 || !supported_shape(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
+  return decode_common(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
+                       num_seqs, num_q_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_context_len, PA_BF16, true, k_scale, v_scale,
+                       chunk_tokens, workspace, workspace_bytes, device_errors, stream);
+}
+
+int pa_reshape_and_cache_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
+                             const int64_t* slot_mapping, const float* k_scale,
+                             const float* v_scale, int num_tokens, int num_kv_heads,
+                             int head_dim, int block_size, int num_blocks,
+                             int32_t* device_errors, void* stream) {
+  if (head_dim != 128 || !supported_shape(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
+  if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!k || !v || !k_cache || !v_cache || !slot_mapping || !k_scale || !v_scale)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARG;
+  const cudaError_t e = pa::launch_reshape_and_cache_fp8(
+      k, v, k_cache, v_cache, slot_mapping, k_scale, v_scale, num_tokens, num_kv_heads, head_dim,
+      block_size, num_blocks, device_errors, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -1,6 +1,6 @@
-// Launch of one instantiation of the persistent decode kernel.  Each element
-// type gets its own translation unit (decode_bf16.cu, decode_f32.cu) so the
-// instantiations compile in parallel.
+// Launch of one instantiation of the persistent decode kernel.  Each cache
+// element type gets its own translation unit (decode_bf16.cu, decode_f32.cu,
+// decode_fp8.cu) so the instantiations compile in parallel.
 #pragma once
 
 #include <atomic>
@@ -9,15 +9,15 @@
 
 namespace pa {
 
-template <bool BF16, int D, int G>
+template <bool BF16, int D, int G, bool KV8 = false>
 cudaError_t run_decode_kernel(const DecodeKernelParams& kp, int grid, int device,
                               cudaStream_t stream) {
-  using Tr = DecodeTraits<BF16, D, G>;
+  using Tr = DecodeTraits<BF16, D, G, KV8>;
   // the opt-in to more than 48 KiB of dynamic shared memory is per device
   static std::atomic<uint64_t> configured{0};
   const uint64_t bit = 1ull << (device & 63);
   if (!(configured.load(std::memory_order_acquire) & bit)) {
-    const cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<BF16, D, G>,
+    const cudaError_t e = cudaFuncSetAttribute(paged_decode_kernel<BF16, D, G, KV8>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                Tr::SMEM_ALLOC);
     if (e != cudaSuccess) return e;
@@ -35,7 +35,7 @@ cudaError_t run_decode_kernel(const DecodeKernelParams& kp, int grid, int device
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, paged_decode_kernel<BF16, D, G>, kp);
+  return cudaLaunchKernelEx(&cfg, paged_decode_kernel<BF16, D, G, KV8>, kp);
 }
 
 template <bool BF16>
@@ -52,6 +52,8 @@ cudaError_t run_decode_dispatch(int head_dim, int group, const DecodeKernelParam
 cudaError_t run_decode_bf16(int head_dim, int group, const DecodeKernelParams& kp, int grid,
                             int device, cudaStream_t stream);
 cudaError_t run_decode_f32(int head_dim, int group, const DecodeKernelParams& kp, int grid,
+                           int device, cudaStream_t stream);
+cudaError_t run_decode_fp8(int head_dim, int group, const DecodeKernelParams& kp, int grid,
                            int device, cudaStream_t stream);
 
 }  // namespace pa

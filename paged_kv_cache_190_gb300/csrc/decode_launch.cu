@@ -283,17 +283,21 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D bf16 view [rows][head_dim] of a K or V pool (rows = blocks * kv heads *
-// block size), boxes of 16 rows x 64 columns (128 bytes) with 128-byte swizzle.
-cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int head_dim, int64_t rows) {
+// 2-D view [rows][head_dim] of a K or V pool (rows = blocks * kv heads * block
+// size) of bf16 or byte (e4m3) elements, boxes of 16 rows x 128 bytes with
+// 128-byte swizzle.
+cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int head_dim, int64_t rows,
+                          int elt) {
   const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (encode == nullptr) return cudaErrorNotSupported;
   if (rows <= 0 || rows > INT_MAX) return cudaErrorInvalidValue;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
-  const cuuint32_t box[2] = {64, 16};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * elt};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elt), 16};
   const cuuint32_t elem_strides[2] = {1, 1};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool), dims,
+  const CUtensorMapDataType type =
+      elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUresult r = encode(map, type, 2, const_cast<void*>(pool), dims,
                             strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -336,10 +340,11 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   DecodeKernelParams kp;
   std::memset(&kp, 0, sizeof(kp));
   const int group = a.num_q_heads / a.num_kv_heads;
-  if (decode_uses_tensor_cores(a.bf16 != 0, group)) {
+  if (a.kv8 || decode_uses_tensor_cores(a.bf16 != 0, group)) {
     const int64_t rows = static_cast<int64_t>(a.num_blocks) * a.num_kv_heads * a.block_size;
-    e = make_pool_map(&kp.tmap_k, a.k_cache, a.head_dim, rows);
-    if (e == cudaSuccess) e = make_pool_map(&kp.tmap_v, a.v_cache, a.head_dim, rows);
+    const int kv_elt = a.kv8 ? 1 : 2;
+    e = make_pool_map(&kp.tmap_k, a.k_cache, a.head_dim, rows, kv_elt);
+    if (e == cudaSuccess) e = make_pool_map(&kp.tmap_v, a.v_cache, a.head_dim, rows, kv_elt);
     if (e != cudaSuccess) return e;
   }
   kp.out = a.out;
@@ -360,13 +365,16 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   kp.part_out = a.ws.part_out;
   kp.device_errors = a.device_errors;
   kp.wait_limit = a.wait_limit < 0 ? kMaxPolls : static_cast<uint32_t>(a.wait_limit);
+  kp.k_scale = a.k_scale;
+  kp.v_scale = a.v_scale;
   const int64_t items_upper = a.ws.max_chunks * a.num_kv_heads;
   const int grid = static_cast<int>(items_upper < a.num_sms ? items_upper : a.num_sms);
   int device = 0;
   e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
-  e = a.bf16 ? run_decode_bf16(a.head_dim, group, kp, grid, device, stream)
-             : run_decode_f32(a.head_dim, group, kp, grid, device, stream);
+  e = a.kv8    ? run_decode_fp8(a.head_dim, group, kp, grid, device, stream)
+      : a.bf16 ? run_decode_bf16(a.head_dim, group, kp, grid, device, stream)
+               : run_decode_f32(a.head_dim, group, kp, grid, device, stream);
   if (e != cudaSuccess) return e;
   if (a.max_context_len > a.chunk_tokens) {
     if (a.bf16 && a.head_dim == 128) e = launch_merge<true, 4>(a, stream);

@@ -37,7 +37,10 @@ struct DecodeArgs {
   float scale;
   int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks;
   int max_blocks_per_seq, max_context_len, chunk_tokens;
-  int bf16;  // element type: 1 bf16, 0 f32
+  int bf16;  // q / out element type: 1 bf16, 0 f32 (and the caches' unless kv8)
+  int kv8;   // caches hold float8 e4m3 codes (q / out bf16)
+  const float* k_scale;  // kv8: dequantisation scale per kv head, device memory
+  const float* v_scale;
   DecodeWorkspace ws;
   int32_t* device_errors;
   int num_sms;
@@ -50,6 +53,13 @@ cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache
                                      const int64_t* slot_mapping, int num_tokens,
                                      int num_kv_heads, int row_bytes, int block_size,
                                      int num_blocks, int32_t* device_errors, cudaStream_t stream);
+
+cudaError_t launch_reshape_and_cache_fp8(const void* k, const void* v, void* k_cache,
+                                         void* v_cache, const int64_t* slot_mapping,
+                                         const float* k_scale, const float* v_scale,
+                                         int num_tokens, int num_kv_heads, int head_dim,
+                                         int block_size, int num_blocks, int32_t* device_errors,
+                                         cudaStream_t stream);
 
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int num_pairs,
                                size_t block_bytes, int num_blocks, int32_t* device_errors,

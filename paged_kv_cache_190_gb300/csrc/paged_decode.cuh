@@ -44,6 +44,8 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -68,19 +70,26 @@ struct ItemDesc {
 // Tensor-core consumer: bf16 with a group of 2..8 query heads per kv head.
 constexpr bool decode_uses_tensor_cores(bool bf16, int group) { return bf16 && group >= 2; }
 
-template <bool BF16, int D, int G>
+// BF16: q, out (and the caches unless KV8) are bf16, else fp32.  KV8: the
+// caches hold float8 e4m3 codes with a scale per kv head (q and out bf16).
+template <bool BF16, int D, int G, bool KV8 = false>
 struct DecodeTraits {
+  static_assert(!KV8 || BF16, "fp8 caches pair with bf16 q and out");
   static constexpr int D_ = D;
   static constexpr int G_ = G;
-  static constexpr bool TC = decode_uses_tensor_cores(BF16, G);
-  static constexpr int ELT = BF16 ? 2 : 4;
-  static constexpr int ROW_BYTES = D * ELT;
+  static constexpr bool KV8_ = KV8;
+  static constexpr bool TC = KV8 || decode_uses_tensor_cores(BF16, G);
+  static constexpr int ELT = KV8 ? 1 : (BF16 ? 2 : 4);         // cache element bytes
+  static constexpr int QELT = BF16 ? 2 : 4;                    // q element bytes
+  static constexpr int ROW_BYTES = D * ELT;                    // one cache row
+  static constexpr int QROW_BYTES = D * QELT;                  // one q row
+  static constexpr int BOX_COLS = 128 / ELT;                   // elements per 128-byte box row
   static constexpr int UT = ROW_BYTES >= 512 ? 8 : 16;          // tokens per stage
   static constexpr int BOXES = ROW_BYTES / 128;                // 128-byte tensor-map boxes per row
   static constexpr int BOX_BYTES = UT * 128;
   static constexpr int TILE_BYTES = UT * ROW_BYTES;            // K (or V) of one stage
   static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int Q_BYTES = G * ROW_BYTES;
+  static constexpr int Q_BYTES = G * QROW_BYTES;
   static constexpr int CE = 16 / ELT;                          // elements per 16-byte chunk
   static constexpr int CPR = ROW_BYTES / 16;                   // chunks per row
   static constexpr int NCH = CPR / 8;                          // chunks per lane in QK
@@ -106,7 +115,8 @@ struct DecodeTraits {
   static constexpr int FIXED = MERGE_ACC + MERGE_ML + PS + QBUF + DESC + TBL + 64 /*flags*/ +
                                (3 * kItemSlots + 4) * 8 + 1024 /*alignment slack*/;
   static constexpr int S_RAW = (kSmemBudget - FIXED) / (STAGE_BYTES + 2 * 8 + 4);
-  static constexpr int S_CAP = S_RAW > 32 ? 32 : S_RAW;
+  static constexpr int S_CAP_MAX = STAGE_BYTES <= 4096 ? 48 : 32;
+  static constexpr int S_CAP = S_RAW > S_CAP_MAX ? S_CAP_MAX : S_RAW;
   static constexpr int S = (S_CAP / kConsumerWarps) * kConsumerWarps;
   static_assert(!TC || (UT == 16 && STAGE_BYTES % 1024 == 0), "swizzled stages need 1 KiB alignment");
   static constexpr int SPW = S / kConsumerWarps;               // stages per consumer warp
@@ -146,6 +156,8 @@ struct DecodeKernelParams {
   float* part_out;
   int32_t* device_errors;
   uint32_t wait_limit;              // polls before a pipeline wait gives up (drains use kMaxPolls)
+  const float* k_scale;             // fp8 caches: dequantisation scale per kv head
+  const float* v_scale;
 };
 
 // Butterfly step over lane bit `mask` (within 8-lane groups): lanes with the
@@ -293,14 +305,14 @@ struct CoreConsumer {
     ps = ps_;
   }
 
-  __device__ __forceinline__ void begin(const char* qs, float scale_log2) {
+  __device__ __forceinline__ void begin(const char* qs, float scale_log2, float) {
     // q scaled so that logits come out in base 2
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
       for (int c = 0; c < Tr::NCH; ++c) {
         const uint4 raw =
-            *reinterpret_cast<const uint4*>(qs + g * Tr::ROW_BYTES + (r + 8 * c) * 16);
+            *reinterpret_cast<const uint4*>(qs + g * Tr::QROW_BYTES + (r + 8 * c) * 16);
         unpack_chunk<Tr>(raw, &qf[g][c * Tr::CE]);
 #pragma unroll
         for (int e = 0; e < Tr::CE; ++e) qf[g][c * Tr::CE + e] *= scale_log2;
@@ -462,16 +474,16 @@ struct TensorConsumer {
 
   __device__ __forceinline__ void init(int lane_, float*) { lane = lane_; }
 
-  __device__ __forceinline__ void begin(const char* qs, float) {
+  __device__ __forceinline__ void begin(const char* qs, float, float) {
     const int g = lane >> 2, c = lane & 3;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
       qa[ks][0] = 0u;
       qa[ks][1] = 0u;
       if (g < G) {
-        qa[ks][0] = *reinterpret_cast<const uint32_t*>(qs + g * Tr::ROW_BYTES + (16 * ks + 2 * c) * 2);
+        qa[ks][0] = *reinterpret_cast<const uint32_t*>(qs + g * Tr::QROW_BYTES + (16 * ks + 2 * c) * 2);
         qa[ks][1] =
-            *reinterpret_cast<const uint32_t*>(qs + g * Tr::ROW_BYTES + (16 * ks + 8 + 2 * c) * 2);
+            *reinterpret_cast<const uint32_t*>(qs + g * Tr::QROW_BYTES + (16 * ks + 8 + 2 * c) * 2);
       }
     }
     m = -INFINITY;
@@ -560,11 +572,164 @@ struct TensorConsumer {
   }
 };
 
-template <bool BF16, int D, int G>
+// ------------------------------------------------------------ fp8 consumer
+// f16 operands of one m16n8k16 tile, fp32 accumulation.
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Two e4m3 codes (low byte first) -> two f16 (exact: every e4m3 value is an f16).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  const __half2_raw h =
+      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Tensor-core consumer for float8 e4m3 pools (any group 1..8).  The same two
+// products as TensorConsumer, with f16 operands: e4m3 -> f16 is exact, q and P
+// are rounded to f16.  The stored codes are used as they are; the kv head's
+// scales are applied outside the loop (K's in the score scale, V's when the
+// item's state is handed over).
+//   Scores: one 16-byte chunk of a K row is one k-step of 16 head_dim columns;
+//   ldmatrix gives lane t the 4 codes d = 4 (t % 4) .. +3 of token t / 4, so the
+//   k order inside a step is permuted the same way for q (a bijection on the
+//   step's columns, which the sum does not see).
+//   Values: ldmatrix.trans on code pairs gives lane t, for tokens 2 (t % 4) and
+//   +1, the codes of columns 2 (t / 4) and 2 (t / 4) + 1; the first feeds O^T
+//   row t / 4, the second row t / 4 + 8, so an m-tile covers one 16-column chunk
+//   with its rows in the order 0, 2, .., 14, 1, 3, .., 15.
+template <typename Tr>
+struct Fp8TensorConsumer {
+  static constexpr int G = Tr::G_, D = Tr::D_;
+  static constexpr int KS = D / 16;     // k-steps (16-byte chunks of a K row)
+  static constexpr int MT = D / 16;     // O^T m-tiles (16-byte chunks of a V row)
+  uint32_t qa[KS][2];                   // f16x2 q fragments (row t/4; columns 4c..4c+1, 4c+2..4c+3)
+  float o[MT][4];
+  float m, l, vscale;
+  int lane;
+
+  __device__ __forceinline__ void init(int lane_, float*) { lane = lane_; }
+
+  __device__ __forceinline__ void begin(const char* qs, float, float v_scale) {
+    const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qa[ks][0] = 0u;
+      qa[ks][1] = 0u;
+      if (g < G) {
+        const uint2 w = *reinterpret_cast<const uint2*>(qs + g * Tr::QROW_BYTES + (16 * ks + 4 * c) * 2);
+        qa[ks][0] = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));
+        qa[ks][1] = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));
+      }
+    }
+    m = -INFINITY;
+    l = 0.f;
+    vscale = v_scale;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  }
+
+  template <typename Release>
+  __device__ __forceinline__ void unit(const char* kt, const char* vt, int nt, float score_scale,
+                                       Release release) {
+    const uint32_t kb = smem_addr(kt), vb = smem_addr(vt);
+    const int mi = lane >> 3, r8 = lane & 7, c = lane & 3;
+    uint32_t kr[KS][2], vr[MT][2];      // raw codes: [step][n-tile] and [m-tile][token half]
+#pragma unroll
+    for (int j = 0; j < KS / 2; ++j)    // tokens 0-7 / 8-15 x chunks 2j, 2j+1
+      ldsm_x4(kb + swz<Tr>((mi >> 1) * 8 + r8, 2 * j + (mi & 1)), kr[2 * j][0], kr[2 * j + 1][0],
+              kr[2 * j][1], kr[2 * j + 1][1]);
+#pragma unroll
+    for (int j = 0; j < MT / 2; ++j)    // chunks 2j, 2j+1 x tokens 0-7 / 8-15
+      ldsm_x4_trans(vb + swz<Tr>((mi & 1) * 8 + r8, 2 * j + (mi >> 1)), vr[2 * j][0], vr[2 * j][1],
+                    vr[2 * j + 1][0], vr[2 * j + 1][1]);
+    release();
+    // ---- scores
+    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      mma_f16(s0, qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_f16x2(kr[ks][0]),
+              e4m3x2_to_f16x2(kr[ks][0] >> 16));
+      mma_f16(s1, qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_f16x2(kr[ks][1]),
+              e4m3x2_to_f16x2(kr[ks][1] >> 16));
+    }
+    float sv[4] = {s0[0], s0[1], s1[0], s1[1]};
+    const int tk[4] = {2 * c, 2 * c + 1, 8 + 2 * c, 9 + 2 * c};
+    float mx = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      sv[e] = tk[e] < nt ? sv[e] * score_scale : -INFINITY;
+      mx = fmaxf(mx, sv[e]);
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
+    const float mn = fmaxf(m, mx);
+    const float alpha = fast_exp2(m - mn);
+    m = mn;
+    float pr[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pr[e] = fast_exp2(sv[e] - mn);
+    l = l * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
+    const uint32_t pb0 = pack_f16x2(pr[0], pr[1]);
+    const uint32_t pb1 = pack_f16x2(pr[2], pr[3]);
+    const float a_even = __shfl_sync(kFull, alpha, 8 * c);
+    const float a_odd = __shfl_sync(kFull, alpha, 8 * c + 4);
+    // ---- values: codes (token 2c: cols 2g, 2g+1 | token 2c+1: cols 2g, 2g+1)
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      o[mt][0] *= a_even;
+      o[mt][1] *= a_odd;
+      o[mt][2] *= a_even;
+      o[mt][3] *= a_odd;
+      const uint32_t a0 = e4m3x2_to_f16x2(__byte_perm(vr[mt][0], 0u, 0x0020));   // col 2g
+      const uint32_t a1 = e4m3x2_to_f16x2(__byte_perm(vr[mt][0], 0u, 0x0031));   // col 2g+1
+      const uint32_t a2 = e4m3x2_to_f16x2(__byte_perm(vr[mt][1], 0u, 0x0020));
+      const uint32_t a3 = e4m3x2_to_f16x2(__byte_perm(vr[mt][1], 0u, 0x0031));
+      mma_f16(o[mt], a0, a1, a2, a3, pb0, pb1);
+    }
+  }
+
+  __device__ __forceinline__ void store(float* macc_w, float* mml_w) {
+    float lt = l + __shfl_xor_sync(kFull, l, 1);
+    lt += __shfl_xor_sync(kFull, lt, 2);
+    const int g = lane >> 2, c = lane & 3;
+    if (g < G && c == 0) {
+      mml_w[g * 2 + 0] = m;
+      mml_w[g * 2 + 1] = lt;
+    }
+    const int h0 = 2 * c, h1 = 2 * c + 1;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int d0 = 16 * mt + 2 * g, d1 = d0 + 1;     // O^T rows g and g + 8
+      if (h0 < G) {
+        macc_w[h0 * D + d0] = o[mt][0] * vscale;
+        macc_w[h0 * D + d1] = o[mt][2] * vscale;
+      }
+      if (h1 < G) {
+        macc_w[h1 * D + d0] = o[mt][1] * vscale;
+        macc_w[h1 * D + d1] = o[mt][3] * vscale;
+      }
+    }
+  }
+};
+
+template <bool BF16, int D, int G, bool KV8>
 __global__ void __launch_bounds__(kDecodeThreads, 1)
     paged_decode_kernel(const __grid_constant__ DecodeKernelParams p) {
-  using Tr = DecodeTraits<BF16, D, G>;
-  using Consumer = typename std::conditional<Tr::TC, TensorConsumer<Tr>, CoreConsumer<Tr>>::type;
+  using Tr = DecodeTraits<BF16, D, G, KV8>;
+  using Consumer = typename std::conditional<
+      KV8, Fp8TensorConsumer<Tr>,
+      typename std::conditional<Tr::TC, TensorConsumer<Tr>, CoreConsumer<Tr>>::type>::type;
   constexpr int S = Tr::S;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // swizzled tensor-map copies need 1 KiB-aligned stages
@@ -688,7 +853,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         mbar_arrive_expect_tx(&item_full[slot], Tr::Q_BYTES);
         const char* qsrc =
             p.q + (static_cast<int64_t>(w.x) * p.num_q_heads + static_cast<int64_t>(h) * G) *
-                      Tr::ROW_BYTES;
+                      Tr::QROW_BYTES;
         bulk_g2s(qbuf + slot * Tr::Q_BYTES, qsrc, Tr::Q_BYTES, &item_full[slot]);
       }
       ++q_issued;
@@ -755,9 +920,9 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
               if constexpr (Tr::TC) {
 #pragma unroll
                 for (int bx = 0; bx < Tr::BOXES; ++bx) {
-                  tma_load_2d(dst + bx * Tr::BOX_BYTES, &p.tmap_k, bx * 64, static_cast<int>(row),
+                  tma_load_2d(dst + bx * Tr::BOX_BYTES, &p.tmap_k, bx * Tr::BOX_COLS, static_cast<int>(row),
                               &full[s]);
-                  tma_load_2d(dst + Tr::TILE_BYTES + bx * Tr::BOX_BYTES, &p.tmap_v, bx * 64,
+                  tma_load_2d(dst + Tr::TILE_BYTES + bx * Tr::BOX_BYTES, &p.tmap_v, bx * Tr::BOX_COLS,
                               static_cast<int>(row), &full[s]);
                 }
               } else {
@@ -817,7 +982,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     const ItemDesc d = desc[slot];
     if (d.b < 0 || *abort_flag) break;
-    cs.begin(qbuf + slot * Tr::Q_BYTES, p.scale_log2);
+    // fp8 caches: K's head scale folds into the score scale, V's into the output
+    const float kv_k = KV8 ? p.k_scale[d.h] : 1.f, kv_v = KV8 ? p.v_scale[d.h] : 1.f;
+    const float item_scale = p.scale_log2 * kv_k;
+    cs.begin(qbuf + slot * Tr::Q_BYTES, item_scale, kv_v);
     __syncwarp();
     if (lane == 0) mbar_arrive(&item_empty[slot]);
 
@@ -848,7 +1016,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
             __syncwarp();
           }
         }
-        cs.unit(kt, vt, nt, p.scale_log2, [&] {
+        cs.unit(kt, vt, nt, item_scale, [&] {
           if constexpr (Tr::TC) {
             // order this warp's generic-proxy writes before the next tensor copy here
             if (nt < Tr::UT) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

@@ -16,6 +16,7 @@ pytestmark = pytest.mark.gpu
 CASES = [
     ("gqa_bf16", dict(B=12)),          # tensor-core consumer, tensor-map copies
     ("tiny_fp32", dict()),             # CUDA-core consumer, bulk copies
+    ("gqa_fp8", dict(B=12)),           # e4m3 pools: f16 tensor-core consumer
 ]
 
 
