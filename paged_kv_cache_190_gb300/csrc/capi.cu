@@ -188,6 +188,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   a.ws.work = reinterpret_cast<int4*>(ws + lay.work);
   a.ws.part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
   a.ws.part_out = reinterpret_cast<float*>(ws + lay.part_out);
+  a.ws.q8 = reinterpret_cast<unsigned char*>(ws + lay.q8);
   a.ws.max_chunks = lay.max_chunks;
   a.device_errors = device_errors;
   a.num_sms = sms;

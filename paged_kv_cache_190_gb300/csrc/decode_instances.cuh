@@ -27,7 +27,7 @@ cudaError_t run_decode_kernel(const DecodeKernelParams& kp, int grid, int device
   // kernel finishes and wait for it on the device
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kDecodeThreads);
+  cfg.blockDim = dim3(Tr::THREADS);
   cfg.dynamicSmemBytes = Tr::SMEM_ALLOC;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

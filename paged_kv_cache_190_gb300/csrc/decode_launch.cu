@@ -2,6 +2,8 @@
 // -> split-K merge kernel, all on the caller's stream.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <climits>
@@ -16,6 +18,45 @@ namespace pa {
 namespace {
 
 constexpr int kPlanThreads = 1024;
+constexpr int kQPrepWarps = 8;
+
+// q preparation of the fp8-cache decode (head_dim 128): each bf16 row q[b][i]
+// is scaled by the power of two 2^e that brings its largest magnitude into
+// [128, 256) and split into e4m3 hi = e4m3(x 2^e) and lo = e4m3(x 2^e - hi)
+// (nearest, saturating).  Output row (272 bytes): hi codes [128], lo codes
+// [128], 2^-e as float32, 12 bytes of padding.  One warp per row, four
+// columns per lane.
+__global__ void __launch_bounds__(kQPrepWarps * 32) q_prep_fp8_kernel(
+    const uint2* __restrict__ q, unsigned char* __restrict__ q8, int64_t rows) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kQPrepWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const uint2 w = q[row * 32 + lane];
+  float x[4] = {bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y)};
+  float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu);
+  const int se = min(max(134 - e, -126), 126);            // amax 2^se in [128, 256)
+  const float up = __uint_as_float(static_cast<uint32_t>(se + 127) << 23);
+  uint32_t hi = 0, lo = 0;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float2 v = make_float2(x[2 * j] * up, x[2 * j + 1] * up);
+    const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3);
+    const float2 back = __half22float2(static_cast<__half2>(__nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3)));
+    const float2 r = make_float2(v.x - back.x, v.y - back.y);
+    const __nv_fp8x2_storage_t l = __nv_cvt_float2_to_fp8x2(r, __NV_SATFINITE, __NV_E4M3);
+    hi |= static_cast<uint32_t>(h) << (16 * j);
+    lo |= static_cast<uint32_t>(l) << (16 * j);
+  }
+  unsigned char* dst = q8 + row * 272;
+  reinterpret_cast<uint32_t*>(dst)[lane] = hi;
+  reinterpret_cast<uint32_t*>(dst + 128)[lane] = lo;
+  if (lane < 4)
+    reinterpret_cast<float*>(dst + 256)[lane] =
+        lane == 0 ? __uint_as_float(static_cast<uint32_t>(127 - se) << 23) : 0.f;
+}
 
 // Lists every (sequence, chunk) pair in sequence order, records where each
 // sequence's chunks start, resets the work counter and writes zero rows for
@@ -283,21 +324,26 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// 2-D view [rows][head_dim] of a K or V pool (rows = blocks * kv heads * block
-// size) of bf16 or byte (e4m3) elements, boxes of 16 rows x 128 bytes with
-// 128-byte swizzle.
+// View of a K or V pool (rows = blocks * kv heads * block size, bf16 or byte
+// (e4m3) elements) for copies of box_rows whole rows with 128-byte swizzle: 2-D
+// {128 bytes, rows} when a row is 128 bytes; otherwise 3-D {128 bytes, rows,
+// 128-byte slabs of a row}, so that one box takes every slab of the rows and
+// lands them slab after slab (the layout the consumers read).
 cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int head_dim, int64_t rows,
-                          int elt) {
+                          int elt, int box_rows) {
   const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (encode == nullptr) return cudaErrorNotSupported;
   if (rows <= 0 || rows > INT_MAX) return cudaErrorInvalidValue;
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * elt};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / elt), 16};
-  const cuuint32_t elem_strides[2] = {1, 1};
+  const int row_bytes = head_dim * elt;
+  if (row_bytes % 128 != 0) return cudaErrorInvalidValue;
+  const cuuint32_t slabs = static_cast<cuuint32_t>(row_bytes / 128);
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(128 / elt), static_cast<cuuint64_t>(rows), slabs};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes), 128};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elt), static_cast<cuuint32_t>(box_rows), slabs};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
   const CUtensorMapDataType type =
       elt == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const CUresult r = encode(map, type, 2, const_cast<void*>(pool), dims,
+  const CUresult r = encode(map, type, slabs == 1 ? 2 : 3, const_cast<void*>(pool), dims,
                             strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -322,6 +368,8 @@ WorkspaceLayout decode_workspace_layout(int num_seqs, int num_q_heads, int head_
   off += align256(static_cast<size_t>(w.max_chunks) * num_q_heads * 4);
   w.part_out = off;
   off += align256(static_cast<size_t>(w.max_chunks) * num_q_heads * head_dim * 4);
+  w.q8 = off;                             // the fp8-cache path's prepared q rows
+  off += align256(static_cast<size_t>(num_seqs) * num_q_heads * (2 * head_dim + 16));
   w.total = off;
   return w;
 }
@@ -329,6 +377,14 @@ WorkspaceLayout decode_workspace_layout(int num_seqs, int num_q_heads, int head_
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.num_seqs == 0) return cudaSuccess;
   const int elt = a.bf16 ? 2 : 4;
+  if (a.kv8) {
+    const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
+    q_prep_fp8_kernel<<<static_cast<unsigned>((rows + kQPrepWarps - 1) / kQPrepWarps),
+                        kQPrepWarps * 32, 0, stream>>>(static_cast<const uint2*>(a.q), a.ws.q8,
+                                                       rows);
+    const cudaError_t qe = cudaGetLastError();
+    if (qe != cudaSuccess) return qe;
+  }
   const int64_t row_chunks = static_cast<int64_t>(a.num_q_heads) * a.head_dim * elt / 16;
   decode_plan_kernel<<<1, kPlanThreads, 0, stream>>>(
       a.context_lens, a.num_seqs, a.chunk_tokens, a.max_context_len, a.ws.header,
@@ -343,12 +399,17 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.kv8 || decode_uses_tensor_cores(a.bf16 != 0, group)) {
     const int64_t rows = static_cast<int64_t>(a.num_blocks) * a.num_kv_heads * a.block_size;
     const int kv_elt = a.kv8 ? 1 : 2;
-    e = make_pool_map(&kp.tmap_k, a.k_cache, a.head_dim, rows, kv_elt);
-    if (e == cudaSuccess) e = make_pool_map(&kp.tmap_v, a.v_cache, a.head_dim, rows, kv_elt);
+    // one box per page a unit touches: min(page, unit) rows
+    const int unit_tokens =
+        a.kv8 ? DecodeTraits<true, 128, 4, true>::UT : DecodeTraits<true, 128, 4, false>::UT;
+    const int box_rows = a.block_size < unit_tokens ? a.block_size : unit_tokens;
+    e = make_pool_map(&kp.tmap_k, a.k_cache, a.head_dim, rows, kv_elt, box_rows);
+    if (e == cudaSuccess)
+      e = make_pool_map(&kp.tmap_v, a.v_cache, a.head_dim, rows, kv_elt, box_rows);
     if (e != cudaSuccess) return e;
   }
   kp.out = a.out;
-  kp.q = static_cast<const char*>(a.q);
+  kp.q = a.kv8 ? reinterpret_cast<const char*>(a.ws.q8) : static_cast<const char*>(a.q);
   kp.k_cache = static_cast<const char*>(a.k_cache);
   kp.v_cache = static_cast<const char*>(a.v_cache);
   kp.block_tables = a.block_tables;

@@ -16,11 +16,12 @@ struct DecodeWorkspace {
   int4* work;            // [max_chunks] {b, chunk index, length, global chunk}
   float* part_lse;       // [max_chunks][num_q_heads] base-2 log-sum-exp of a chunk
   float* part_out;       // [max_chunks][num_q_heads][head_dim] chunk output, normalised
+  unsigned char* q8;     // fp8 caches: [num_seqs * num_q_heads][2 * head_dim + 16] prepared q
   int64_t max_chunks;
 };
 
 struct WorkspaceLayout {
-  size_t chunk_base, work, part_lse, part_out, total;
+  size_t chunk_base, work, part_lse, part_out, q8, total;
   int64_t max_chunks;
 };
 

@@ -11,30 +11,37 @@
 //   * Work item = (sequence, kv head, chunk of `chunk_tokens` tokens).  A tiny
 //     plan kernel lists the (sequence, chunk) pairs; items are handed out by an
 //     atomic counter, so lognormal lengths balance across SMs.
-//   * One CTA per SM, persistent, ten warps.  Warp 9 schedules: it claims items
-//     and resolves them (work entry, block-table slice) into shared item slots.
-//     Warp 8 produces: it copies the GQA group's q rows into shared memory and
-//     streams 16-token K and V tiles into a ring of stages guarded by
-//     mbarriers -- eight lanes issuing at once, lane w feeding consumer warp w,
-//     because a single issuing thread cannot keep HBM busy.  Tiles move with
-//     cp.async.bulk (one contiguous run per tile) or, for the tensor-core
-//     consumer, with cp.async.bulk.tensor through a 2-D tensor map with 128-byte
-//     swizzle so that ldmatrix reads them without bank conflicts.
-//   * Warps 0..7 consume.  Unit u (16 tokens) of item i goes to warp
-//     (u + i) % 8, through that warp's own sub-ring of S / 8 stages (stage
-//     w + 8 k).  The split of an item between warps is therefore a function of
-//     the item alone, which makes the result bit-reproducible whatever CTA runs
-//     it.  Each warp keeps an online-softmax state (running max m, sum l,
-//     accumulator) in fp32 registers for every query head of the GQA group --
-//     one K/V read serves the whole group.  Two consumers:
+//   * One CTA per SM, persistent.  The last warp schedules: it claims items and
+//     resolves them (work entry, block-table slice) into shared item slots and
+//     starts the copy of each item's q rows.  The warp before it produces: lane
+//     w streams the K and V tiles of consumer warp w's units into that warp's
+//     ring of stages (mbarrier-guarded), with blocking waits of its own, so the
+//     lanes advance independently and several copies are in issue at once (a
+//     single issuing thread cannot keep HBM busy).  Tiles move with
+//     cp.async.bulk (one contiguous run per tile) for the CUDA-core consumer,
+//     or with cp.async.bulk.tensor through a tensor map with 128-byte swizzle
+//     (so that ldmatrix reads them without bank conflicts) for the tensor-core
+//     consumers: one box per page touched and pool, taking every 128-byte slab
+//     of its rows (a 3-D box when a row is wider than 128 bytes) -- the number
+//     of copies per byte, not their size, limits one issuing warp.
+//   * The other warps consume.  Unit u (16 tokens; 32 for e4m3 pools) of item i
+//     goes to warp (u + i) % CW, through that warp's own ring of S / CW stages
+//     (stage w + CW k).  The split of an item between warps is therefore a
+//     function of the item alone, which makes the result bit-reproducible
+//     whatever CTA runs it.  Each warp keeps an online-softmax state (running
+//     max m, sum l, accumulator) in fp32 registers for every query head of the
+//     GQA group -- one K/V read serves the whole group.  Three consumers:
 //       - CUDA cores (fp32 inputs, and bf16 with one query head per kv head):
 //         QK with 8 lanes per token and a butterfly reduction, PV with each
 //         lane owning head_dim / 32 output columns;
-//       - tensor cores (bf16, 2..8 query heads per kv head): mma.sync
+//       - tensor cores, bf16 (2..8 query heads per kv head): mma.sync
 //         m16n8k16 with the group's q rows as the A operand (rows past the
 //         group are zero), K through ldmatrix, P re-packed from the score
-//         fragments as the next A operand, V through ldmatrix.trans.
-//   * At the end of an item the 8 partial states are merged through shared
+//         fragments as the next B operand, V through ldmatrix.trans;
+//       - tensor cores, float8 e4m3 pools (any group): mma.sync m16n8k32 with
+//         e4m3 operands, so the stored codes enter the products unconverted
+//         (see Fp8TensorConsumer).
+//   * At the end of an item the partial states are merged through shared
 //     memory (log-sum-exp) and the item's rows are written either straight to
 //     `out` (single-chunk sequence) or as a normalised partial plus its base-2
 //     log-sum-exp for the split-K merge kernel.
@@ -56,10 +63,9 @@
 
 namespace pa {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 8;    // consumer warps of the bf16 / fp32 kernels
 constexpr int kItemSlots = 8;        // items the producer may run ahead
 constexpr int kUnitsAhead = 32;      // claimed-but-unissued units a CTA may hold
-constexpr int kDecodeThreads = (kConsumerWarps + 2) * 32;   // + producer + scheduler
 constexpr int kSmemBudget = 227 * 1024;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -79,12 +85,19 @@ struct DecodeTraits {
   static constexpr int G_ = G;
   static constexpr bool KV8_ = KV8;
   static constexpr bool TC = KV8 || decode_uses_tensor_cores(BF16, G);
+  // Consumer warps: the fp8 kernel keeps 6 so that the CTA's 8 warps get up to
+  // 255 registers each (9 or more warps put 3 on some SM sub-partitions, which
+  // caps a thread at 168).
+  static constexpr int CW = KV8 ? 6 : kConsumerWarps;
+  static constexpr int THREADS = (CW + 2) * 32;                // + producer + scheduler
   static constexpr int ELT = KV8 ? 1 : (BF16 ? 2 : 4);         // cache element bytes
   static constexpr int QELT = BF16 ? 2 : 4;                    // q element bytes
   static constexpr int ROW_BYTES = D * ELT;                    // one cache row
-  static constexpr int QROW_BYTES = D * QELT;                  // one q row
+  // one q row; fp8 caches: the row prepared as e4m3 hi and lo parts plus its
+  // inverse scale (see Fp8TensorConsumer)
+  static constexpr int QROW_BYTES = KV8 ? 2 * D + 16 : D * QELT;
   static constexpr int BOX_COLS = 128 / ELT;                   // elements per 128-byte box row
-  static constexpr int UT = ROW_BYTES >= 512 ? 8 : 16;          // tokens per stage
+  static constexpr int UT = KV8 ? 32 : (ROW_BYTES >= 512 ? 8 : 16);   // tokens per stage
   static constexpr int BOXES = ROW_BYTES / 128;                // 128-byte tensor-map boxes per row
   static constexpr int BOX_BYTES = UT * 128;
   static constexpr int TILE_BYTES = UT * ROW_BYTES;            // K (or V) of one stage
@@ -106,9 +119,9 @@ struct DecodeTraits {
   static_assert(D % 32 == 0, "head_dim must split over 32 lanes");
 
   // shared memory carve-up (bytes)
-  static constexpr int MERGE_ACC = kConsumerWarps * G * D * 4;
-  static constexpr int MERGE_ML = kConsumerWarps * G * 2 * 4;
-  static constexpr int PS = TC ? 0 : kConsumerWarps * UT * G * 4;   // CUDA-core probabilities
+  static constexpr int MERGE_ACC = CW * G * D * 4;
+  static constexpr int MERGE_ML = CW * G * 2 * 4;
+  static constexpr int PS = TC ? 0 : CW * UT * G * 4;   // CUDA-core probabilities
   static constexpr int QBUF = kItemSlots * Q_BYTES;
   static constexpr int DESC = kItemSlots * static_cast<int>(sizeof(ItemDesc));
   static constexpr int TBL = kItemSlots * 32 * 4;              // block-table slice per item
@@ -117,10 +130,11 @@ struct DecodeTraits {
   static constexpr int S_RAW = (kSmemBudget - FIXED) / (STAGE_BYTES + 2 * 8 + 4);
   static constexpr int S_CAP_MAX = STAGE_BYTES <= 4096 ? 48 : 32;
   static constexpr int S_CAP = S_RAW > S_CAP_MAX ? S_CAP_MAX : S_RAW;
-  static constexpr int S = (S_CAP / kConsumerWarps) * kConsumerWarps;
-  static_assert(!TC || (UT == 16 && STAGE_BYTES % 1024 == 0), "swizzled stages need 1 KiB alignment");
-  static constexpr int SPW = S / kConsumerWarps;               // stages per consumer warp
-  static_assert(S >= kConsumerWarps, "at least one stage per consumer warp");
+  static constexpr int S = (S_CAP / CW) * CW;
+  static_assert(!TC || (UT % 16 == 0 && STAGE_BYTES % 1024 == 0),
+                "swizzled stages need 1 KiB alignment");
+  static constexpr int SPW = S / CW;               // stages per consumer warp
+  static_assert(S >= CW, "at least one stage per consumer warp");
 
   static constexpr int OFF_STAGES = 0;
   static constexpr int OFF_QBUF = OFF_STAGES + S * STAGE_BYTES;
@@ -225,6 +239,28 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
       " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
       : "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Rows [row, row + rows) of a K or V pool into a stage tile: one tensor-map box
+// of every 128-byte column slab of the rows (a 3-D box {128 B, rows, slabs}
+// when a row is wider than 128 bytes: one copy lands all slabs, slab b at
+// b * UT * 128 bytes).
+template <typename Tr>
+__device__ __forceinline__ void tma_rows(void* smem_dst, const CUtensorMap* map, int row,
+                                         uint64_t* bar) {
+  if constexpr (Tr::BOXES == 1)
+    tma_load_2d(smem_dst, map, 0, row, bar);
+  else
+    tma_load_3d(smem_dst, map, 0, row, 0, bar);
 }
 
 // Byte offset of (row, 16-byte chunk) inside a tile stored as 128-byte-wide boxes
@@ -573,129 +609,202 @@ struct TensorConsumer {
 };
 
 // ------------------------------------------------------------ fp8 consumer
-// f16 operands of one m16n8k16 tile, fp32 accumulation.
-__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                        uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+// e4m3 operands of one m16n8k32 tile, fp32 accumulation.  A: row-major 16 x 32
+// (a0: row r, columns 4c..4c+3; a1: row r + 8; a2, a3: columns + 16), B:
+// column-major 32 x 8 (b0: rows 4c..4c+3 of column r; b1: rows + 16), where
+// r = lane / 4 and c = lane % 4; bytes in increasing column (row) order.
+__device__ __forceinline__ void mma_e4m3(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
       "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Two e4m3 codes (low byte first) -> two f16 (exact: every e4m3 value is an f16).
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-  const __half2_raw h =
-      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+__device__ __forceinline__ uint32_t lds_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
 }
 
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-  const __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
+// Two non-negative floats x0, x1 (< 448) as e4m3 hi + lo parts: hi = e4m3(x),
+// lo = e4m3(x - hi).  hi + lo is within 2^-8 relative of x (for x above the
+// subnormal range).  Returned as two codes each, x0's in the low byte.
+__device__ __forceinline__ void split_e4m3x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __half2 x = __floats2half2_rn(x0, x1);
+  const __nv_fp8x2_storage_t h =
+      __nv_cvt_halfraw2_to_fp8x2(static_cast<__half2_raw>(x), __NV_SATFINITE, __NV_E4M3);
+  const __half2 back = static_cast<__half2>(__nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3));
+  const __half2 r = __hsub2(x, back);
+  hi = h;
+  lo = __nv_cvt_halfraw2_to_fp8x2(static_cast<__half2_raw>(r), __NV_SATFINITE, __NV_E4M3);
 }
 
-// Tensor-core consumer for float8 e4m3 pools (any group 1..8).  The same two
-// products as TensorConsumer, with f16 operands: e4m3 -> f16 is exact, q and P
-// are rounded to f16.  The stored codes are used as they are; the kv head's
-// scales are applied outside the loop (K's in the score scale, V's when the
-// item's state is handed over).
-//   Scores: one 16-byte chunk of a K row is one k-step of 16 head_dim columns;
-//   ldmatrix gives lane t the 4 codes d = 4 (t % 4) .. +3 of token t / 4, so the
-//   k order inside a step is permuted the same way for q (a bijection on the
-//   step's columns, which the sum does not see).
-//   Values: ldmatrix.trans on code pairs gives lane t, for tokens 2 (t % 4) and
-//   +1, the codes of columns 2 (t / 4) and 2 (t / 4) + 1; the first feeds O^T
-//   row t / 4, the second row t / 4 + 8, so an m-tile covers one 16-column chunk
-//   with its rows in the order 0, 2, .., 14, 1, 3, .., 15.
+// Tensor-core consumer for float8 e4m3 pools (any group 1..8), 32-token units,
+// with e4m3 operands on both sides so that the stored codes enter the products
+// without conversion (an e4m3 -> f16 conversion costs about ten issue slots;
+// an m16n8k32 e4m3 MMA about four).  The other operand of each product is
+// split into two e4m3 parts, hi + lo, and both are multiplied:
+//   * q: prepared once per step by the q-preparation kernel (row scaled by a
+//     power of two 2^e so that its largest element lies in [128, 256); hi, lo
+//     and 2^-e stored side by side).  Scores use q' K^T * 2^-e * scale * k_scale.
+//   * P: the probabilities scaled by 2^8 are split per unit; the output is
+//     multiplied by v_scale / 2^8 at the end.
+// The split keeps 2^-8 relative precision per element, against 2^-9 for a bf16
+// operand.  The lo parts ride in MMA rows / columns the group leaves empty, so
+// they cost no extra MMA: q' lo in A row g + 8 under q' hi in row g (any
+// group), P lo in B columns 4..7 beside P hi in columns 0..3 (groups <= 4).
+//   Scores S = q' K^T: the q rows are A (rows past the group are zero), K rows
+//   are B: ldmatrix gives lane t the codes 4 (t % 4) .. + 3 of a 16-byte chunk
+//   of token t / 4's row, which is exactly b0 (first 16 columns of a 32-column
+//   step) or b1 (last 16).
+//   Values O^T = V^T P^T: ldmatrix.trans on code pairs gives lane t, for
+//   tokens 2 (t % 4), +1 of an 8-token block, the codes of columns 2 (t / 4) and
+//   2 (t / 4) + 1 of a 16-byte chunk; a byte permutation of two such registers
+//   (blocks 0-7 and 8-15) forms a0 / a1 (columns 2 (t / 4) and 2 (t / 4) + 1,
+//   tokens 2c, 2c + 1, 2c + 8, 2c + 9), and blocks 16-31 form a2 / a3.  The
+//   same token order is what each lane holds of P after the scores, so the
+//   B operand of P is built from the lane's own probabilities.  An m-tile
+//   covers one 16-byte chunk of V with its rows in the order 0, 2, .., 14,
+//   1, 3, .., 15.
 template <typename Tr>
 struct Fp8TensorConsumer {
   static constexpr int G = Tr::G_, D = Tr::D_;
-  static constexpr int KS = D / 16;     // k-steps (16-byte chunks of a K row)
-  static constexpr int MT = D / 16;     // O^T m-tiles (16-byte chunks of a V row)
-  uint32_t qa[KS][2];                   // f16x2 q fragments (row t/4; columns 4c..4c+1, 4c+2..4c+3)
+  static constexpr int KS = D / 32;     // score k-steps (32 columns: two 16-byte chunks)
+  static constexpr int MT = D / 16;     // O^T m-tiles (one 16-byte chunk of a V row)
+  static constexpr int NT = 4;          // score n-tiles (8 tokens) of a 32-token block
+  static constexpr int NB = Tr::UT / 32;  // 32-token blocks per unit
+  static_assert(Tr::UT % 32 == 0, "the fp8 consumer takes units of 32-token blocks");
+  static constexpr float kPScale = 256.f;
+  // a group of at most 4 leaves columns 4..7 of the PV product free for the lo
+  // parts of P: one MMA per m-tile instead of two
+  static constexpr bool kPackPV = G <= 4;
+  uint32_t qaddr;                       // shared address of this lane's q' hi codes
+  bool qrow;                            // lane / 4 is a row of the group
   float o[MT][4];
-  float m, l, vscale;
+  float m, l, sc, vscale;
   int lane;
 
   __device__ __forceinline__ void init(int lane_, float*) { lane = lane_; }
 
-  __device__ __forceinline__ void begin(const char* qs, float, float v_scale) {
+  __device__ __forceinline__ void begin(const char* qs, float score_scale, float v_scale) {
     const int g = lane >> 2, c = lane & 3;
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      qa[ks][0] = 0u;
-      qa[ks][1] = 0u;
-      if (g < G) {
-        const uint2 w = *reinterpret_cast<const uint2*>(qs + g * Tr::QROW_BYTES + (16 * ks + 4 * c) * 2);
-        qa[ks][0] = pack_f16x2(bf16_lo(w.x), bf16_hi(w.x));
-        qa[ks][1] = pack_f16x2(bf16_lo(w.y), bf16_hi(w.y));
-      }
-    }
+    float qinv = 0.f;
+    qrow = g < G;
+    // the q' fragments are read from shared memory in every unit (the slot
+    // stays valid for the whole item), which keeps 16 registers free
+    qaddr = smem_addr(qs + (qrow ? g : 0) * Tr::QROW_BYTES + 4 * c);
+    if (qrow) qinv = *reinterpret_cast<const float*>(qs + g * Tr::QROW_BYTES + 2 * D);
+    sc = score_scale * qinv;
+    vscale = v_scale * (1.f / kPScale);
     m = -INFINITY;
     l = 0.f;
-    vscale = v_scale;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   }
 
+  // A unit is NB blocks of 32 tokens (block b: rows 32 b .. 32 b + 31 of the K
+  // and V tiles, 4 KiB apart, which keeps the 128-byte swizzle phase); the
+  // stage is released after the last block has been read.
   template <typename Release>
-  __device__ __forceinline__ void unit(const char* kt, const char* vt, int nt, float score_scale,
+  __device__ __forceinline__ void unit(const char* kt, const char* vt, int nt, float,
                                        Release release) {
-    const uint32_t kb = smem_addr(kt), vb = smem_addr(vt);
-    const int mi = lane >> 3, r8 = lane & 7, c = lane & 3;
-    uint32_t kr[KS][2], vr[MT][2];      // raw codes: [step][n-tile] and [m-tile][token half]
-#pragma unroll
-    for (int j = 0; j < KS / 2; ++j)    // tokens 0-7 / 8-15 x chunks 2j, 2j+1
-      ldsm_x4(kb + swz<Tr>((mi >> 1) * 8 + r8, 2 * j + (mi & 1)), kr[2 * j][0], kr[2 * j + 1][0],
-              kr[2 * j][1], kr[2 * j + 1][1]);
-#pragma unroll
-    for (int j = 0; j < MT / 2; ++j)    // chunks 2j, 2j+1 x tokens 0-7 / 8-15
-      ldsm_x4_trans(vb + swz<Tr>((mi & 1) * 8 + r8, 2 * j + (mi >> 1)), vr[2 * j][0], vr[2 * j][1],
-                    vr[2 * j + 1][0], vr[2 * j + 1][1]);
+#pragma unroll 1
+    for (int b = 0; b < NB && 32 * b < nt; ++b)
+      block32(smem_addr(kt) + 4096 * b, smem_addr(vt) + 4096 * b, nt - 32 * b);
     release();
-    // ---- scores
-    float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+  }
+
+  __device__ __forceinline__ void block32(uint32_t kb, uint32_t vb, int nt) {
+    const int mi = lane >> 3, r8 = lane & 7, c = lane & 3;
+    // ---- scores: per step ks, kr[n][0 / 1] = b0 / b1 of n-tile n.  The A rows
+    // past the group are free, so q' lo sits in row g + 8 under q' hi in row g:
+    // one MMA gives both products (c0, c1: hi; c2, c3: lo)
+    float sh[NT][4];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) sh[n][0] = sh[n][1] = sh[n][2] = sh[n][3] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      mma_f16(s0, qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_f16x2(kr[ks][0]),
-              e4m3x2_to_f16x2(kr[ks][0] >> 16));
-      mma_f16(s1, qa[ks][0], 0u, qa[ks][1], 0u, e4m3x2_to_f16x2(kr[ks][1]),
-              e4m3x2_to_f16x2(kr[ks][1] >> 16));
+      uint32_t qh0 = 0u, qh1 = 0u, ql0 = 0u, ql1 = 0u;
+      if (qrow) {
+        qh0 = lds_u32(qaddr + 32 * ks);
+        qh1 = lds_u32(qaddr + 32 * ks + 16);
+        ql0 = lds_u32(qaddr + D + 32 * ks);
+        ql1 = lds_u32(qaddr + D + 32 * ks + 16);
+      }
+      uint32_t kr[NT][2];
+#pragma unroll
+      for (int hb = 0; hb < NT / 2; ++hb)   // tokens 16 hb + (0-7 | 8-15) x chunks 2ks, 2ks+1
+        ldsm_x4(kb + swz<Tr>(16 * hb + (mi >> 1) * 8 + r8, 2 * ks + (mi & 1)),
+                kr[2 * hb][0], kr[2 * hb][1], kr[2 * hb + 1][0], kr[2 * hb + 1][1]);
+#pragma unroll
+      for (int n = 0; n < NT; ++n) {
+        mma_e4m3(sh[n], qh0, ql0, qh1, ql1, kr[n][0], kr[n][1]);
+      }
     }
-    float sv[4] = {s0[0], s0[1], s1[0], s1[1]};
-    const int tk[4] = {2 * c, 2 * c + 1, 8 + 2 * c, 9 + 2 * c};
+    // ---- online softmax over the unit's tokens 8 n + 2c, 8 n + 2c + 1 (row lane / 4)
+    float sv[2 * NT];
     float mx = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      sv[e] = tk[e] < nt ? sv[e] * score_scale : -INFINITY;
-      mx = fmaxf(mx, sv[e]);
-    }
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int tk = 8 * n + 2 * c + e;
+        const float v = (sh[n][e] + sh[n][e + 2]) * sc;
+        sv[2 * n + e] = tk < nt ? v : -INFINITY;
+        mx = fmaxf(mx, sv[2 * n + e]);
+      }
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 2));
     const float mn = fmaxf(m, mx);
     const float alpha = fast_exp2(m - mn);
     m = mn;
-    float pr[4];
+    float psum = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) pr[e] = fast_exp2(sv[e] - mn);
-    l = l * alpha + ((pr[0] + pr[1]) + (pr[2] + pr[3]));
-    const uint32_t pb0 = pack_f16x2(pr[0], pr[1]);
-    const uint32_t pb1 = pack_f16x2(pr[2], pr[3]);
-    const float a_even = __shfl_sync(kFull, alpha, 8 * c);
-    const float a_odd = __shfl_sync(kFull, alpha, 8 * c + 4);
-    // ---- values: codes (token 2c: cols 2g, 2g+1 | token 2c+1: cols 2g, 2g+1)
+    for (int e = 0; e < 2 * NT; ++e) {
+      sv[e] = fast_exp2(sv[e] - mn);
+      psum += sv[e];
+    }
+    l = l * alpha + psum;
+    // P^T operand: b0 = tokens (2c, 2c+1, 2c+8, 2c+9), b1 = the same + 16
+    uint32_t ph[NT], pl[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) split_e4m3x2(sv[2 * n] * kPScale, sv[2 * n + 1] * kPScale, ph[n], pl[n]);
+    uint32_t bh0 = ph[0] | (ph[1] << 16), bh1 = ph[2] | (ph[3] << 16);
+    const uint32_t bl0 = pl[0] | (pl[1] << 16), bl1 = pl[2] | (pl[3] << 16);
+    if constexpr (kPackPV) {
+      // columns 4..7 of P^T (rows 4..7 of the group, unused) carry the lo parts
+      // of heads 0..3: lane (g, c), g >= 4, takes them from lane (g - 4, c)
+      const uint32_t xl0 = __shfl_xor_sync(kFull, bl0, 16), xl1 = __shfl_xor_sync(kFull, bl1, 16);
+      if (lane >= 16) {
+        bh0 = xl0;
+        bh1 = xl1;
+      }
+    }
+    // rescale the accumulators when some row's maximum moved
+    if (__any_sync(kFull, alpha != 1.f)) {
+      const int hc = kPackPV ? (c & 1) : c;           // head pair of this lane's columns
+      const float a_even = __shfl_sync(kFull, alpha, 8 * hc);
+      const float a_odd = __shfl_sync(kFull, alpha, 8 * hc + 4);
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        o[mt][0] *= a_even;
+        o[mt][1] *= a_odd;
+        o[mt][2] *= a_even;
+        o[mt][3] *= a_odd;
+      }
+    }
+    // ---- values: vr[blk] = the ldmatrix.trans register of token block blk (8 tokens)
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
-      o[mt][0] *= a_even;
-      o[mt][1] *= a_odd;
-      o[mt][2] *= a_even;
-      o[mt][3] *= a_odd;
-      const uint32_t a0 = e4m3x2_to_f16x2(__byte_perm(vr[mt][0], 0u, 0x0020));   // col 2g
-      const uint32_t a1 = e4m3x2_to_f16x2(__byte_perm(vr[mt][0], 0u, 0x0031));   // col 2g+1
-      const uint32_t a2 = e4m3x2_to_f16x2(__byte_perm(vr[mt][1], 0u, 0x0020));
-      const uint32_t a3 = e4m3x2_to_f16x2(__byte_perm(vr[mt][1], 0u, 0x0031));
-      mma_f16(o[mt], a0, a1, a2, a3, pb0, pb1);
+      uint32_t vr[4];
+      ldsm_x4_trans(vb + swz<Tr>(mi * 8 + r8, mt), vr[0], vr[1], vr[2], vr[3]);
+      const uint32_t a0 = __byte_perm(vr[0], vr[1], 0x6420);   // column 2g
+      const uint32_t a1 = __byte_perm(vr[0], vr[1], 0x7531);   // column 2g + 1
+      const uint32_t a2 = __byte_perm(vr[2], vr[3], 0x6420);
+      const uint32_t a3 = __byte_perm(vr[2], vr[3], 0x7531);
+      mma_e4m3(o[mt], a0, a1, a2, a3, bh0, bh1);
+      if constexpr (!kPackPV) mma_e4m3(o[mt], a0, a1, a2, a3, bl0, bl1);
     }
   }
 
@@ -710,6 +819,10 @@ struct Fp8TensorConsumer {
     const int h0 = 2 * c, h1 = 2 * c + 1;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
+      if constexpr (kPackPV) {             // add the lo columns (lane c + 2) to the hi ones
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[mt][e] += __shfl_xor_sync(kFull, o[mt][e], 2);
+      }
       const int d0 = 16 * mt + 2 * g, d1 = d0 + 1;     // O^T rows g and g + 8
       if (h0 < G) {
         macc_w[h0 * D + d0] = o[mt][0] * vscale;
@@ -724,9 +837,10 @@ struct Fp8TensorConsumer {
 };
 
 template <bool BF16, int D, int G, bool KV8>
-__global__ void __launch_bounds__(kDecodeThreads, 1)
+__global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
     paged_decode_kernel(const __grid_constant__ DecodeKernelParams p) {
   using Tr = DecodeTraits<BF16, D, G, KV8>;
+  constexpr int CW = Tr::CW;
   using Consumer = typename std::conditional<
       KV8, Fp8TensorConsumer<Tr>,
       typename std::conditional<Tr::TC, TensorConsumer<Tr>, CoreConsumer<Tr>>::type>::type;
@@ -763,14 +877,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     }
     for (int k = 0; k < kItemSlots; ++k) {
       mbar_init(&item_full[k], 1);
-      // released by the 8 producer lanes (done issuing) and the 8 consumer warps (q read)
-      mbar_init(&item_empty[k], 2 * kConsumerWarps);
+      // released by every consumer warp (q read) and by its producer lane
+      // (done issuing)
+      mbar_init(&item_empty[k], 2 * CW);
       mbar_init(&sched_full[k], 1);
     }
     mbar_init(merge_free, 1);
     *abort_flag = 0;
     *merge_cnt = 0;
-    for (int w = 0; w < kConsumerWarps; ++w) issued_by[w] = 0;
+    for (int w = 0; w < CW; ++w) issued_by[w] = 0;
     fence_mbar_init();
   }
   // launched as a programmatic dependent of the plan kernel: everything above
@@ -782,7 +897,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
   const int Hkv = p.num_kv_heads;
   const int bs = p.block_size;
 
-  if (warp == kConsumerWarps + 1) {
+  if (warp == CW + 1) {
     // ----------------------------------------------------------- scheduler
     // Claims work items and resolves them (atomic counter -> work entry ->
     // block-table slice) into the shared item slots, then starts the copy of
@@ -797,7 +912,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       for (uint32_t spin = 0; spin < p.wait_limit; ++spin) {
         uint32_t issued = 0;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) issued += issued_by[w];
+        for (int w = 0; w < CW; ++w) issued += issued_by[w];
         if (*abort_flag || static_cast<int>(claimed - issued) <= kUnitsAhead) break;
         __nanosleep(100);
       }
@@ -844,7 +959,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         ItemDesc d;
         d.b = w.x; d.h = h; d.chunk = w.y; d.len = w.z; d.gchunk = w.w;
         d.n_units = n_units; d.n_tokens = ntok; d.single = (w.z <= p.chunk_tokens);
-        d.rot = i % kConsumerWarps;
+        d.rot = i % CW;
         desc[slot] = d;
       }
       __syncwarp();
@@ -871,98 +986,87 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     return;
   }
 
-  if (warp == kConsumerWarps) {
+  if (warp == CW) {
     // ------------------------------------------------------------ producer
-    // Lane w < 8 feeds consumer warp w's sub-ring: the units u of every item
-    // with (u + rot) % 8 == w, in order.  Eight copies are in issue at once (one
-    // issuing thread cannot keep HBM busy), and the lanes advance independently
-    // -- each polls its own barriers without blocking -- so a consumer that is
+    // Lane w < CW feeds consumer warp w: the units u of every item with
+    // (u + rot) % CW == w, in order, into w's sub-ring.
+    // Each lane runs its own sequence with blocking (bounded) barrier waits;
+    // the lanes of the warp diverge freely, so several copies are in issue at
+    // once (one issuing thread cannot keep HBM busy) and a consumer that is
     // busy merging only holds back its own sub-ring.
-    const bool mine = lane < kConsumerWarps;
-    bool active = mine;
-    uint32_t k = 0;          // item this lane is in
-    uint32_t c = 0;          // units this lane has issued
-    int u = -1;              // next unit of item k for this lane; -1: descriptor not read yet
-    int n_units = 0, h = 0;
-    uint32_t idle = 0;
-    bool ok = true;
-    while (__any_sync(kFull, active)) {
-      bool progressed = false;
-      if (active) {
+    const int w = lane;
+    if (w < CW) {
+      uint32_t c = 0;                      // units this lane has issued
+      bool ok = true;
+      for (uint32_t k = 0; ok; ++k) {
         const int slot = k % kItemSlots;
-        if (u < 0) {
-          if (mbar_test(&sched_full[slot], (k / kItemSlots) & 1)) {
-            const ItemDesc d = desc[slot];
-            progressed = true;
-            if (d.b < 0) {
-              active = false;
-            } else {
-              n_units = d.n_units;
-              h = d.h;
-              u = (lane - d.rot + kConsumerWarps) % kConsumerWarps;
-              if (u >= n_units) {                // no unit of this item for this lane
-                mbar_arrive(&item_empty[slot]);
-                ++k;
-                u = -1;
-              }
-            }
+        if (!mbar_wait(&sched_full[slot], (k / kItemSlots) & 1, p.wait_limit) || *abort_flag) {
+          ok = false;
+          break;
+        }
+        const ItemDesc d = desc[slot];
+        if (d.b < 0) break;
+        for (int u = (w - d.rot + CW) % CW; u < d.n_units; u += CW) {
+          const int s = w + CW * static_cast<int>(c % Tr::SPW);
+          if (!mbar_wait(&empty[s], ((c / Tr::SPW) & 1) ^ 1, p.wait_limit)) {
+            ok = false;
+            break;
           }
-        } else {
-          const int s = lane + kConsumerWarps * static_cast<int>(c % Tr::SPW);
-          if (mbar_test(&empty[s], ((c / Tr::SPW) & 1) ^ 1)) {
-            const int tok = u * Tr::UT;
-            const int pp = tbl_s[slot * 32 + tok / bs];
-            if (pp >= 0) {
+          const int tok = u * Tr::UT;
+          char* dst = stages + s * Tr::STAGE_BYTES;
+          const int pp = tbl_s[slot * 32 + tok / bs];
+          if constexpr (Tr::TC) {
+            // one tensor-map box per page the unit touches (a unit longer than
+            // a page takes several; the last unit of an item only those it
+            // needs) and pool, each taking all 128-byte slabs of its rows
+            const int rows_op = bs < Tr::UT ? bs : Tr::UT;
+            int n_op = 1;
+            bool pages_ok = pp >= 0;
+            if (rows_op < Tr::UT) {
+              n_op = (min(Tr::UT, d.n_tokens - tok) + rows_op - 1) / rows_op;
+              for (int j = 1; j < n_op; ++j)
+                pages_ok &= tbl_s[slot * 32 + (tok + j * rows_op) / bs] >= 0;
+            }
+            if (pages_ok) {
               stage_bad[s] = 0;
-              mbar_arrive_expect_tx(&full[s], Tr::STAGE_BYTES);
-              char* dst = stages + s * Tr::STAGE_BYTES;
-              const int64_t row = (static_cast<int64_t>(pp) * Hkv + h) * bs + (tok % bs);
-              if constexpr (Tr::TC) {
-#pragma unroll
-                for (int bx = 0; bx < Tr::BOXES; ++bx) {
-                  tma_load_2d(dst + bx * Tr::BOX_BYTES, &p.tmap_k, bx * Tr::BOX_COLS, static_cast<int>(row),
-                              &full[s]);
-                  tma_load_2d(dst + Tr::TILE_BYTES + bx * Tr::BOX_BYTES, &p.tmap_v, bx * Tr::BOX_COLS,
-                              static_cast<int>(row), &full[s]);
-                }
-              } else {
-                const int64_t off = row * Tr::ROW_BYTES;
-                bulk_g2s(dst, p.k_cache + off, Tr::TILE_BYTES, &full[s]);
-                bulk_g2s(dst + Tr::TILE_BYTES, p.v_cache + off, Tr::TILE_BYTES, &full[s]);
+              mbar_arrive_expect_tx(&full[s], n_op * rows_op * Tr::ROW_BYTES * 2);
+              for (int j = 0; j < n_op; ++j) {
+                const int t = tok + j * rows_op;
+                const int pj = j == 0 ? pp : tbl_s[slot * 32 + t / bs];
+                const int row = (pj * Hkv + d.h) * bs + t % bs;
+                tma_rows<Tr>(dst + j * rows_op * 128, &p.tmap_k, row, &full[s]);
+                tma_rows<Tr>(dst + Tr::TILE_BYTES + j * rows_op * 128, &p.tmap_v, row, &full[s]);
               }
             } else {
               stage_bad[s] = 1;
               mbar_arrive(&full[s]);
             }
-            ++c;
-            issued_by[lane] = c;
-            progressed = true;
-            u += kConsumerWarps;
-            if (u >= n_units) {                  // done with this item
-              mbar_arrive(&item_empty[slot]);
-              ++k;
-              u = -1;
-            }
+          } else if (pp >= 0) {
+            stage_bad[s] = 0;
+            mbar_arrive_expect_tx(&full[s], Tr::STAGE_BYTES);
+            const int64_t off =
+                ((static_cast<int64_t>(pp) * Hkv + d.h) * bs + (tok % bs)) * Tr::ROW_BYTES;
+            bulk_g2s(dst, p.k_cache + off, Tr::TILE_BYTES, &full[s]);
+            bulk_g2s(dst + Tr::TILE_BYTES, p.v_cache + off, Tr::TILE_BYTES, &full[s]);
+          } else {
+            stage_bad[s] = 1;
+            mbar_arrive(&full[s]);
           }
+          ++c;
+          issued_by[w] = c;
         }
+        if (!ok) break;
+        mbar_arrive(&item_empty[slot]);      // done issuing from this item
       }
-      if (__any_sync(kFull, progressed)) {
-        idle = 0;
-      } else {
-        if (++idle > p.wait_limit || *abort_flag) { ok = false; break; }
-        __nanosleep(20);
+      if (!ok) {                             // gave up: tell the others
+        report(p.device_errors, PA_DEVERR_TIMEOUT);
+        *abort_flag = 1;
       }
-    }
-    if (!ok && lane == 0) {            // give up: tell the others
-      report(p.device_errors, PA_DEVERR_TIMEOUT);
-      *abort_flag = 1;
-    }
-    // Wait (bounded) for copies still in flight on warp `lane`'s sub-ring: only
-    // the last SPW can be (immediate when the consumers took them all).
-    if (mine) {
+      // Wait (bounded) for copies still in flight on warp w's sub-ring: only
+      // the last SPW can be (immediate when the consumer took them all).
       const uint32_t first = c > static_cast<uint32_t>(Tr::SPW) ? c - Tr::SPW : 0;
       for (uint32_t cc = first; cc < c; ++cc)
-        mbar_wait(&full[lane + kConsumerWarps * (cc % Tr::SPW)], (cc / Tr::SPW) & 1);
+        mbar_wait(&full[w + CW * (cc % Tr::SPW)], (cc / Tr::SPW) & 1);
     }
     return;
   }
@@ -989,10 +1093,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     __syncwarp();
     if (lane == 0) mbar_arrive(&item_empty[slot]);
 
-    // this warp's units of the item: u = u0, u0 + 8, ... (u + rot == warp mod 8)
-    const int u0 = (warp - d.rot + kConsumerWarps) % kConsumerWarps;
-    for (int u = u0; u < d.n_units && !aborted; u += kConsumerWarps, ++consumed) {
-      const int s = warp + kConsumerWarps * static_cast<int>(consumed % Tr::SPW);
+    // this warp's units of the item: u = u0, u0 + CW, ... (u + rot == warp mod CW)
+    const int u0 = (warp - d.rot + CW) % CW;
+    for (int u = u0; u < d.n_units && !aborted; u += CW, ++consumed) {
+      const int s = warp + CW * static_cast<int>(consumed % Tr::SPW);
       if (!mbar_wait(&full[s], (consumed / Tr::SPW) & 1, p.wait_limit)) {
         report(p.device_errors, PA_DEVERR_TIMEOUT);
         *abort_flag = 1;
@@ -1004,7 +1108,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
         char* kt = stages + s * Tr::STAGE_BYTES;
         char* vt = kt + Tr::TILE_BYTES;
         if constexpr (Tr::TC) {
-          // The tensor cores multiply every one of the 16 rows, so value rows past
+          // The tensor cores multiply every row of the tile, so value rows past
           // the sequence (stale or never-written slots) must not hold NaN or Inf.
           if (nt < Tr::UT) {
             for (int i = lane; i < (Tr::UT - nt) * Tr::BOXES * 8; i += 32) {
@@ -1042,7 +1146,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
     int last = 0;
     if (lane == 0) {
       __threadfence_block();
-      last = atomicAdd(merge_cnt, 1) == kConsumerWarps - 1;
+      last = atomicAdd(merge_cnt, 1) == CW - 1;
       __threadfence_block();
     }
     last = __shfl_sync(kFull, last, 0);
@@ -1053,11 +1157,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
       for (int g = 0; g < G; ++g) {
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mml[(w * G + g) * 2]);
-        float f[kConsumerWarps];
+        for (int w = 0; w < CW; ++w) M = fmaxf(M, mml[(w * G + g) * 2]);
+        float f[CW];
         float lam = 0.f;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
+        for (int w = 0; w < CW; ++w) {
           f[w] = fast_exp2(mml[(w * G + g) * 2] - M);
           lam = fmaf(f[w], mml[(w * G + g) * 2 + 1], lam);
         }
@@ -1068,7 +1172,7 @@ __global__ void __launch_bounds__(kDecodeThreads, 1)
           const int dcol = 2 * cp;
           float o0 = 0.f, o1 = 0.f;
 #pragma unroll
-          for (int w = 0; w < kConsumerWarps; ++w) {
+          for (int w = 0; w < CW; ++w) {
             const float2 a = *reinterpret_cast<const float2*>(macc + (w * G + g) * D + dcol);
             o0 = fmaf(f[w], a.x, o0);
             o1 = fmaf(f[w], a.y, o1);
