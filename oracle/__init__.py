@@ -12,15 +12,17 @@ Contents, each written from the pages (cited in the modules):
   * ``e4m3_encode`` / ``decode_kv8_f64`` / ``reshape_and_cache_fp8`` -- the same
                               path with float8 e4m3 pools and per-kv-head scales.
   * ``RefBlockManager``    -- the teaching allocator of "PagedAttention原理" §3.3.4
-                              with the reference counts of §3.3.3 and copy-on-write.
+                              with the reference counts of §3.3.3, copy-on-write and
+                              swapping whole sequences to a host pool.
+  * ``copy_pages``         -- byte copy of pages between two pools (the swap copy).
 """
 from ._decode import build, decode_f64, decode_kv8_f64, library_path, max_threads, widen
-from ._cache_ops import (copy_blocks, e4m3_encode, e4m3_value, reshape_and_cache,
+from ._cache_ops import (copy_blocks, copy_pages, e4m3_encode, e4m3_value, reshape_and_cache,
                          reshape_and_cache_fp8)
-from .ref_block_manager import OutOfBlocks, RefBlockManager
+from .ref_block_manager import OutOfBlocks, RefBlockManager, Swapped
 
 __all__ = [
     "build", "decode_f64", "decode_kv8_f64", "library_path", "max_threads", "widen",
-    "copy_blocks", "e4m3_encode", "e4m3_value", "reshape_and_cache", "reshape_and_cache_fp8",
-    "OutOfBlocks", "RefBlockManager",
+    "copy_blocks", "copy_pages", "e4m3_encode", "e4m3_value", "reshape_and_cache",
+    "reshape_and_cache_fp8", "OutOfBlocks", "RefBlockManager", "Swapped",
 ]

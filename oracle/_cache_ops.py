@@ -51,6 +51,22 @@ def copy_blocks(k_cache, v_cache, src_dst_pairs) -> None:
         v_cache[dst] = v_cache[src]
 
 
+def copy_pages(src_k, src_v, dst_k, dst_v, src_dst_pairs) -> None:
+    """Copy whole pages between two pools: dst[d] = src[s] for each pair, K and V.
+
+    "PagedAttention MLX：为Apple Silicon打造的高吞吐量LLM推理引擎" (dynamic
+    scheduling; physical KV pool): pages of inactive requests are swapped out to
+    CPU memory and back.  A swap is this copy from the device pool to a host pool
+    (or back) for the pairs the block manager hands out.
+    """
+    pairs = np.asarray(src_dst_pairs, dtype=np.int64).reshape(-1, 2)
+    for src, dst in pairs:
+        if not (0 <= src < src_k.shape[0] and 0 <= dst < dst_k.shape[0]):
+            raise ValueError(f"pair ({src}, {dst}) is outside a pool")
+        dst_k[dst] = src_k[src]
+        dst_v[dst] = src_v[src]
+
+
 # ------------------------------------------------------------------ float8 e4m3
 def e4m3_value(code: int) -> float:
     """Value of an e4m3 code: 1 sign bit, 4 exponent bits (bias 7), 3 fraction

@@ -305,11 +305,14 @@ def shared_prefix_script(scale_parents=None, scale_children=None, seed=None,
                               initial_free_order=free_order)
 
 
-def random_bm_ops(seed: int, num_ops: int, max_seqs: int = 6):
+def random_bm_ops(seed: int, num_ops: int, max_seqs: int = 6, swap: bool = False):
     """A seeded random sequence of block-manager operations (names and operands
-    only; whether each succeeds is up to the manager under test)."""
+    only; whether each succeeds is up to the manager under test).  With ``swap``
+    the mix includes swapping sequences out to the host pool and back in."""
     rng = np.random.Generator(np.random.PCG64(seed))
     kinds = ["add", "append", "append", "append", "fork", "free"]
+    if swap:
+        kinds += ["swapout", "swapin"]
     ops = []
     for _ in range(num_ops):
         kind = kinds[int(rng.integers(0, len(kinds)))]

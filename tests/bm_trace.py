@@ -1,8 +1,10 @@
 """Reader and replayer of the hand-written block-manager traces in tests/golden/.
 
-A trace line reads ``op args -> result ; SEQ=[pages] ; free=[pages]``.  The
-replayer drives any manager with the oracle's method names (add_seq,
-append_slot, fork, free, block_table, free_list) and compares each result.
+A trace line reads ``op args -> result ; SEQ=[pages] ; free=[pages]``, with an
+optional ``; host=[blocks]`` (the host free list) for swap traces.  The replayer
+drives any manager with the oracle's method names (add_seq, append_slot, fork,
+free, swap_out, swap_in, block_table, free_list, host_free_list) and compares
+each result.
 """
 import os
 
@@ -27,22 +29,40 @@ def load_trace(name):
                 continue
             lhs, rhs = line.split("->")
             op = lhs.split()
-            result, table, free = [part.strip() for part in rhs.split(";")]
-            steps.append((op, result, table, _ids(free.split("=", 1)[1])))
+            parts = [part.strip() for part in rhs.split(";")]
+            result, table, free = parts[:3]
+            host = _ids(parts[3].split("=", 1)[1]) if len(parts) > 3 else None
+            steps.append((op, result, table, _ids(free.split("=", 1)[1]), host))
     return header, steps
 
 
-def replay(manager, steps, is_oom):
+def _pairs(text):
+    return [tuple(int(x) for x in p.split(":")) for p in text.split(",")] if text else []
+
+
+def replay(manager, steps, is_oom, is_swapped=None):
     """``is_oom(callable)`` runs an operation and says whether it reported an
-    out-of-blocks error (raising anything else)."""
+    out-of-blocks error (raising anything else); ``is_swapped(callable)`` likewise
+    for the refusal of an operation on a swapped-out sequence."""
     names = {}
 
     def sid(name):
         return names.setdefault(name, len(names) + 10)
 
-    for op, result, table, free in steps:
+    for op, result, table, free, host in steps:
         kind = op[0]
-        if kind == "add":
+        if result == "swapped":
+            args = [sid(x) for x in op[1:]]
+            fn = {"append": manager.append_slot, "fork": manager.fork}[kind]
+            assert is_swapped(lambda: fn(*args)), op
+        elif kind in ("swapout", "swapin") and result == "oom":
+            fn = manager.swap_out if kind == "swapout" else manager.swap_in
+            assert is_oom(lambda: fn(sid(op[1]))), op
+        elif kind in ("swapout", "swapin"):
+            fn = manager.swap_out if kind == "swapout" else manager.swap_in
+            got = [tuple(int(x) for x in p) for p in fn(sid(op[1]))]
+            assert got == _pairs(result), (op, got, result)
+        elif kind == "add":
             if result == "oom":
                 assert is_oom(lambda: manager.add_seq(sid(op[1]))), op
             else:
@@ -66,6 +86,8 @@ def replay(manager, steps, is_oom):
             got, _ = manager.block_table(sid(seq))
             assert list(got) == _ids(pages), (op, got, pages)
         assert list(manager.free_list()) == free, (op, manager.free_list(), free)
+        if host is not None:
+            assert list(manager.host_free_list()) == host, (op, manager.host_free_list(), host)
 
 
 def check_invariants(manager, num_blocks, live):
