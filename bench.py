@@ -409,6 +409,120 @@ def run_gpu(args, world, rank, local):
     return result
 
 
+SWAP_METRIC = "page swap GB/s (device pool <-> pinned host pool, out + in)"
+
+
+def host_link_peak(torch, device, nbytes=1 << 30, reps=5):
+    """Measured copy-engine rate of one large pinned <-> device copy each way
+    (GB/s): the denominator of the swap roofline."""
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    rates = {}
+    for name, (dst, src) in (("d2h", (h, d)), ("h2d", (d, h))):
+        dst.copy_(src, non_blocking=True)
+        torch.cuda.synchronize(device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize(device)
+        rates[name] = nbytes * reps / (a.elapsed_time(b) * 1e-3) / 1e9
+    del h, d
+    return rates
+
+
+def run_swap(args, world, rank, local):
+    """Swap a quarter of the GQA workload's sequences (every 4th) out to a
+    pinned host pool and back into their pages, every step: one pa_swap_blocks
+    call each way, plus the host block manager's swap bookkeeping for the same
+    sequences timed separately."""
+    import torch
+    import paged_kv_cache_190_gb300 as pa
+    pa.library()
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    if rank != 0:
+        return None
+    case = pa_inputs.workload("gqa_bf16")
+    NB, Hkv, bs, D = case.k_cache.shape
+    to = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(device)
+    kc, vc = to(case.k_cache), to(case.v_cache)
+    victims = list(range(0, case.num_seqs, 4))
+    pages = [int(p) for b in victims for p in case.block_tables[b] if p >= 0]
+    H = len(pages)
+    hk = torch.empty((H, Hkv, bs, D), dtype=torch.bfloat16).pin_memory()
+    hv = torch.empty((H, Hkv, bs, D), dtype=torch.bfloat16).pin_memory()
+    out_pairs = torch.tensor([[p, h] for h, p in enumerate(pages)], dtype=torch.int64, device=device)
+    in_pairs = out_pairs[:, [1, 0]].contiguous()
+    errs = torch.zeros(1, dtype=torch.int32, device=device)
+    block_bytes = Hkv * bs * D * 2
+    bytes_step = 2 * 2 * H * block_bytes                  # K and V, out and in
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        pa.pa_swap_blocks(kc, vc, hk, hv, out_pairs, device_errors=errs)
+        pa.pa_swap_blocks(hk, hv, kc, vc, in_pairs, device_errors=errs)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    K = min(args.steps, 200)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    with ClockSampler(device.index if device.index is not None else 0) as clocks:
+        for i in range(K):
+            ev[i][0].record(stream)
+            pa.pa_swap_blocks(kc, vc, hk, hv, out_pairs, device_errors=errs)
+            ev[i][1].record(stream)
+            pa.pa_swap_blocks(hk, hv, kc, vc, in_pairs, device_errors=errs)
+            ev[i][2].record(stream)
+        torch.cuda.synchronize(device)
+    flags = pa.pa_read_device_errors(errs)
+    if flags:
+        raise RuntimeError(f"device error bits {flags}")
+    out_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(K))
+    in_ms = statistics.mean(ev[i][1].elapsed_time(ev[i][2]) for i in range(K))
+    ms = out_ms + in_ms
+    peak = host_link_peak(torch, device)
+    half = bytes_step / 2
+    out_gbs, in_gbs = half / (out_ms * 1e-3) / 1e9, half / (in_ms * 1e-3) / 1e9
+    # host bookkeeping: swap the same sequences out and in through the C++ manager
+    bm = pa.BlockManager(NB, bs)
+    bm.enable_swap(H + 1)
+    lens = case.context_lens
+    for b in victims:
+        bm.add_seq(b)
+        for _ in range(int(lens[b])):
+            bm.append_slot(b)
+    t0 = time.perf_counter()
+    for b in victims:
+        bm.swap_out(b)
+    t1 = time.perf_counter()
+    for b in victims:
+        bm.swap_in(b)
+    t2 = time.perf_counter()
+    bm.close()
+    return {
+        "metric": SWAP_METRIC, "value": round(bytes_step / (ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "n_gpus": 1, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bytes",
+        "data": "synthetic (seeded pa_inputs; no dataset or weights)",
+        "config": {"workload": "swap_gqa", "sequences_swapped": len(victims), "pages": H,
+                   "page_bytes_per_pool": block_bytes, "bytes_per_step": bytes_step,
+                   "host_pool": "pinned host memory, addressed by the kernel over the host link"},
+        "roofline": {"bound": "host-link", "achieved": round(min(out_gbs, in_gbs), 1),
+                     "peak": round(min(peak["d2h"], peak["h2d"]), 1), "unit": "GB/s",
+                     "frac": round(min(out_gbs / peak["d2h"], in_gbs / peak["h2d"]), 4),
+                     "traffic": None, "out_gbs": round(out_gbs, 1), "in_gbs": round(in_gbs, 1),
+                     "peak_source": "measured in this run: one 1 GiB pinned<->device copy each way "
+                                    f"(d2h {peak['d2h']:.1f}, h2d {peak['h2d']:.1f} GB/s)"},
+        "host_block_manager": {"swap_out_all_us": round((t1 - t0) * 1e6, 1),
+                               "swap_in_all_us": round((t2 - t1) * 1e6, 1),
+                               "sequences": len(victims)},
+        "gpu_launches": 2 * K, "clocks": clocks.summary(),
+    }
+
+
 def host_block_manager_time(case, pa, repeats: int = 100):
     """Host cost of the block manager for this batch, after the sequences have
     been grown to the workload's lengths: one decode step (every sequence takes
@@ -557,12 +671,48 @@ def cpu_baseline(case, budget_s=15.0, kind="oracle"):
             "seconds": round(elapsed, 2)}
 
 
+def run_reference_swap(args, world):
+    """The oracle's page copy (numpy) on the swap_gqa pages: out to a host pool
+    and back, every step."""
+    import oracle
+    case = pa_inputs.workload("gqa_bf16")
+    NB, Hkv, bs, D = case.k_cache.shape
+    victims = list(range(0, case.num_seqs, 4))
+    pages = [int(p) for b in victims for p in case.block_tables[b] if p >= 0]
+    out_pairs = np.array([[p, h] for h, p in enumerate(pages)], np.int64)
+    in_pairs = out_pairs[:, ::-1].copy()
+    hk = np.empty((len(pages), Hkv, bs, D), case.k_cache.dtype)
+    hv = np.empty_like(hk)
+    kc, vc = case.k_cache, case.v_cache
+    bytes_step = 2 * 2 * len(pages) * Hkv * bs * D * 2
+    for _ in range(min(args.warmup, 2)):
+        oracle.copy_pages(kc, vc, hk, hv, out_pairs)
+        oracle.copy_pages(hk, hv, kc, vc, in_pairs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.copy_pages(kc, vc, hk, hv, out_pairs)
+        oracle.copy_pages(hk, hv, kc, vc, in_pairs)
+    sec = (time.perf_counter() - t0) / args.steps
+    value = bytes_step / sec / 1e9
+    return {"metric": SWAP_METRIC, "value": round(value, 3), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bytes",
+            "data": "synthetic (seeded pa_inputs)", "impl": "reference",
+            "config": {"workload": "swap_gqa", "pages": len(pages)},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": "every step whole (numpy page copies)"},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
 def run_reference(args, world, rank):
     """The reference arm: the CPU oracle on a bounded sample per step."""
     if rank != 0:
         return None
     import oracle
     oracle.build()
+    if args.workload == "swap_gqa":
+        return run_reference_swap(args, world)
     if args.workload == "shared_prefix_bf16":
         case = pa_inputs.workload("gqa_bf16")
     else:
@@ -609,7 +759,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=list(pa_inputs.WORKLOADS) + ["shared_prefix_bf16"])
+                    choices=list(pa_inputs.WORKLOADS) + ["shared_prefix_bf16", "swap_gqa"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--chunk-tokens", type=int, default=0,
@@ -622,6 +772,8 @@ def main(argv=None):
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE {world}")
     if args.impl == "reference":
         res = run_reference(args, world, rank)
+    elif args.workload == "swap_gqa":
+        res = run_swap(args, world, rank, local)
     else:
         res = run_gpu(args, world, rank, local)
     if res is not None:

@@ -60,6 +60,7 @@ typedef enum pa_dtype { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
 #define PA_ERR_NOT_FOUND (-5)     /* block manager: unknown sequence id          */
 #define PA_ERR_EXISTS (-6)        /* block manager: sequence id already in use   */
 #define PA_ERR_WORKSPACE (-7)     /* decode workspace missing or too small       */
+#define PA_ERR_SWAPPED (-8)       /* block manager: the sequence is swapped out   */
 
 /* Bits the kernels OR into *device_errors. */
 #define PA_DEVERR_BAD_BLOCK 1     /* block id outside [0, num_blocks)            */
@@ -96,6 +97,26 @@ int pa_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_ca
  */
 int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst_pairs, int num_pairs,
                    size_t block_bytes, int num_blocks, int32_t* device_errors, void* stream);
+
+/*
+ * Page copy between two pools, for swapping pages to host memory and back
+ * ("PagedAttention MLX：为Apple Silicon打造的高吞吐量LLM推理引擎": dynamic
+ * scheduling swaps the caches of inactive requests out to CPU memory; the
+ * physical KV pool supports swapping out).  For each pair (src, dst) in
+ * src_dst_pairs (device int64 [num_pairs][2]):
+ *     dst_k[dst] = src_k[src]; dst_v[dst] = src_v[src]
+ * where one block is block_bytes bytes (a multiple of 16).  Either pool may be
+ * device memory or pinned host memory the GPU can address (cudaHostAlloc /
+ * cudaHostRegister, or a pinned torch tensor), e.g. device -> host with the
+ * pairs of pa_bm_swap_out and host -> device with those of pa_bm_swap_in.  The
+ * copy runs as one kernel (all pages at once over the host link).  Ids outside
+ * [0, num_src_blocks) or [0, num_dst_blocks) set PA_DEVERR_BAD_BLOCK and that
+ * pair is skipped.  Destinations must be distinct; the two pools must not
+ * overlap.
+ */
+int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                   const int64_t* src_dst_pairs, int num_pairs, size_t block_bytes,
+                   int num_src_blocks, int num_dst_blocks, int32_t* device_errors, void* stream);
 
 /*
  * Split size (in tokens) pa_decode uses when chunk_tokens == 0: the work of each
@@ -228,6 +249,18 @@ int pa_read_device_errors(int32_t* device_errors, int32_t* host_flags, int clear
  *   - fork gives `child` the parent's table and length, one more reference each.
  *   - free drops one reference per page; pages at zero return to the free list.
  *   - PA_ERR_OUT_OF_BLOCKS leaves every piece of state unchanged.
+ *   - Swapping (after pa_bm_enable_swap): pa_bm_swap_out moves a whole sequence
+ *     to host blocks -- each of its pages in table order takes a host block
+ *     from the end of the host free list, pairs[i] = (device page, host block);
+ *     then each page drops one reference (pages at zero return to the device
+ *     free list in table order).  pa_bm_swap_in takes a device page for each
+ *     host block in table order, pairs[i] = (host block, device page), and
+ *     returns the host blocks in table order.  The caller runs pa_swap_blocks
+ *     with the pairs before anything else writes the freed pages.  A swapped
+ *     sequence keeps its length; append_slot, fork and block_table refuse it
+ *     with PA_ERR_SWAPPED; free returns its host blocks.  A page still shared
+ *     with a resident sequence stays with that holder; the swapped copy is
+ *     private from then on.  cap < the sequence's pages is PA_ERR_INVALID_ARG.
  * ------------------------------------------------------------------------- */
 typedef struct pa_bm pa_bm;
 
@@ -258,6 +291,16 @@ int pa_bm_append_slots(pa_bm* bm, const int64_t* seq_ids, int n, int64_t* slots,
 /* Fill tables [n][max_blocks] (padded with -1) and context_lens [n] for seq_ids. */
 int pa_bm_build_block_tables(const pa_bm* bm, const int64_t* seq_ids, int n, int32_t* tables,
                              int max_blocks, int32_t* context_lens);
+/* Give the manager a host pool of num_host_blocks blocks (free list as for the
+ * device pool: initial_host_order or 0..num_host_blocks-1).  Once per manager. */
+int pa_bm_enable_swap(pa_bm* bm, int num_host_blocks, const int32_t* initial_host_order);
+/* Swap a resident sequence out / a swapped one in; pairs [cap][2] as above,
+ * *num_pairs = the sequence's page count. */
+int pa_bm_swap_out(pa_bm* bm, int64_t seq_id, int64_t* pairs, int cap, int* num_pairs);
+int pa_bm_swap_in(pa_bm* bm, int64_t seq_id, int64_t* pairs, int cap, int* num_pairs);
+int pa_bm_num_free_host(const pa_bm* bm);
+/* Copy the host free list, bottom to top, up to cap; returns its length. */
+int pa_bm_host_free_list(const pa_bm* bm, int32_t* out, int cap);
 
 #ifdef __cplusplus
 }

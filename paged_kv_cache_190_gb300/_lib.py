@@ -13,16 +13,18 @@ _LIB_PATH = os.path.join(PKG, "libpagedattn.so")
 PA_F32, PA_BF16 = 0, 1
 PA_OK = 0
 PA_ERR_OUT_OF_BLOCKS = -3
+PA_ERR_SWAPPED = -8
 PA_DEVERR_BAD_BLOCK, PA_DEVERR_BAD_LENGTH, PA_DEVERR_BAD_SLOT, PA_DEVERR_TIMEOUT = 1, 2, 4, 8
 
 # Every function include/pa.h declares (checked by the tests).
 EXPORTED_SYMBOLS = [
     "pa_get_error_string", "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_chunk_tokens",
     "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc", "pa_debug_set_wait_limit",
-    "pa_read_device_errors", "pa_reshape_and_cache_fp8", "pa_decode_fp8",
+    "pa_read_device_errors", "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_swap_blocks",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq", "pa_bm_append_slot", "pa_bm_fork",
     "pa_bm_free", "pa_bm_block_table", "pa_bm_refcount", "pa_bm_num_free", "pa_bm_free_list",
-    "pa_bm_stats", "pa_bm_append_slots", "pa_bm_build_block_tables",
+    "pa_bm_stats", "pa_bm_append_slots", "pa_bm_build_block_tables", "pa_bm_enable_swap",
+    "pa_bm_swap_out", "pa_bm_swap_in", "pa_bm_num_free_host", "pa_bm_host_free_list",
 ]
 
 _vp = ctypes.c_void_p
@@ -47,6 +49,7 @@ _SIGNATURES = {
                                         _i32, _i32, _vp, _vp]),
     "pa_decode_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _i32, _i32,
                              _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
+    "pa_swap_blocks": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _sz, _i32, _i32, _vp, _vp]),
     "pa_debug_set_wait_limit": (_i32, [_i32]),
     "pa_read_device_errors": (_i32, [_vp, _pi32, _i32, _vp]),
     "pa_bm_create": (_i32, [_i32, _i32, _pi32, ctypes.POINTER(_vp)]),
@@ -62,6 +65,11 @@ _SIGNATURES = {
     "pa_bm_stats": (_i32, [_vp, _pi64]),
     "pa_bm_append_slots": (_i32, [_vp, _pi64, _i32, _pi64, _pi64, _pi32, _pi32]),
     "pa_bm_build_block_tables": (_i32, [_vp, _pi64, _i32, _pi32, _i32, _pi32]),
+    "pa_bm_enable_swap": (_i32, [_vp, _i32, _pi32]),
+    "pa_bm_swap_out": (_i32, [_vp, _i64, _pi64, _i32, _pi32]),
+    "pa_bm_swap_in": (_i32, [_vp, _i64, _pi64, _i32, _pi32]),
+    "pa_bm_num_free_host": (_i32, [_vp]),
+    "pa_bm_host_free_list": (_i32, [_vp, _pi32, _i32]),
 }
 
 _lock = threading.Lock()
@@ -100,10 +108,16 @@ class OutOfBlocks(PaError):
     pass
 
 
+class Swapped(PaError):
+    pass
+
+
 def _check(rc: int, what: str):
     if rc != PA_OK:
         if rc == PA_ERR_OUT_OF_BLOCKS:
             raise OutOfBlocks(rc, what)
+        if rc == PA_ERR_SWAPPED:
+            raise Swapped(rc, what)
         raise PaError(rc, what)
 
 
@@ -166,6 +180,28 @@ def pa_copy_blocks(k_cache, v_cache, src_dst_pairs, device_errors=None, stream=N
                                   int(src_dst_pairs.shape[0]), block_bytes, int(NB),
                                   _ptr(device_errors), _stream(stream, k_cache.device))
     _check(rc, "pa_copy_blocks")
+
+
+def pa_swap_blocks(src_k, src_v, dst_k, dst_v, src_dst_pairs, device_errors=None, stream=None):
+    """dst[d] = src[s] for each (s, d) row of src_dst_pairs (int64 [P, 2] on the
+    device), K and V; pools [blocks, ...] of equal block size, each in device
+    memory or pinned host memory (see pa.h)."""
+    import torch
+    for n, t in (("src_k", src_k), ("src_v", src_v), ("dst_k", dst_k), ("dst_v", dst_v)):
+        if not t.is_contiguous() or not (t.is_cuda or t.is_pinned()):
+            raise ValueError(f"{n} must be a contiguous CUDA tensor or pinned host tensor")
+    _need_cuda_contig("src_dst_pairs", src_dst_pairs)
+    if src_dst_pairs.dtype != torch.int64:
+        raise TypeError("src_dst_pairs must be int64")
+    block_bytes = src_k[0].numel() * src_k.element_size()
+    if dst_k[0].numel() * dst_k.element_size() != block_bytes:
+        raise ValueError("the two pools have different block sizes")
+    device = src_dst_pairs.device
+    rc = library().pa_swap_blocks(_ptr(src_k), _ptr(src_v), _ptr(dst_k), _ptr(dst_v),
+                                  _ptr(src_dst_pairs), int(src_dst_pairs.shape[0]), block_bytes,
+                                  int(src_k.shape[0]), int(dst_k.shape[0]), _ptr(device_errors),
+                                  _stream(stream, device))
+    _check(rc, "pa_swap_blocks")
 
 
 def pa_decode_chunk_tokens(num_seqs, num_kv_heads, block_size, max_context_len) -> int:
@@ -416,6 +452,41 @@ class BlockManager:
                                           ctypes.byref(num_cow), ctypes.byref(done))
         _check(rc, "pa_bm_append_slots")
         return slots[:n], pairs[:num_cow.value]
+
+    # swapping to a host pool
+    def enable_swap(self, num_host_blocks: int, initial_host_order=None):
+        order = None
+        if initial_host_order is not None:
+            self._host_order = np.ascontiguousarray(initial_host_order, dtype=np.int32)
+            order = _i32p(self._host_order)
+        _check(self._lib.pa_bm_enable_swap(self._h, int(num_host_blocks), order),
+               "pa_bm_enable_swap")
+        self.num_host_blocks = int(num_host_blocks)
+
+    def _swap(self, fn, seq_id, what):
+        # a sequence holds at most every block of the pool it moves from
+        cap = max(self.num_blocks, getattr(self, "num_host_blocks", 0))
+        pairs = np.zeros((cap, 2), dtype=np.int64)
+        n = ctypes.c_int()
+        _check(fn(self._h, int(seq_id), _i64p(pairs), cap, ctypes.byref(n)), what)
+        return pairs[:n.value]
+
+    def swap_out(self, seq_id: int):
+        """Returns int64 [pages, 2] (device page, host block), table order."""
+        return self._swap(self._lib.pa_bm_swap_out, seq_id, "pa_bm_swap_out")
+
+    def swap_in(self, seq_id: int):
+        """Returns int64 [pages, 2] (host block, device page), table order."""
+        return self._swap(self._lib.pa_bm_swap_in, seq_id, "pa_bm_swap_in")
+
+    def num_free_host(self) -> int:
+        return self._lib.pa_bm_num_free_host(self._h)
+
+    def host_free_list(self):
+        n = self._lib.pa_bm_host_free_list(self._h, None, 0)
+        out = np.zeros(max(n, 1), dtype=np.int32)
+        self._lib.pa_bm_host_free_list(self._h, _i32p(out), n)
+        return out[:n].tolist()
 
     def build_block_tables(self, seq_ids, max_blocks: int):
         ids = np.ascontiguousarray(seq_ids, dtype=np.int64)

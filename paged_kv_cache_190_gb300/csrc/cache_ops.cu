@@ -110,7 +110,67 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4* __restrict__ k_
   }
 }
 
+// Page copy between two pools (device <-> pinned host memory for swapping).
+// Block (pair, part); each thread keeps four 16-byte loads of K and four of V in
+// flight before storing, because a load over the host link takes microseconds.
+__global__ void __launch_bounds__(256) swap_pages_kernel(
+    const uint4* __restrict__ src_k, const uint4* __restrict__ src_v, uint4* __restrict__ dst_k,
+    uint4* __restrict__ dst_v, const int64_t* __restrict__ pairs, int64_t chunks_per_block,
+    int num_src_blocks, int num_dst_blocks, int32_t* device_errors) {
+  constexpr int kU = 4;
+  const int64_t src = pairs[2 * blockIdx.x];
+  const int64_t dst = pairs[2 * blockIdx.x + 1];
+  if (src < 0 || src >= num_src_blocks || dst < 0 || dst >= num_dst_blocks) {
+    if (threadIdx.x == 0 && blockIdx.y == 0) report(device_errors, PA_DEVERR_BAD_BLOCK);
+    return;
+  }
+  const uint4* ks = src_k + src * chunks_per_block;
+  const uint4* vs = src_v + src * chunks_per_block;
+  uint4* kd = dst_k + dst * chunks_per_block;
+  uint4* vd = dst_v + dst * chunks_per_block;
+  const int64_t step = static_cast<int64_t>(gridDim.y) * blockDim.x;
+  for (int64_t i0 = blockIdx.y * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+       i0 < chunks_per_block; i0 += kU * step) {
+    uint4 a[kU], b[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t i = i0 + u * step;
+      if (i < chunks_per_block) {
+        a[u] = ks[i];
+        b[u] = vs[i];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int64_t i = i0 + u * step;
+      if (i < chunks_per_block) {
+        kd[i] = a[u];
+        vd[i] = b[u];
+      }
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                               const int64_t* pairs, int num_pairs, size_t block_bytes,
+                               int num_src_blocks, int num_dst_blocks, int32_t* device_errors,
+                               cudaStream_t stream) {
+  if (num_pairs == 0) return cudaSuccess;
+  const int64_t chunks = static_cast<int64_t>(block_bytes / 16);
+  const int threads = 256;
+  // parts per pair: about four chunks per thread per part
+  int64_t parts = (chunks + 4 * threads - 1) / (4 * threads);
+  if (parts < 1) parts = 1;
+  if (parts > 64) parts = 64;
+  dim3 grid(static_cast<unsigned>(num_pairs), static_cast<unsigned>(parts));
+  swap_pages_kernel<<<grid, threads, 0, stream>>>(
+      static_cast<const uint4*>(src_k), static_cast<const uint4*>(src_v),
+      static_cast<uint4*>(dst_k), static_cast<uint4*>(dst_v), pairs, chunks, num_src_blocks,
+      num_dst_blocks, device_errors);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
                                      const int64_t* slot_mapping, int num_tokens,

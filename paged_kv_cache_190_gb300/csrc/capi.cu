@@ -65,6 +65,7 @@ const char* pa_get_error_string(int status) {
     case PA_ERR_NOT_FOUND: return "unknown sequence id";
     case PA_ERR_EXISTS: return "sequence id already in use";
     case PA_ERR_WORKSPACE: return "decode workspace missing, misaligned or too small";
+    case PA_ERR_SWAPPED: return "the sequence is swapped out to host memory";
     default: return "unknown status";
   }
 }
@@ -96,6 +97,23 @@ int pa_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst_pairs, i
   const cudaError_t e =
       pa::launch_copy_blocks(k_cache, v_cache, src_dst_pairs, num_pairs, block_bytes, num_blocks,
                              device_errors, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                   const int64_t* src_dst_pairs, int num_pairs, size_t block_bytes,
+                   int num_src_blocks, int num_dst_blocks, int32_t* device_errors, void* stream) {
+  if (num_pairs < 0 || num_src_blocks <= 0 || num_dst_blocks <= 0 || block_bytes == 0 ||
+      block_bytes % 16 != 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PA_OK;
+  if (!src_k || !src_v || !dst_k || !dst_v || !src_dst_pairs || !aligned16(src_k) ||
+      !aligned16(src_v) || !aligned16(dst_k) || !aligned16(dst_v))
+    return PA_ERR_INVALID_ARG;
+  const cudaError_t e = pa::launch_swap_blocks(src_k, src_v, dst_k, dst_v, src_dst_pairs,
+                                               num_pairs, block_bytes, num_src_blocks,
+                                               num_dst_blocks, device_errors,
+                                               static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -62,6 +62,11 @@ cudaError_t launch_reshape_and_cache_fp8(const void* k, const void* v, void* k_c
                                          int block_size, int num_blocks, int32_t* device_errors,
                                          cudaStream_t stream);
 
+cudaError_t launch_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                               const int64_t* pairs, int num_pairs, size_t block_bytes,
+                               int num_src_blocks, int num_dst_blocks, int32_t* device_errors,
+                               cudaStream_t stream);
+
 cudaError_t launch_copy_blocks(void* k_cache, void* v_cache, const int64_t* pairs, int num_pairs,
                                size_t block_bytes, int num_blocks, int32_t* device_errors,
                                cudaStream_t stream);

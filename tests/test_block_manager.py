@@ -20,10 +20,22 @@ def _is_oom(fn):
     return False
 
 
-@pytest.mark.parametrize("name", ["bm_teaching_trace.txt", "bm_refcount_cow_trace.txt"])
+def _is_swapped(fn):
+    try:
+        fn()
+    except pa.Swapped:
+        return True
+    return False
+
+
+@pytest.mark.parametrize("name", ["bm_teaching_trace.txt", "bm_refcount_cow_trace.txt",
+                                  "bm_swap_trace.txt"])
 def test_hand_trace(name):
     header, steps = load_trace(name)
-    replay(pa.BlockManager(header["num_pages"], header["page_size"]), steps, _is_oom)
+    bm = pa.BlockManager(header["num_pages"], header["page_size"])
+    if "host_blocks" in header:
+        bm.enable_swap(header["host_blocks"])
+    replay(bm, steps, _is_oom, _is_swapped)
 
 
 def _state(bm, nb, live, refcount):
@@ -177,3 +189,68 @@ def test_shared_prefix_script_matches_oracle_and_returns_every_page():
     assert prod.num_free() == script.num_blocks
     assert sorted(prod.free_list()) == list(range(script.num_blocks))
     assert all(prod.refcount(p) == 0 for p in range(script.num_blocks))
+
+
+@pytest.mark.parametrize("seed", range(16))
+@pytest.mark.parametrize("nb,nh,bs", [(7, 5, 2), (20, 9, 4)])
+def test_swapping_matches_oracle_on_random_operations(seed, nb, nh, bs):
+    """Swap-out / swap-in mixed into the random operations: the copy pairs, the
+    refusals, both free lists and the resident tables match the oracle's."""
+    rng = np.random.default_rng(seed)
+    order, host_order = rng.permutation(nb), rng.permutation(nh)
+    prod, ref = pa.BlockManager(nb, bs, order), oracle.RefBlockManager(nb, bs, order.tolist())
+    prod.enable_swap(nh, host_order)
+    ref.enable_swap(nh, host_order.tolist())
+    resident, swapped = set(), set()
+    for kind, a, b in pa_inputs.random_bm_ops(seed * 11 + nb, 500, swap=True):
+        if kind == "add" and (a in resident or a in swapped):
+            continue
+        if kind == "fork" and (b in resident or b in swapped):
+            continue
+        if kind in ("append", "fork", "free", "swapout") and a not in resident | swapped:
+            continue
+        if kind == "swapin" and a not in resident | swapped:
+            continue
+        results = []
+        for bm, errs in ((prod, (pa.OutOfBlocks, pa.Swapped, pa.PaError)),
+                         (ref, (oracle.OutOfBlocks, oracle.Swapped, KeyError))):
+            try:
+                if kind == "add":
+                    bm.add_seq(a); r = "ok"
+                elif kind == "append":
+                    r = tuple(bm.append_slot(a))
+                elif kind == "fork":
+                    bm.fork(a, b); r = "ok"
+                elif kind == "free":
+                    bm.free(a); r = "ok"
+                elif kind == "swapout":
+                    r = [tuple(int(x) for x in p) for p in bm.swap_out(a)]
+                else:
+                    r = [tuple(int(x) for x in p) for p in bm.swap_in(a)]
+            except errs as e:
+                r = {"Swapped": "swapped", "OutOfBlocks": "oom"}.get(type(e).__name__, "refused")
+            results.append(r)
+        r_prod, r_ref = results
+        assert r_prod == r_ref, (kind, a, b, r_prod, r_ref)
+        if r_ref not in ("oom", "swapped", "refused"):
+            if kind == "add":
+                resident.add(a)
+            elif kind == "fork":
+                resident.add(b)
+            elif kind == "free":
+                resident.discard(a); swapped.discard(a)
+            elif kind == "swapout":
+                resident.discard(a); swapped.add(a)
+            elif kind == "swapin":
+                swapped.discard(a); resident.add(a)
+        assert list(prod.free_list()) == ref.free_list()
+        assert list(prod.host_free_list()) == ref.host_free_list()
+        for q in sorted(resident):
+            got, L = prod.block_table(q)
+            assert (list(got), L) == ref.block_table(q)
+        assert prod.stats() == ref.stats()
+    for q in sorted(resident | swapped):
+        prod.free(q)
+    assert sorted(prod.free_list()) == list(range(nb))
+    assert sorted(prod.host_free_list()) == list(range(nh))
+
