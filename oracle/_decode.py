@@ -152,3 +152,34 @@ def decode_kv8_f64(q, k_cache, v_cache, block_tables, context_lens, scale, k_sca
     if rc != 0:
         raise ValueError(f"oracle_decode_kv8_f64 refused the input (status {rc})")
     return out
+
+
+def decode_multi_f64(q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
+                     dtype: str, rows=None, threads: int = 0) -> np.ndarray:
+    """fp64 paged attention for q_len new tokens per sequence, causal.
+
+    q [B, q_len, Hq, D]; context_lens counts all q_len new tokens, so query token
+    j of sequence b sits at position L_b - q_len + j and attends to positions
+    0 .. L_b - q_len + j of its own sequence (each new token sees the prefix and
+    the new tokens before it, itself included).  That is the single-token decode
+    of a sequence cut at that position, so this is written as exactly that:
+    one decode row per (b, j) over the same block table with length
+    L_b - q_len + j + 1 (rows with no key return zeros).
+    Returns float64 [B, q_len, Hq, D], or [len(rows), D] for (b, j, i) triples.
+    """
+    q = np.asarray(q)
+    B, q_len, Hq, D = q.shape
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    cl = np.asarray(context_lens, dtype=np.int64)
+    vlens = (cl[:, None] - q_len + np.arange(q_len)[None, :] + 1).clip(min=0).astype(np.int32)
+    vq = np.ascontiguousarray(q.reshape(B * q_len, Hq, D))
+    vbt = np.ascontiguousarray(np.repeat(bt, q_len, axis=0))
+    if rows is None:
+        out = decode_f64(vq, k_cache, v_cache, vbt, vlens.reshape(-1), scale, num_kv_heads, dtype,
+                         threads=threads)
+        return out.reshape(B, q_len, Hq, D)
+    trip = np.asarray(rows, dtype=np.int64).reshape(-1, 3)
+    vrows = np.stack([trip[:, 0] * q_len + trip[:, 1], trip[:, 2]], axis=1)
+    return decode_f64(vq, k_cache, v_cache, vbt, vlens.reshape(-1), scale, num_kv_heads, dtype,
+                      rows=vrows, threads=threads)
+

@@ -334,3 +334,52 @@ def test_pins_catch_planted_mistake(name, tmp_path):
     want = _sdpa_reference(q, k_log, v_log, lens, scale, Hkv, dtype)
     caught = rc != 0 or not np.all(np.isfinite(out)) or np.max(np.abs(out - want)) > 1e-6
     assert caught, f"planted mistake '{name}' was not caught by the dense pin"
+
+
+# ------------------------------------- q_len > 1: causal attention over the pages
+def _causal_sdpa_reference(q, k_log, v_log, lens, scale, Hkv, dtype):
+    """Dense fp64 SDPA with an explicit mask: query token j of sequence b (at
+    position L_b - q_len + j) attends to keys t <= L_b - q_len + j."""
+    B, q_len, Hq, D = q.shape
+    G = Hq // Hkv
+    out = np.zeros((B, q_len, Hq, D))
+    for b, L in enumerate(lens):
+        qt = _torch_widen(q[b], dtype).permute(1, 0, 2)                 # [Hq, q_len, D]
+        kt = _torch_widen(k_log[b], dtype).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        vt = _torch_widen(v_log[b], dtype).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        pos = torch.arange(q_len)[:, None] + (L - q_len)
+        mask = torch.arange(L)[None, :] <= pos                          # [q_len, L]
+        o = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask, scale=scale)
+        out[b] = o.permute(1, 0, 2).numpy()
+    return out
+
+
+@pytest.mark.parametrize("dtype,q_len,Hq,Hkv,bs", [("f32", 4, 4, 4, 16), ("bf16", 2, 8, 2, 16),
+                                                   ("bf16", 8, 2, 2, 32), ("f32", 3, 8, 4, 16)])
+def test_multi_token_oracle_equals_causal_dense_sdpa(dtype, q_len, Hq, Hkv, bs):
+    lens = [q_len, 19, 70]
+    D = 64
+    rng, k_log, v_log, _ = _random_logical(41 + q_len, lens, Hq, Hkv, D, dtype)
+    q = pa_inputs.to_storage(rng.standard_normal((len(lens), q_len, Hq, D), dtype=np.float32), dtype)
+    mb = max((L + bs - 1) // bs for L in lens)
+    NB = sum((L + bs - 1) // bs for L in lens) + 2
+    tables = _tables_from_perm(rng.permutation(NB).astype(np.int32), lens, bs, mb)
+    kp, vp = _scatter_into_pool(k_log, v_log, tables, lens, NB, bs, dtype)
+    got = oracle.decode_multi_f64(q, kp, vp, tables, np.array(lens, np.int32), 0.125, Hkv, dtype)
+    want = _causal_sdpa_reference(q, k_log, v_log, lens, 0.125, Hkv, dtype)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+    rows = [(1, q_len - 1, Hq - 1), (2, 0, 0), (0, q_len - 1, 0)]
+    sel = oracle.decode_multi_f64(q, kp, vp, tables, np.array(lens, np.int32), 0.125, Hkv, dtype,
+                                  rows=rows)
+    np.testing.assert_array_equal(sel, np.stack([got[b, j, i] for b, j, i in rows]))
+
+
+def test_multi_token_with_one_token_is_decode():
+    dtype, Hq, Hkv, D, bs = "bf16", 8, 2, 128, 16
+    lens = [5, 40]
+    rng, k_log, v_log, q = _random_logical(47, lens, Hq, Hkv, D, dtype)
+    tables = _tables_from_perm(rng.permutation(6).astype(np.int32), lens, bs, 3)
+    kp, vp = _scatter_into_pool(k_log, v_log, tables, lens, 6, bs, dtype)
+    cl = np.array(lens, np.int32)
+    multi = oracle.decode_multi_f64(q[:, None], kp, vp, tables, cl, 0.09, Hkv, dtype)
+    np.testing.assert_array_equal(multi[:, 0], oracle.decode_f64(q, kp, vp, tables, cl, 0.09, Hkv, dtype))
