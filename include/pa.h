@@ -187,6 +187,29 @@ int pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void*
                       int32_t* device_errors, void* stream);
 
 /*
+ * Paged attention for q_len new tokens per sequence, causal among them -- the
+ * verify step of speculative decoding ("mlx-paged-attention", future plans:
+ * "speculative decoding"), or a short chunked extend.  q and out are
+ * [num_seqs][q_len][num_q_heads][head_dim] (token-major), in the pool's element
+ * type.  context_lens[b] counts all q_len new tokens (written beforehand with
+ * pa_reshape_and_cache, q_len slots per sequence); new token j of sequence b
+ * sits at position L_b - q_len + j and attends to positions 0 .. L_b - q_len + j:
+ *     out[b][j][i] = softmax_t<=L_b-q_len+j (scale q[b][j][i] . K_t) V_t.
+ * One pass over each (sequence, kv head)'s pages serves all q_len x group query
+ * rows; q_len * (num_q_heads / num_kv_heads) must be 1, 2, 4 or 8
+ * (PA_ERR_UNSUPPORTED otherwise).  A length below q_len sets
+ * PA_DEVERR_BAD_LENGTH (the rows with no visible key are zero).  Workspace:
+ * pa_decode_workspace_size(num_seqs, q_len * num_q_heads, ...).  Other
+ * arguments and rules as pa_decode; q_len = 1 is pa_decode.
+ */
+int pa_decode_multi(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, const int32_t* context_lens, float scale,
+                    int num_kv_heads, int num_seqs, int num_q_heads, int q_len, int head_dim,
+                    int block_size, int num_blocks, int max_blocks_per_seq, int max_context_len,
+                    pa_dtype dtype, int chunk_tokens, void* workspace, size_t workspace_bytes,
+                    int32_t* device_errors, void* stream);
+
+/*
  * float8 e4m3 KV pools.  "mlx-paged-attention" (future plans) names
  * quantization as the next optimisation; the pages give no format, so this is
  * the plainest one: the pools hold one-byte e4m3 codes (1 sign, 4 exponent bits

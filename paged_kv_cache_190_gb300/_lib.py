@@ -21,6 +21,7 @@ EXPORTED_SYMBOLS = [
     "pa_get_error_string", "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_chunk_tokens",
     "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc", "pa_debug_set_wait_limit",
     "pa_read_device_errors", "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_swap_blocks",
+    "pa_decode_multi",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq", "pa_bm_append_slot", "pa_bm_fork",
     "pa_bm_free", "pa_bm_block_table", "pa_bm_refcount", "pa_bm_num_free", "pa_bm_free_list",
     "pa_bm_stats", "pa_bm_append_slots", "pa_bm_build_block_tables", "pa_bm_enable_swap",
@@ -50,6 +51,9 @@ _SIGNATURES = {
     "pa_decode_fp8": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _vp, _vp, _i32, _i32,
                              _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _vp, _vp]),
     "pa_swap_blocks": (_i32, [_vp, _vp, _vp, _vp, _vp, _i32, _sz, _i32, _i32, _vp, _vp]),
+    "pa_decode_multi": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _i32, _i32, _i32,
+                               _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _vp,
+                               _vp]),
     "pa_debug_set_wait_limit": (_i32, [_i32]),
     "pa_read_device_errors": (_i32, [_vp, _pi32, _i32, _vp]),
     "pa_bm_create": (_i32, [_i32, _i32, _pi32, ctypes.POINTER(_vp)]),
@@ -245,6 +249,34 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_k
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(device_errors),
         _stream(stream, q.device))
     _check(rc, "pa_decode")
+    return out
+
+
+def pa_decode_multi(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
+                    max_context_len, workspace=None, chunk_tokens=0, device_errors=None,
+                    stream=None):
+    """Causal paged attention for q_len new tokens per sequence: out, q
+    [B, q_len, Hq, D]; the rest as pa_decode (see pa.h)."""
+    import torch
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("block_tables", block_tables), ("context_lens", context_lens)):
+        _need_cuda_contig(n, t)
+    if block_tables.dtype != torch.int32 or context_lens.dtype != torch.int32:
+        raise TypeError("block_tables and context_lens must be int32")
+    B, q_len, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    if int(Hkv) != int(num_kv_heads):
+        raise ValueError("num_kv_heads does not match the cache shape")
+    if workspace is None:
+        nbytes = pa_decode_workspace_size(B, q_len * Hq, Hkv, D, bs, max_context_len, chunk_tokens)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    rc = library().pa_decode_multi(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        float(scale), int(num_kv_heads), int(B), int(Hq), int(q_len), int(D), int(bs), int(NB),
+        int(block_tables.shape[1]), int(max_context_len), _dtype_code(q), int(chunk_tokens),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(device_errors),
+        _stream(stream, q.device))
+    _check(rc, "pa_decode_multi")
     return out
 
 

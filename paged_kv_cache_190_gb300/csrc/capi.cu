@@ -149,15 +149,18 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
                   const int32_t* block_tables, const int32_t* context_lens, float scale,
                   int num_kv_heads, int num_seqs, int num_q_heads, int head_dim, int block_size,
                   int num_blocks, int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
-                  bool kv8, const float* k_scale, const float* v_scale, int chunk_tokens,
-                  void* workspace, size_t workspace_bytes, int32_t* device_errors,
-                  void* stream) {
+                  bool kv8, const float* k_scale, const float* v_scale, int q_len,
+                  int chunk_tokens, void* workspace, size_t workspace_bytes,
+                  int32_t* device_errors, void* stream) {
   if (num_kv_heads <= 0 || num_q_heads <= 0 || num_seqs < 0 || num_blocks <= 0 ||
       max_blocks_per_seq <= 0 || max_context_len < 0)
     return PA_ERR_INVALID_ARG;
   if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
   const int group = num_q_heads / num_kv_heads;
-  if (group != 1 && group != 2 && group != 4 && group != 8) return PA_ERR_UNSUPPORTED;
+  if (q_len < 1) return PA_ERR_INVALID_ARG;
+  // an item holds the q_len new tokens of one kv head's group: 1, 2, 4 or 8 rows
+  const int rows = q_len * group;
+  if (rows != 1 && rows != 2 && rows != 4 && rows != 8) return PA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_context_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
     return PA_ERR_INVALID_ARG;
   if (num_seqs == 0) return PA_OK;
@@ -174,7 +177,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   else if (!valid_chunk(chunk, block_size))
     return PA_ERR_INVALID_ARG;
   const pa::WorkspaceLayout lay =
-      pa::decode_workspace_layout(num_seqs, num_q_heads, head_dim, max_context_len, chunk);
+      pa::decode_workspace_layout(num_seqs, q_len * num_q_heads, head_dim, max_context_len, chunk);
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < lay.total)
     return PA_ERR_WORKSPACE;
@@ -197,6 +200,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.max_context_len = max_context_len;
   a.chunk_tokens = chunk;
+  a.q_len = q_len;
   a.bf16 = dtype == PA_BF16;
   a.kv8 = kv8 ? 1 : 0;
   a.k_scale = kv8 ? k_scale : nullptr;
@@ -228,7 +232,7 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
   if (!elt_size(dtype) || !supported_shape(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
   return decode_common(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
                        num_seqs, num_q_heads, head_dim, block_size, num_blocks,
-                       max_blocks_per_seq, max_context_len, dtype, false, nullptr, nullptr,
+                       max_blocks_per_seq, max_context_len, dtype, false, nullptr, nullptr, 1,
                        chunk_tokens, workspace, workspace_bytes, device_errors, stream);
 }
 
@@ -241,7 +245,20 @@ int pa_decode_fp8(void* out, const void* q, const void* k_cache, const void* v_c
   if (head_dim != 128 || !supported_shape(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
   return decode_common(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
                        num_seqs, num_q_heads, head_dim, block_size, num_blocks,
-                       max_blocks_per_seq, max_context_len, PA_BF16, true, k_scale, v_scale,
+                       max_blocks_per_seq, max_context_len, PA_BF16, true, k_scale, v_scale, 1,
+                       chunk_tokens, workspace, workspace_bytes, device_errors, stream);
+}
+
+int pa_decode_multi(void* out, const void* q, const void* k_cache, const void* v_cache,
+                    const int32_t* block_tables, const int32_t* context_lens, float scale,
+                    int num_kv_heads, int num_seqs, int num_q_heads, int q_len, int head_dim,
+                    int block_size, int num_blocks, int max_blocks_per_seq, int max_context_len,
+                    pa_dtype dtype, int chunk_tokens, void* workspace, size_t workspace_bytes,
+                    int32_t* device_errors, void* stream) {
+  if (!elt_size(dtype) || !supported_shape(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
+  return decode_common(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
+                       num_seqs, num_q_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_context_len, dtype, false, nullptr, nullptr, q_len,
                        chunk_tokens, workspace, workspace_bytes, device_errors, stream);
 }
 

@@ -65,8 +65,9 @@ __global__ void __launch_bounds__(kQPrepWarps * 32) q_prep_fp8_kernel(
 // together (entry -> sequence by binary search over the tile's offsets).
 __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(
     const int32_t* __restrict__ context_lens, int num_seqs, int chunk_tokens, int max_len,
-    int32_t* __restrict__ header, int32_t* __restrict__ chunk_base, int4* __restrict__ work,
-    uint4* __restrict__ out, int64_t row_chunks, int32_t* device_errors) {
+    int q_len, int32_t* __restrict__ header, int32_t* __restrict__ chunk_base,
+    int4* __restrict__ work, uint4* __restrict__ out, int64_t row_chunks,
+    int32_t* device_errors) {
   __shared__ int warp_sums[kPlanThreads / 32];
   __shared__ int first_s[kPlanThreads + 1];     // tile-local exclusive offsets (+ total)
   __shared__ int len_s[kPlanThreads];
@@ -85,6 +86,8 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(
         report(device_errors, PA_DEVERR_BAD_LENGTH);
         L = L < 0 ? 0 : max_len;
       }
+      // fewer tokens than new tokens: the first new tokens see no key (zero rows)
+      if (L > 0 && L < q_len) report(device_errors, PA_DEVERR_BAD_LENGTH);
       n = (L + chunk_tokens - 1) / chunk_tokens;
     }
     int x = n;  // inclusive scan within the warp
@@ -143,11 +146,13 @@ constexpr int kWideMergeWarps = 16;
 //   M = max lse_c, S = sum 2^(lse_c - M), acc = sum 2^(lse_c - M) o_c.
 template <int CPL>
 struct LseAcc {
-  float M = -INFINITY, S = 0.f, acc[CPL] = {};
+  // M starts finite and below any real log-sum-exp, so that a chunk in which
+  // the row saw no token (lse = -inf) adds weight 2^-inf = 0 instead of NaN
+  float M = -3.0e38f, S = 0.f, acc[CPL] = {};
 
   __device__ __forceinline__ void add(float lse, const float* v) {
     const float Mn = fmaxf(M, lse);
-    const float sc = fast_exp2(M - Mn);     // 0 on the first chunk (M = -inf)
+    const float sc = fast_exp2(M - Mn);     // 0 on the first real chunk
     const float w = fast_exp2(lse - Mn);
     S = fmaf(S, sc, w);
 #pragma unroll
@@ -213,7 +218,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(
     st.add(part_lse[prow], v);
   }
   float r[CPL];
-  const float inv = 1.f / st.S;
+  const float inv = st.S > 0.f ? 1.f / st.S : 0.f;   // 0: the row saw no token
 #pragma unroll
   for (int k = 0; k < CPL; ++k) r[k] = st.acc[k] * inv;
   store_row<BF16, CPL>(out, row * D + lane * CPL, r);
@@ -255,7 +260,7 @@ __global__ void __launch_bounds__(kWideMergeWarps * 32) decode_merge_wide_kernel
   }
   __syncthreads();
   if (warp != 0) return;
-  float M = -INFINITY;
+  float M = -3.0e38f;
 #pragma unroll
   for (int w = 0; w < kWideMergeWarps; ++w) M = fmaxf(M, sM[w]);
   float S = 0.f, r[CPL] = {};
@@ -266,7 +271,7 @@ __global__ void __launch_bounds__(kWideMergeWarps * 32) decode_merge_wide_kernel
 #pragma unroll
     for (int k = 0; k < CPL; ++k) r[k] = fmaf(f, sacc[w][lane * CPL + k], r[k]);
   }
-  const float inv = 1.f / S;
+  const float inv = S > 0.f ? 1.f / S : 0.f;
 #pragma unroll
   for (int k = 0; k < CPL; ++k) r[k] *= inv;
   store_row<BF16, CPL>(out, row * D + lane * CPL, r);
@@ -292,7 +297,8 @@ cudaError_t launch_dependent(void (*kernel)(Args...), unsigned blocks, unsigned 
 
 template <bool BF16, int CPL>
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream) {
-  const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
+  const int rows_q = a.q_len * a.num_q_heads;         // query rows per sequence
+  const int64_t rows = static_cast<int64_t>(a.num_seqs) * rows_q;
   const int64_t max_chunks_per_seq = (static_cast<int64_t>(a.max_context_len) + a.chunk_tokens - 1) /
                                      a.chunk_tokens;
   if (max_chunks_per_seq >= 32)
@@ -300,12 +306,12 @@ cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream) {
                             kWideMergeWarps * 32, stream,
                             static_cast<const int32_t*>(a.ws.chunk_base),
                             static_cast<const float*>(a.ws.part_lse),
-                            static_cast<const float*>(a.ws.part_out), a.out, a.num_q_heads);
+                            static_cast<const float*>(a.ws.part_out), a.out, rows_q);
   const unsigned blocks = static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps);
   return launch_dependent(decode_merge_kernel<BF16, CPL>, blocks, kMergeWarps * 32, stream,
                           static_cast<const int32_t*>(a.ws.chunk_base),
                           static_cast<const float*>(a.ws.part_lse),
-                          static_cast<const float*>(a.ws.part_out), a.out, a.num_q_heads, rows);
+                          static_cast<const float*>(a.ws.part_out), a.out, rows_q, rows);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -377,17 +383,18 @@ WorkspaceLayout decode_workspace_layout(int num_seqs, int num_q_heads, int head_
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (a.num_seqs == 0) return cudaSuccess;
   const int elt = a.bf16 ? 2 : 4;
+  const int rows_q = a.q_len * a.num_q_heads;         // query rows per sequence
   if (a.kv8) {
-    const int64_t rows = static_cast<int64_t>(a.num_seqs) * a.num_q_heads;
+    const int64_t rows = static_cast<int64_t>(a.num_seqs) * rows_q;
     q_prep_fp8_kernel<<<static_cast<unsigned>((rows + kQPrepWarps - 1) / kQPrepWarps),
                         kQPrepWarps * 32, 0, stream>>>(static_cast<const uint2*>(a.q), a.ws.q8,
                                                        rows);
     const cudaError_t qe = cudaGetLastError();
     if (qe != cudaSuccess) return qe;
   }
-  const int64_t row_chunks = static_cast<int64_t>(a.num_q_heads) * a.head_dim * elt / 16;
+  const int64_t row_chunks = static_cast<int64_t>(rows_q) * a.head_dim * elt / 16;
   decode_plan_kernel<<<1, kPlanThreads, 0, stream>>>(
-      a.context_lens, a.num_seqs, a.chunk_tokens, a.max_context_len, a.ws.header,
+      a.context_lens, a.num_seqs, a.chunk_tokens, a.max_context_len, a.q_len, a.ws.header,
       a.ws.chunk_base, a.ws.work, static_cast<uint4*>(a.out), row_chunks, a.device_errors);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -396,7 +403,9 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   DecodeKernelParams kp;
   std::memset(&kp, 0, sizeof(kp));
   const int group = a.num_q_heads / a.num_kv_heads;
-  if (a.kv8 || decode_uses_tensor_cores(a.bf16 != 0, group)) {
+  const int rows = a.q_len * group;                   // rows per (sequence, kv head) item
+  // the kernel instance is chosen by the rows of an item, and so is its consumer
+  if (a.kv8 || decode_uses_tensor_cores(a.bf16 != 0, rows)) {
     const int64_t rows = static_cast<int64_t>(a.num_blocks) * a.num_kv_heads * a.block_size;
     const int kv_elt = a.kv8 ? 1 : 2;
     // one box per page a unit touches: min(page, unit) rows
@@ -428,14 +437,17 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   kp.wait_limit = a.wait_limit < 0 ? kMaxPolls : static_cast<uint32_t>(a.wait_limit);
   kp.k_scale = a.k_scale;
   kp.v_scale = a.v_scale;
+  kp.q_len = a.q_len;
+  kp.group = group;
+  kp.group_log2 = group >= 8 ? 3 : (group >= 4 ? 2 : (group >= 2 ? 1 : 0));
   const int64_t items_upper = a.ws.max_chunks * a.num_kv_heads;
   const int grid = static_cast<int>(items_upper < a.num_sms ? items_upper : a.num_sms);
   int device = 0;
   e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
-  e = a.kv8    ? run_decode_fp8(a.head_dim, group, kp, grid, device, stream)
-      : a.bf16 ? run_decode_bf16(a.head_dim, group, kp, grid, device, stream)
-               : run_decode_f32(a.head_dim, group, kp, grid, device, stream);
+  e = a.kv8    ? run_decode_fp8(a.head_dim, rows, kp, grid, device, stream)
+      : a.bf16 ? run_decode_bf16(a.head_dim, rows, kp, grid, device, stream)
+               : run_decode_f32(a.head_dim, rows, kp, grid, device, stream);
   if (e != cudaSuccess) return e;
   if (a.max_context_len > a.chunk_tokens) {
     if (a.bf16 && a.head_dim == 128) e = launch_merge<true, 4>(a, stream);

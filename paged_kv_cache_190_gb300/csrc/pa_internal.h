@@ -38,6 +38,7 @@ struct DecodeArgs {
   float scale;
   int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks;
   int max_blocks_per_seq, max_context_len, chunk_tokens;
+  int q_len;  // new tokens per sequence (q and out are [num_seqs][q_len][num_q_heads][head_dim])
   int bf16;  // q / out element type: 1 bf16, 0 f32 (and the caches' unless kv8)
   int kv8;   // caches hold float8 e4m3 codes (q / out bf16)
   const float* k_scale;  // kv8: dequantisation scale per kv head, device memory

@@ -68,6 +68,10 @@ constexpr int kItemSlots = 8;        // items the producer may run ahead
 constexpr int kUnitsAhead = 32;      // claimed-but-unissued units a CTA may hold
 constexpr int kSmemBudget = 227 * 1024;
 constexpr unsigned kFull = 0xffffffffu;
+// Start of every running maximum: finite, below any real logit, so that a row
+// with no visible token yet (the first new tokens of a step, in a chunk past
+// them) keeps alpha = 2^0 and probabilities 2^-inf = 0 instead of NaN.
+constexpr float kNoScore = -3.0e38f;
 
 struct ItemDesc {
   int b, h, chunk, len, gchunk, n_units, n_tokens, single, rot;
@@ -172,6 +176,10 @@ struct DecodeKernelParams {
   uint32_t wait_limit;              // polls before a pipeline wait gives up (drains use kMaxPolls)
   const float* k_scale;             // fp8 caches: dequantisation scale per kv head
   const float* v_scale;
+  // new tokens per sequence (causal among themselves) and the query heads per kv
+  // head (a power of two, as log2): an item's G rows are (token j, head g) =
+  // row j * group + g
+  int q_len, group, group_log2;
 };
 
 // Butterfly step over lane bit `mask` (within 8-lane groups): lanes with the
@@ -341,6 +349,9 @@ struct CoreConsumer {
     ps = ps_;
   }
 
+  // new-token index of this lane's row (rows are token-major: j * group + head)
+  __device__ __forceinline__ int row_token(int group_log2) const { return g_lane >> group_log2; }
+
   __device__ __forceinline__ void begin(const char* qs, float scale_log2, float) {
     // q scaled so that logits come out in base 2
 #pragma unroll
@@ -356,14 +367,16 @@ struct CoreConsumer {
     lsum = 0.f;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      m[g] = -INFINITY;
+      m[g] = kNoScore;
 #pragma unroll
       for (int c = 0; c < Tr::CPL; ++c) acc[g][c] = 0.f;
     }
   }
 
+  // qlim: the last of the unit's tokens this lane's row may see (causal among
+  // the new tokens; with one new token it is never below nt - 1)
   template <typename Release>
-  __device__ __forceinline__ void unit(const char* kt, const char* vt, int nt, float,
+  __device__ __forceinline__ void unit(const char* kt, const char* vt, int nt, int qlim, float,
                                        Release release) {
     // ---- scores: 8 lanes per token, 4 tokens per pass
     float part[Tr::N];
@@ -390,10 +403,11 @@ struct CoreConsumer {
     butterfly_level<(Tr::N >= 8 ? Tr::N / 4 : 1)>(part, lane, 1);
     // part[e], e < RC: score of head g_lane, token 4 * ((base % P) + e) + j4
     float umax = -INFINITY;
+    const int lim = min(nt - 1, qlim);          // last token this lane's row sees
 #pragma unroll
     for (int e = 0; e < Tr::RC; ++e) {
       const int t = 4 * ((base % Tr::P) + e) + j4;
-      if (t >= nt) part[e] = -INFINITY;
+      if (t > lim) part[e] = -INFINITY;
       umax = fmaxf(umax, part[e]);
     }
     // max over the lanes that hold the same head
@@ -510,6 +524,10 @@ struct TensorConsumer {
 
   __device__ __forceinline__ void init(int lane_, float*) { lane = lane_; }
 
+  __device__ __forceinline__ int row_token(int group_log2) const {
+    return (lane >> 2) >> group_log2;
+  }
+
   __device__ __forceinline__ void begin(const char* qs, float, float) {
     const int g = lane >> 2, c = lane & 3;
 #pragma unroll
@@ -522,15 +540,15 @@ struct TensorConsumer {
             *reinterpret_cast<const uint32_t*>(qs + g * Tr::QROW_BYTES + (16 * ks + 8 + 2 * c) * 2);
       }
     }
-    m = -INFINITY;
+    m = kNoScore;
     l = 0.f;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   }
 
   template <typename Release>
-  __device__ __forceinline__ void unit(const char* kt, const char* vt, int nt, float scale_log2,
-                                       Release release) {
+  __device__ __forceinline__ void unit(const char* kt, const char* vt, int nt, int qlim,
+                                       float scale_log2, Release release) {
     const uint32_t kb = smem_addr(kt), vb = smem_addr(vt);
     const int mi = lane >> 3, r8 = lane & 7, c = lane & 3;
     const int frow = (mi >> 1) * 8 + r8;          // token row this lane addresses
@@ -553,10 +571,11 @@ struct TensorConsumer {
     // this lane's scores: head t/4, tokens 2c, 2c+1 (n-tile 0) and 8+2c, 9+2c (n-tile 1)
     float sv[4] = {s0[0], s0[1], s1[0], s1[1]};
     const int tk[4] = {2 * c, 2 * c + 1, 8 + 2 * c, 9 + 2 * c};
+    const int lim = min(nt - 1, qlim);            // last token this lane's row sees
     float mx = -INFINITY;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      sv[e] = tk[e] < nt ? sv[e] * scale_log2 : -INFINITY;
+      sv[e] = tk[e] <= lim ? sv[e] * scale_log2 : -INFINITY;
       mx = fmaxf(mx, sv[e]);
     }
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
@@ -687,6 +706,10 @@ struct Fp8TensorConsumer {
 
   __device__ __forceinline__ void init(int lane_, float*) { lane = lane_; }
 
+  __device__ __forceinline__ int row_token(int group_log2) const {
+    return (lane >> 2) >> group_log2;
+  }
+
   __device__ __forceinline__ void begin(const char* qs, float score_scale, float v_scale) {
     const int g = lane >> 2, c = lane & 3;
     float qinv = 0.f;
@@ -697,7 +720,7 @@ struct Fp8TensorConsumer {
     if (qrow) qinv = *reinterpret_cast<const float*>(qs + g * Tr::QROW_BYTES + 2 * D);
     sc = score_scale * qinv;
     vscale = v_scale * (1.f / kPScale);
-    m = -INFINITY;
+    m = kNoScore;
     l = 0.f;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
@@ -707,15 +730,15 @@ struct Fp8TensorConsumer {
   // and V tiles, 4 KiB apart, which keeps the 128-byte swizzle phase); the
   // stage is released after the last block has been read.
   template <typename Release>
-  __device__ __forceinline__ void unit(const char* kt, const char* vt, int nt, float,
+  __device__ __forceinline__ void unit(const char* kt, const char* vt, int nt, int qlim, float,
                                        Release release) {
 #pragma unroll 1
     for (int b = 0; b < NB && 32 * b < nt; ++b)
-      block32(smem_addr(kt) + 4096 * b, smem_addr(vt) + 4096 * b, nt - 32 * b);
+      block32(smem_addr(kt) + 4096 * b, smem_addr(vt) + 4096 * b, nt - 32 * b, qlim - 32 * b);
     release();
   }
 
-  __device__ __forceinline__ void block32(uint32_t kb, uint32_t vb, int nt) {
+  __device__ __forceinline__ void block32(uint32_t kb, uint32_t vb, int nt, int qlim) {
     const int mi = lane >> 3, r8 = lane & 7, c = lane & 3;
     // ---- scores: per step ks, kr[n][0 / 1] = b0 / b1 of n-tile n.  The A rows
     // past the group are free, so q' lo sits in row g + 8 under q' hi in row g:
@@ -745,13 +768,14 @@ struct Fp8TensorConsumer {
     // ---- online softmax over the unit's tokens 8 n + 2c, 8 n + 2c + 1 (row lane / 4)
     float sv[2 * NT];
     float mx = -INFINITY;
+    const int lim = min(nt - 1, qlim);            // last token this lane's row sees
 #pragma unroll
     for (int n = 0; n < NT; ++n)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int tk = 8 * n + 2 * c + e;
         const float v = (sh[n][e] + sh[n][e + 2]) * sc;
-        sv[2 * n + e] = tk < nt ? v : -INFINITY;
+        sv[2 * n + e] = tk <= lim ? v : -INFINITY;
         mx = fmaxf(mx, sv[2 * n + e]);
       }
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
@@ -966,10 +990,15 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
       if (lane == 0) {
         mbar_arrive(&sched_full[slot]);
         mbar_arrive_expect_tx(&item_full[slot], Tr::Q_BYTES);
-        const char* qsrc =
-            p.q + (static_cast<int64_t>(w.x) * p.num_q_heads + static_cast<int64_t>(h) * G) *
-                      Tr::QROW_BYTES;
-        bulk_g2s(qbuf + slot * Tr::Q_BYTES, qsrc, Tr::Q_BYTES, &item_full[slot]);
+        // the G rows: for each new token j, the group's `group` heads (q is
+        // [B][q_len][Hq] rows)
+        for (int j = 0; j < p.q_len; ++j) {
+          const char* qsrc =
+              p.q + ((static_cast<int64_t>(w.x) * p.q_len + j) * p.num_q_heads +
+                     static_cast<int64_t>(h) * p.group) * Tr::QROW_BYTES;
+          bulk_g2s(qbuf + slot * Tr::Q_BYTES + j * p.group * Tr::QROW_BYTES, qsrc,
+                   p.group * Tr::QROW_BYTES, &item_full[slot]);
+        }
       }
       ++q_issued;
       claimed += static_cast<uint32_t>(n_units);
@@ -1090,6 +1119,9 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
     const float kv_k = KV8 ? p.k_scale[d.h] : 1.f, kv_v = KV8 ? p.v_scale[d.h] : 1.f;
     const float item_scale = p.scale_log2 * kv_k;
     cs.begin(qbuf + slot * Tr::Q_BYTES, item_scale, kv_v);
+    // row j may see positions up to L - q_len + j: relative to the item's first
+    // token, the last visible token of this lane's row
+    const int qlim0 = d.len - p.q_len - d.chunk * p.chunk_tokens + cs.row_token(p.group_log2);
     __syncwarp();
     if (lane == 0) mbar_arrive(&item_empty[slot]);
 
@@ -1120,7 +1152,7 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
             __syncwarp();
           }
         }
-        cs.unit(kt, vt, nt, item_scale, [&] {
+        cs.unit(kt, vt, nt, qlim0 - u * Tr::UT, item_scale, [&] {
           if constexpr (Tr::TC) {
             // order this warp's generic-proxy writes before the next tensor copy here
             if (nt < Tr::UT) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -1162,11 +1194,15 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
         float lam = 0.f;
 #pragma unroll
         for (int w = 0; w < CW; ++w) {
-          f[w] = fast_exp2(mml[(w * G + g) * 2] - M);
+          // a row with no visible token in this item (a new token before the
+          // item's first position) has M = -inf: it contributes nothing
+          f[w] = M == -INFINITY ? 0.f : fast_exp2(mml[(w * G + g) * 2] - M);
           lam = fmaf(f[w], mml[(w * G + g) * 2 + 1], lam);
         }
-        const float inv = 1.f / lam;
-        const int qh = d.h * G + g;
+        const float inv = lam > 0.f ? 1.f / lam : 0.f;
+        // row g = (new token j, head gi of the group): query row j * Hq + h * group + gi
+        const int qh = (g >> p.group_log2) * p.num_q_heads + d.h * p.group + (g & (p.group - 1));
+        const int64_t rows_per_seq = static_cast<int64_t>(p.q_len) * p.num_q_heads;
 #pragma unroll
         for (int cp = lane; cp < D / 2; cp += 32) {
           const int dcol = 2 * cp;
@@ -1180,7 +1216,7 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
           o0 *= inv;
           o1 *= inv;
           if (d.single) {
-            const int64_t o = (static_cast<int64_t>(d.b) * p.num_q_heads + qh) * D + dcol;
+            const int64_t o = (static_cast<int64_t>(d.b) * rows_per_seq + qh) * D + dcol;
             if constexpr (BF16) {
               const uint32_t packed = f32_to_bf16_bits(o0) | (f32_to_bf16_bits(o1) << 16);
               *reinterpret_cast<uint32_t*>(static_cast<char*>(p.out) + o * 2) = packed;
@@ -1188,9 +1224,9 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
               *reinterpret_cast<float2*>(static_cast<float*>(p.out) + o) = make_float2(o0, o1);
             }
           } else {
-            const int64_t row = static_cast<int64_t>(d.gchunk) * p.num_q_heads + qh;
+            const int64_t row = static_cast<int64_t>(d.gchunk) * rows_per_seq + qh;
             *reinterpret_cast<float2*>(p.part_out + row * D + dcol) = make_float2(o0, o1);
-            if (dcol == 0) p.part_lse[row] = M + __log2f(lam);
+            if (dcol == 0) p.part_lse[row] = lam > 0.f ? M + __log2f(lam) : -INFINITY;
           }
         }
       }
