@@ -52,14 +52,15 @@ def algorithmic_bytes(case) -> dict:
     L = case.context_lens.astype(np.int64)
     B, Hq, Hkv, D, bs = (case.num_seqs, case.num_q_heads, case.num_kv_heads, case.head_dim,
                          case.block_size)
+    T = B * case.q_len                                   # new tokens (query rows per head)
     kv = int(L.sum()) * 2 * Hkv * D * kv_elt
-    q = B * Hq * D * act_elt
-    out = B * Hq * D * act_elt
+    q = T * Hq * D * act_elt
+    out = T * Hq * D * act_elt
     tables = 4 * (int(((L + bs - 1) // bs).sum()) + B)
     scales = 2 * 4 * Hkv if case.dtype == "fp8" else 0
     decode = kv + q + out + tables + scales
     # read the new k/v, write them into the pool, the slots (and the scales)
-    write = 2 * B * Hkv * D * (act_elt + kv_elt) + 8 * B + scales
+    write = 2 * T * Hkv * D * (act_elt + kv_elt) + 8 * T + scales
     return dict(kv=kv, decode=decode, write=write, step=decode + write)
 
 
@@ -266,9 +267,9 @@ class GpuStep:
     def _finish_init(self):
         torch, pa = self.torch, self.pa
         c = self.case
-        self.ws_bytes = pa.pa_decode_workspace_size(c.num_seqs, c.num_q_heads, c.num_kv_heads,
-                                                    c.head_dim, c.block_size, self.max_len,
-                                                    self.chunk_tokens)
+        self.ws_bytes = pa.pa_decode_workspace_size(c.num_seqs, c.q_len * c.num_q_heads,
+                                                    c.num_kv_heads, c.head_dim, c.block_size,
+                                                    self.max_len, self.chunk_tokens)
         self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8,
                                      device=self.device)
         self.errs = torch.zeros(1, dtype=torch.int32, device=self.device)
@@ -291,6 +292,12 @@ class GpuStep:
                                 device_errors=self.errs)
 
     def decode(self):
+        if self.case.q_len > 1:
+            self.pa.pa_decode_multi(self.out, self.q, self.k_cache, self.v_cache, self.tables,
+                                    self.lens, self.scale, self.Hkv, self.max_len,
+                                    workspace=self.workspace, chunk_tokens=self.chunk_tokens,
+                                    device_errors=self.errs)
+            return
         if self.fp8:
             self.pa.pa_decode_fp8(self.out, self.q, self.k_cache, self.v_cache, self.tables,
                                   self.lens, self.scale, self.k_scale, self.v_scale, self.Hkv,
@@ -603,15 +610,20 @@ def run_e2e(ws, args, torch, pa, device, stream, barrier, world):
 
 # -------------------------------------------------------------- CPU oracle
 def _oracle_sample(case, n_rows, rng):
-    rows = [(int(rng.integers(case.num_seqs)), int(rng.integers(case.num_q_heads)))
-            for _ in range(n_rows)]
+    if case.q_len > 1:                                   # (sequence, new token, query head)
+        rows = [(int(rng.integers(case.num_seqs)), int(rng.integers(case.q_len)),
+                 int(rng.integers(case.num_q_heads))) for _ in range(n_rows)]
+    else:
+        rows = [(int(rng.integers(case.num_seqs)), int(rng.integers(case.num_q_heads)))
+                for _ in range(n_rows)]
     elt, act_elt = element_sizes(case)
     D = case.head_dim
     # bytes the sampled rows stand for: each row reads its sequence's K and V for
     # one head (shared by the GQA group, counted once per group member here is
     # avoided by dividing by the group size), plus its q and out row
     G = case.num_q_heads // case.num_kv_heads
-    nbytes = sum(int(case.context_lens[b]) * 2 * D * elt / G + 2 * D * act_elt for b, _ in rows)
+    nbytes = sum(int(case.context_lens[r[0]]) * 2 * D * elt / G / case.q_len + 2 * D * act_elt
+                 for r in rows)
     return rows, nbytes
 
 
@@ -626,6 +638,9 @@ def _oracle_write(case, kc, vc):
 
 def _oracle_decode(case, kc, vc, rows=None):
     import oracle
+    if case.q_len > 1:
+        return oracle.decode_multi_f64(case.q, kc, vc, case.block_tables, case.context_lens,
+                                       case.scale, case.num_kv_heads, case.dtype, rows=rows)
     if case.dtype == "fp8":
         return oracle.decode_kv8_f64(case.q, kc, vc, case.block_tables, case.context_lens,
                                      case.scale, case.extra["k_scale"], case.extra["v_scale"],
@@ -643,7 +658,7 @@ def cpu_baseline(case, budget_s=15.0, kind="oracle"):
     kc, vc = case.k_cache.copy(), case.v_cache.copy()
     threads = oracle.max_threads()
     rng = np.random.default_rng(9)
-    all_rows = case.num_seqs * case.num_q_heads
+    all_rows = case.num_seqs * case.q_len * case.num_q_heads
     # calibrate on a few rows
     rows, _ = _oracle_sample(case, 8, rng)
     t0 = time.perf_counter()

@@ -42,6 +42,10 @@ WORKLOADS = {
 for _name in ("mha_bf16", "gqa_bf16", "long128k_bf16"):
     WORKLOADS[_name.replace("bf16", "fp8")] = dict(WORKLOADS[_name], dtype="fp8")
 
+# Speculative-verify steps: q_len new (draft) tokens per sequence, causal.
+WORKLOADS["spec4_mha_bf16"] = dict(WORKLOADS["mha_bf16"], q_len=4)
+WORKLOADS["spec2_gqa_bf16"] = dict(WORKLOADS["gqa_bf16"], q_len=2)
+
 SHARED_PREFIX = dict(seed=1005, dtype="bf16", num_parents=8, children_per_parent=16,
                      prompt_len=2048, parent_extra=(1, 15), tail=(0, 512), num_q_heads=32,
                      num_kv_heads=8, head_dim=128, block_size=16, std=1.0)
@@ -101,9 +105,10 @@ def draw_lengths(rng: np.random.Generator, spec, num_seqs: int) -> np.ndarray:
 
 @dataclass
 class DecodeCase:
-    """One decode step's inputs.  ``context_lens`` counts the new token: position
-    L_b - 1 is written by the step's cache write, positions 0 .. L_b - 2 are
-    already in the pool."""
+    """One decode step's inputs.  ``context_lens`` counts the new tokens: the
+    last q_len positions L_b - q_len .. L_b - 1 are written by the step's cache
+    write, positions before them are already in the pool (q_len = 1: a plain
+    decode step)."""
     name: str
     dtype: str
     num_seqs: int
@@ -115,13 +120,14 @@ class DecodeCase:
     scale: float
     context_lens: np.ndarray      # int32 [B]
     block_tables: np.ndarray      # int32 [B, max_blocks], -1 past each sequence's pages
-    slot_mapping: np.ndarray      # int64 [B], slot of position L_b - 1 (-1 when L_b == 0)
+    slot_mapping: np.ndarray      # int64 [B * q_len], slots of the new positions (-1: none)
     k_cache: np.ndarray           # [NB, Hkv, bs, D] storage
     v_cache: np.ndarray
-    k_new: np.ndarray             # [B, Hkv, D] storage
+    k_new: np.ndarray             # [B * q_len, Hkv, D] storage
     v_new: np.ndarray
-    q: np.ndarray                 # [B, Hq, D] storage
+    q: np.ndarray                 # [B, Hq, D] storage; [B, q_len, Hq, D] when q_len > 1
     extra: dict = field(default_factory=dict)
+    q_len: int = 1
 
     @property
     def max_blocks_per_seq(self) -> int:
@@ -146,8 +152,10 @@ def _draw_normal(rng, shape, std):
 
 def make_decode_case(name="custom", *, seed, dtype, num_seqs, num_q_heads, num_kv_heads,
                      head_dim, block_size, lens, std=1.0, num_blocks=None, slack=0.10,
-                     scale=None, max_blocks_per_seq=None) -> DecodeCase:
-    """Build a seeded decode case; ``lens`` is a length spec (see ``draw_lengths``)."""
+                     scale=None, max_blocks_per_seq=None, q_len=1) -> DecodeCase:
+    """Build a seeded decode case; ``lens`` is a length spec (see ``draw_lengths``).
+    With q_len > 1 the step writes and attends with q_len new tokens per
+    sequence (lengths below q_len are raised to q_len)."""
     rng = np.random.Generator(np.random.PCG64(seed))
     B, Hq, Hkv, D, bs = num_seqs, num_q_heads, num_kv_heads, head_dim, block_size
     # fp8 cases: e4m3 pools with per-kv-head scales; q and the new token in bf16
@@ -155,6 +163,8 @@ def make_decode_case(name="custom", *, seed, dtype, num_seqs, num_q_heads, num_k
     ksc = fp8_scales(Hkv, std) if dtype == "fp8" else None
     vsc = ksc * np.float32(1.25) if dtype == "fp8" else None
     L = draw_lengths(rng, lens, B)
+    if q_len > 1:
+        L = np.maximum(L, q_len).astype(np.int32)
     pages = [(int(l) + bs - 1) // bs for l in L]
     need = int(sum(pages))
     NB = int(num_blocks) if num_blocks is not None else max(1, int(math.ceil((1.0 + slack) * need)))
@@ -172,27 +182,30 @@ def make_decode_case(name="custom", *, seed, dtype, num_seqs, num_q_heads, num_k
     k_cache = nan_fill((NB, Hkv, bs, D), kv_dtype)
     v_cache = nan_fill((NB, Hkv, bs, D), kv_dtype)
     for b in range(B):
-        n_old = max(int(L[b]) - 1, 0)
+        n_old = max(int(L[b]) - q_len, 0)
         if n_old == 0:
             continue
         kb = to_storage(_draw_normal(rng, (n_old, Hkv, D), std), kv_dtype, ksc)
         vb = to_storage(_draw_normal(rng, (n_old, Hkv, D), std), kv_dtype, vsc)
         _lay_out_prefix(k_cache, tables[b], kb, bs)
         _lay_out_prefix(v_cache, tables[b], vb, bs)
-    k_new = to_storage(_draw_normal(rng, (B, Hkv, D), std), act_dtype)
-    v_new = to_storage(_draw_normal(rng, (B, Hkv, D), std), act_dtype)
-    q = to_storage(_draw_normal(rng, (B, Hq, D), std), act_dtype)
-    slots = np.full(B, -1, dtype=np.int64)
+    k_new = to_storage(_draw_normal(rng, (B * q_len, Hkv, D), std), act_dtype)
+    v_new = to_storage(_draw_normal(rng, (B * q_len, Hkv, D), std), act_dtype)
+    q_shape = (B, Hq, D) if q_len == 1 else (B, q_len, Hq, D)
+    q = to_storage(_draw_normal(rng, q_shape, std), act_dtype)
+    slots = np.full(B * q_len, -1, dtype=np.int64)
     for b in range(B):
-        if L[b] > 0:
-            pos = int(L[b]) - 1
-            slots[b] = int(tables[b, pos // bs]) * bs + pos % bs
+        for j in range(q_len):
+            pos = int(L[b]) - q_len + j
+            if pos >= 0:
+                slots[b * q_len + j] = int(tables[b, pos // bs]) * bs + pos % bs
     return DecodeCase(name=name, dtype=dtype, num_seqs=B, num_q_heads=Hq, num_kv_heads=Hkv,
                       head_dim=D, block_size=bs, num_blocks=NB,
                       scale=float(scale) if scale is not None else 1.0 / math.sqrt(D),
                       context_lens=L, block_tables=tables, slot_mapping=slots,
                       k_cache=k_cache, v_cache=v_cache, k_new=k_new, v_new=v_new, q=q,
-                      extra={} if ksc is None else {"k_scale": ksc, "v_scale": vsc})
+                      extra={} if ksc is None else {"k_scale": ksc, "v_scale": vsc},
+                      q_len=q_len)
 
 
 def _lay_out_prefix(pool, table_row, rows, bs):
