@@ -38,7 +38,8 @@ import pa_inputs  # noqa: E402
 METRIC = "paged decode KV-read GB/s (% of GB300 HBM peak); decode steps/s, µs/step"
 FALLBACK_HBM_GBS = 6800.0
 DEFAULT_WORKLOAD = "mha_bf16"   # Llama-2-7B-shaped MHA decode, bf16, batch 64
-DECODE_SOURCES = ["paged_decode.cuh", "decode_launch.cu", "decode_instances.cuh", "pa_device.cuh"]
+DECODE_SOURCES = ["paged_decode.cuh", "decode_launch.cu", "decode_instances.cuh", "pa_device.cuh",
+                  "cascade.cu"]
 
 
 # ------------------------------------------------------------------ helpers
@@ -196,7 +197,8 @@ class GpuStep:
         self.torch, self.pa, self.device = torch, pa, device
         self.chunk_tokens = chunk_tokens
         self.name = name
-        if name == "shared_prefix_bf16":
+        self.cascade = name == "shared_prefix_cascade_bf16"
+        if name in ("shared_prefix_bf16", "shared_prefix_cascade_bf16"):
             self._init_shared_prefix()
         else:
             self._init_decode(pa_inputs.workload(name))
@@ -263,21 +265,45 @@ class GpuStep:
         elt = 2
         self.bytes["copy"] = 2 * 2 * len(pairs) * s.num_kv_heads * s.block_size * s.head_dim * elt
         self.bytes["step"] += self.bytes["copy"]
+        if self.cascade:
+            # groups from the host tables (the library's grouping); the decode then
+            # needs each family's shared pages once, each child's own tokens once
+            starts, shared = pa.pa_cascade_groups(tables, lens, s.block_size)
+            self.group_start, self.shared_lens = self._t(starts), self._t(shared)
+            self.host_inputs["group_start"], self.host_inputs["shared_lens"] = starts, shared
+            sizes = np.diff(starts)
+            own = int(lens.astype(np.int64).sum() - (np.repeat(shared, sizes)).sum())
+            unique = (int(shared.astype(np.int64).sum()) + own) * 2 * s.num_kv_heads * s.head_dim * elt
+            self.bytes["kv_logical"] = self.bytes["kv"]
+            self.bytes["decode"] += unique - self.bytes["kv"]
+            self.bytes["step"] += unique - self.bytes["kv"]
+            self.bytes["kv"] = unique
+            self.groups = len(shared)
+            self._finish_init()
 
     def _finish_init(self):
         torch, pa = self.torch, self.pa
         c = self.case
-        self.ws_bytes = pa.pa_decode_workspace_size(c.num_seqs, c.q_len * c.num_q_heads,
-                                                    c.num_kv_heads, c.head_dim, c.block_size,
-                                                    self.max_len, self.chunk_tokens)
+        if getattr(self, "cascade", False) and hasattr(self, "groups"):
+            self.ws_bytes = pa.pa_decode_cascade_workspace_size(
+                c.num_seqs, self.groups, c.num_q_heads, c.num_kv_heads, c.head_dim,
+                c.block_size, self.max_len, self.chunk_tokens)
+        else:
+            self.ws_bytes = pa.pa_decode_workspace_size(c.num_seqs, c.q_len * c.num_q_heads,
+                                                        c.num_kv_heads, c.head_dim,
+                                                        c.block_size, self.max_len,
+                                                        self.chunk_tokens)
         self.workspace = torch.empty(max(self.ws_bytes, 256), dtype=torch.uint8,
                                      device=self.device)
         self.errs = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.chunk = self.chunk_tokens or pa.pa_decode_chunk_tokens(
             c.num_seqs, c.num_kv_heads, c.block_size, self.max_len)
-        # kernels of ours per step: [copy_blocks] + reshape + plan + decode [+ merge]
+        # kernels of ours per step: [copy_blocks] + reshape + plan + decode [+ merge];
+        # the cascade adds the prefix kernel and always merges
         self.launches_per_step = (1 if self.pairs is not None else 0) + 3 + (
             1 if self.max_len > self.chunk else 0)
+        if getattr(self, "cascade", False):
+            self.launches_per_step = (1 if self.pairs is not None else 0) + 5
 
     def write(self):
         pa = self.pa
@@ -292,6 +318,12 @@ class GpuStep:
                                 device_errors=self.errs)
 
     def decode(self):
+        if self.cascade:
+            self.pa.pa_decode_cascade(self.out, self.q, self.k_cache, self.v_cache, self.tables,
+                                      self.lens, self.group_start, self.shared_lens, self.scale,
+                                      self.Hkv, self.max_len, workspace=self.workspace,
+                                      chunk_tokens=self.chunk_tokens, device_errors=self.errs)
+            return
         if self.case.q_len > 1:
             self.pa.pa_decode_multi(self.out, self.q, self.k_cache, self.v_cache, self.tables,
                                     self.lens, self.scale, self.Hkv, self.max_len,
@@ -411,6 +443,20 @@ def run_gpu(args, world, rank, local):
         "gpu_launches": ws.launches_per_step * K,
         "clocks": clocks.summary(),
     }
+    if ws.cascade:
+        # algorithmic bytes above count each family's shared pages once; the same
+        # call measured against every child's whole context, for comparison with
+        # pa_decode on the same batch
+        result["config"]["step"] = ("copy_blocks + reshape_and_cache + cascade decode (plan, "
+                                    "shared-prefix kernel, persistent decode over each "
+                                    "sequence's own pages, merge)")
+        result["config"]["groups"] = ws.groups
+        result["cascade"] = {
+            "unique_kv_bytes": b["kv"], "logical_kv_bytes": b["kv_logical"],
+            "logical_decode_gbs": round((b["decode"] - b["kv"] + b["kv_logical"])
+                                        / (dec_avg_ms * 1e-3) / 1e9, 1)}
+        result["roofline"]["kernel"] = ("pa_decode_cascade call (plan + prefix kernel + "
+                                        "paged_decode_kernel + merge), CUDA events")
     if not args.no_cpu_baseline and world == 1:
         result["cpu_baseline"] = cpu_baseline(ws.case, budget_s=args.cpu_budget)
     return result
@@ -581,6 +627,8 @@ def run_e2e(ws, args, torch, pa, device, stream, barrier, world):
                lens=ws.lens)
     if "pairs" in host:
         dev["pairs"] = ws.pairs
+    if "group_start" in host:
+        dev["group_start"], dev["shared_lens"] = ws.group_start, ws.shared_lens
     out_host = torch.empty(ws.out.shape, dtype=ws.out.dtype).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_host.numel() * out_host.element_size()
@@ -728,7 +776,7 @@ def run_reference(args, world, rank):
     oracle.build()
     if args.workload == "swap_gqa":
         return run_reference_swap(args, world)
-    if args.workload == "shared_prefix_bf16":
+    if args.workload in ("shared_prefix_bf16", "shared_prefix_cascade_bf16"):
         case = pa_inputs.workload("gqa_bf16")
     else:
         case = pa_inputs.workload(args.workload)
@@ -774,7 +822,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
-                    choices=list(pa_inputs.WORKLOADS) + ["shared_prefix_bf16", "swap_gqa"])
+                    choices=list(pa_inputs.WORKLOADS) + ["shared_prefix_bf16",
+                                                         "shared_prefix_cascade_bf16", "swap_gqa"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--chunk-tokens", type=int, default=0,

@@ -210,6 +210,56 @@ int pa_decode_multi(void* out, const void* q, const void* k_cache, const void* v
                     int32_t* device_errors, void* stream);
 
 /*
+ * Shared-prefix ("cascade") decode.  "mlx-paged-attention" (feature 2, memory
+ * sharing) and "PagedAttention原理" §3.3.3 let several sequences hold the same
+ * physical pages for a common prefix; this call reads those pages once per
+ * group instead of once per sequence.  The result is pa_decode's (softmax
+ * attention of each sequence's q over its whole context, same tolerance).
+ *
+ * Groups: sequences group_start[f] .. group_start[f + 1] - 1 form group f
+ * (group_start: device int32 [num_groups + 1], group_start[0] = 0, increasing,
+ * group_start[num_groups] = num_seqs).  shared_lens: device int32 [num_groups],
+ * the number of leading tokens every member of group f shares: a whole number
+ * of pages, 0 <= shared_lens[f] < context_lens[b] for every member b (0: no
+ * sharing), and every member's block table holds the group leader's
+ * (group_start[f]'s) pages for them.  Device-side checks: a shared length that
+ * is not a whole number of pages or not below a member's length sets
+ * PA_DEVERR_BAD_LENGTH (that member, or the group, is then decoded without the
+ * sharing); a member whose table differs from the leader's over the prefix sets
+ * PA_DEVERR_BAD_BLOCK (its rows use the leader's pages).
+ *
+ * bf16 only; q_len 1; num_q_heads / num_kv_heads in {1, 2, 4, 8}; other
+ * arguments as pa_decode.  Workspace: pa_decode_cascade_workspace_size (0 for
+ * unsupported sizes).  Host errors: PA_ERR_INVALID_ARG when num_groups is not
+ * in 1 .. num_seqs or a group array is null.
+ */
+int pa_decode_cascade(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* context_lens,
+                      const int32_t* group_start, const int32_t* shared_lens, int num_groups,
+                      float scale, int num_kv_heads, int num_seqs, int num_q_heads, int head_dim,
+                      int block_size, int num_blocks, int max_blocks_per_seq,
+                      int max_context_len, int chunk_tokens, void* workspace,
+                      size_t workspace_bytes, int32_t* device_errors, void* stream);
+size_t pa_decode_cascade_workspace_size(int num_seqs, int num_groups, int num_q_heads,
+                                         int num_kv_heads, int head_dim, int block_size,
+                                         int max_context_len, int chunk_tokens);
+
+/*
+ * Groups for pa_decode_cascade, from HOST copies of the block tables
+ * [num_seqs][max_blocks_per_seq] and context lengths [num_seqs].  A run of
+ * consecutive sequences with the same first page forms a group; its shared
+ * length is the number of leading pages all members hold in common, times
+ * block_size, cut to whole pages below the shortest member's length.
+ * Sequences that share no page with a neighbour are gathered into groups with
+ * shared length 0.  Outputs (host, caller-owned): group_start [num_seqs + 1],
+ * shared_lens [num_seqs], *num_groups.  PA_ERR_INVALID_ARG on null pointers,
+ * non-positive sizes or a negative length.
+ */
+int pa_cascade_groups(const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                      int max_blocks_per_seq, int block_size, int32_t* group_start,
+                      int32_t* shared_lens, int* num_groups);
+
+/*
  * float8 e4m3 KV pools.  "mlx-paged-attention" (future plans) names
  * quantization as the next optimisation; the pages give no format, so this is
  * the plainest one: the pools hold one-byte e4m3 codes (1 sign, 4 exponent bits

@@ -221,6 +221,27 @@ def _lay_out_prefix(pool, table_row, rows, bs):
         pool[table_row[full], :, :rem, :] = rows[full * bs:].transpose(1, 0, 2)
 
 
+def share_leading_pages(case: DecodeCase, group_sizes, shared_pages) -> DecodeCase:
+    """The case with its sequences cut into consecutive groups (sizes
+    ``group_sizes``) whose members read their group leader's first
+    ``shared_pages[f]`` pages instead of their own (as forked sequences do; a
+    member's own first pages are left unused).  Only the tables change; the
+    new-token slots lie past the shared pages.  Returns the new case and the
+    int32 (group_start, shared_lens) arrays."""
+    tables = case.block_tables.copy()
+    starts, shared = [0], []
+    for size, npg in zip(group_sizes, shared_pages):
+        g0 = starts[-1]
+        for b in range(g0 + 1, g0 + size):
+            tables[b, :npg] = tables[g0, :npg]
+        starts.append(g0 + size)
+        shared.append(npg * case.block_size)
+    if starts[-1] != case.num_seqs:
+        raise ValueError("group sizes must add up to the batch")
+    out = DecodeCase(**{**case.__dict__, "block_tables": tables})
+    return out, np.asarray(starts, np.int32), np.asarray(shared, np.int32)
+
+
 def place_at_slots(pool, slots, rows, block_size):
     """Put rows[t] (shape [T, Hkv, D]) at global slot slots[t] (prefill of a pool
     whose slots were handed out by a block manager)."""

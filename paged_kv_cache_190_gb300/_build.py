@@ -19,9 +19,8 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedattn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CU_SOURCES = ["capi.cu", "cache_ops.cu", "decode_launch.cu", "decode_bf16.cu", "decode_f32.cu",
-              "decode_fp8.cu",
-              "decode_noalloc.cu"]
-CPP_SOURCES = ["block_manager.cpp"]
+              "decode_fp8.cu", "decode_noalloc.cu", "cascade.cu"]
+CPP_SOURCES = ["block_manager.cpp", "cascade_groups.cpp"]
 
 
 def _nvcc() -> str:

@@ -21,7 +21,8 @@ EXPORTED_SYMBOLS = [
     "pa_get_error_string", "pa_reshape_and_cache", "pa_copy_blocks", "pa_decode_chunk_tokens",
     "pa_decode_workspace_size", "pa_decode", "pa_decode_noalloc", "pa_debug_set_wait_limit",
     "pa_read_device_errors", "pa_reshape_and_cache_fp8", "pa_decode_fp8", "pa_swap_blocks",
-    "pa_decode_multi",
+    "pa_decode_multi", "pa_decode_cascade", "pa_decode_cascade_workspace_size",
+    "pa_cascade_groups",
     "pa_bm_create", "pa_bm_destroy", "pa_bm_add_seq", "pa_bm_append_slot", "pa_bm_fork",
     "pa_bm_free", "pa_bm_block_table", "pa_bm_refcount", "pa_bm_num_free", "pa_bm_free_list",
     "pa_bm_stats", "pa_bm_append_slots", "pa_bm_build_block_tables", "pa_bm_enable_swap",
@@ -54,6 +55,12 @@ _SIGNATURES = {
     "pa_decode_multi": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_float, _i32, _i32, _i32,
                                _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz, _vp,
                                _vp]),
+    "pa_decode_cascade": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, ctypes.c_float,
+                                 _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _vp, _sz,
+                                 _vp, _vp]),
+    "pa_decode_cascade_workspace_size": (_sz, [_i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32]),
+    "pa_cascade_groups": (_i32, [_pi32, _pi32, _i32, _i32, _i32, _pi32, _pi32,
+                                 ctypes.POINTER(_i32)]),
     "pa_debug_set_wait_limit": (_i32, [_i32]),
     "pa_read_device_errors": (_i32, [_vp, _pi32, _i32, _vp]),
     "pa_bm_create": (_i32, [_i32, _i32, _pi32, ctypes.POINTER(_vp)]),
@@ -277,6 +284,72 @@ def pa_decode_multi(out, q, k_cache, v_cache, block_tables, context_lens, scale,
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(device_errors),
         _stream(stream, q.device))
     _check(rc, "pa_decode_multi")
+    return out
+
+
+def pa_decode_cascade_workspace_size(num_seqs, num_groups, num_q_heads, num_kv_heads, head_dim,
+                                     block_size, max_context_len, chunk_tokens=0):
+    n = library().pa_decode_cascade_workspace_size(
+        int(num_seqs), int(num_groups), int(num_q_heads), int(num_kv_heads), int(head_dim),
+        int(block_size), int(max_context_len), int(chunk_tokens))
+    if n == 0 and num_seqs > 0:
+        raise PaError(PA_ERR_UNSUPPORTED, "pa_decode_cascade_workspace_size: unsupported sizes")
+    return n
+
+
+def pa_cascade_groups(block_tables, context_lens, block_size):
+    """Groups of sequences sharing leading pages (see pa.h), from host int32
+    arrays block_tables [B, max_blocks] and context_lens [B].  Returns numpy
+    int32 (group_start [G + 1], shared_lens [G])."""
+    import numpy as np
+    tables = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B = int(lens.shape[0])
+    if tables.ndim != 2 or tables.shape[0] != B:
+        raise ValueError("block_tables must be [num_seqs, max_blocks]")
+    starts = np.zeros(B + 1, np.int32)
+    shared = np.zeros(max(B, 1), np.int32)
+    n = _i32(0)
+    rc = library().pa_cascade_groups(
+        tables.ctypes.data_as(_pi32), lens.ctypes.data_as(_pi32), B, int(tables.shape[1]),
+        int(block_size), starts.ctypes.data_as(_pi32), shared.ctypes.data_as(_pi32),
+        ctypes.byref(n))
+    _check(rc, "pa_cascade_groups")
+    return starts[:n.value + 1].copy(), shared[:n.value].copy()
+
+
+def pa_decode_cascade(out, q, k_cache, v_cache, block_tables, context_lens, group_start,
+                      shared_lens, scale, num_kv_heads, max_context_len, workspace=None,
+                      chunk_tokens=0, device_errors=None, stream=None):
+    """Shared-prefix decode (see pa.h): pa_decode's arguments plus group_start
+    int32 [groups + 1] and shared_lens int32 [groups] (device tensors); bf16."""
+    import torch
+    for n, t in (("out", out), ("q", q), ("k_cache", k_cache), ("v_cache", v_cache),
+                 ("block_tables", block_tables), ("context_lens", context_lens),
+                 ("group_start", group_start), ("shared_lens", shared_lens)):
+        _need_cuda_contig(n, t)
+    for n, t in (("block_tables", block_tables), ("context_lens", context_lens),
+                 ("group_start", group_start), ("shared_lens", shared_lens)):
+        if t.dtype != torch.int32:
+            raise TypeError(f"{n} must be int32")
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    G = shared_lens.numel()
+    if group_start.numel() != G + 1:
+        raise ValueError("group_start must have one more entry than shared_lens")
+    if int(Hkv) != int(num_kv_heads):
+        raise ValueError("num_kv_heads does not match the cache shape")
+    if workspace is None:
+        nbytes = pa_decode_cascade_workspace_size(B, G, Hq, Hkv, D, bs, max_context_len,
+                                                  chunk_tokens)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    rc = library().pa_decode_cascade(
+        _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        _ptr(group_start), _ptr(shared_lens), int(G), float(scale), int(num_kv_heads), int(B),
+        int(Hq), int(D), int(bs), int(NB), int(block_tables.shape[1]), int(max_context_len),
+        int(chunk_tokens), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _ptr(device_errors), _stream(stream, q.device))
+    _check(rc, "pa_decode_cascade")
     return out
 
 

@@ -140,6 +140,25 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
   return pa::decode_workspace_layout(num_seqs, num_q_heads, head_dim, max_context_len, chunk).total;
 }
 
+size_t pa_decode_cascade_workspace_size(int num_seqs, int num_groups, int num_q_heads,
+                                         int num_kv_heads, int head_dim, int block_size,
+                                         int max_context_len, int chunk_tokens) {
+  if (num_seqs < 0 || num_groups < 1 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      max_context_len < 0)
+    return 0;
+  if (!supported_shape(head_dim, block_size)) return 0;
+  int chunk = chunk_tokens;
+  if (chunk == 0) {
+    const int sms = current_sm_count();
+    if (sms <= 0) return 0;
+    chunk = choose_chunk(num_seqs, num_kv_heads, block_size, max_context_len, sms);
+  } else if (!valid_chunk(chunk, block_size)) {
+    return 0;
+  }
+  return pa::decode_workspace_layout(num_seqs, num_q_heads, head_dim, max_context_len, chunk,
+                                     num_groups).total;
+}
+
 }  // extern "C"
 
 namespace {
@@ -151,7 +170,8 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
                   int num_blocks, int max_blocks_per_seq, int max_context_len, pa_dtype dtype,
                   bool kv8, const float* k_scale, const float* v_scale, int q_len,
                   int chunk_tokens, void* workspace, size_t workspace_bytes,
-                  int32_t* device_errors, void* stream) {
+                  int32_t* device_errors, void* stream, const int32_t* group_start = nullptr,
+                  const int32_t* shared_lens = nullptr, int num_groups = 0) {
   if (num_kv_heads <= 0 || num_q_heads <= 0 || num_seqs < 0 || num_blocks <= 0 ||
       max_blocks_per_seq <= 0 || max_context_len < 0)
     return PA_ERR_INVALID_ARG;
@@ -176,8 +196,9 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
     chunk = choose_chunk(num_seqs, num_kv_heads, block_size, max_context_len, sms);
   else if (!valid_chunk(chunk, block_size))
     return PA_ERR_INVALID_ARG;
-  const pa::WorkspaceLayout lay =
-      pa::decode_workspace_layout(num_seqs, q_len * num_q_heads, head_dim, max_context_len, chunk);
+  const pa::WorkspaceLayout lay = pa::decode_workspace_layout(
+      num_seqs, q_len * num_q_heads, head_dim, max_context_len, chunk, num_groups);
+  if (lay.max_chunks >= (int64_t{1} << 30)) return PA_ERR_INVALID_ARG;   // chunk ids keep 30 bits
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
       workspace_bytes < lay.total)
     return PA_ERR_WORKSPACE;
@@ -211,6 +232,11 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   a.ws.part_lse = reinterpret_cast<float*>(ws + lay.part_lse);
   a.ws.part_out = reinterpret_cast<float*>(ws + lay.part_out);
   a.ws.q8 = reinterpret_cast<unsigned char*>(ws + lay.q8);
+  a.ws.prefix_parts = reinterpret_cast<int32_t*>(ws + lay.prefix_parts);
+  a.ws.prefix_items = reinterpret_cast<int2*>(ws + lay.prefix_items);
+  a.group_start = group_start;
+  a.shared_lens = shared_lens;
+  a.num_groups = num_groups;
   a.ws.max_chunks = lay.max_chunks;
   a.device_errors = device_errors;
   a.num_sms = sms;
@@ -260,6 +286,24 @@ int pa_decode_multi(void* out, const void* q, const void* k_cache, const void* v
                        num_seqs, num_q_heads, head_dim, block_size, num_blocks,
                        max_blocks_per_seq, max_context_len, dtype, false, nullptr, nullptr, q_len,
                        chunk_tokens, workspace, workspace_bytes, device_errors, stream);
+}
+
+int pa_decode_cascade(void* out, const void* q, const void* k_cache, const void* v_cache,
+                      const int32_t* block_tables, const int32_t* context_lens,
+                      const int32_t* group_start, const int32_t* shared_lens, int num_groups,
+                      float scale, int num_kv_heads, int num_seqs, int num_q_heads, int head_dim,
+                      int block_size, int num_blocks, int max_blocks_per_seq,
+                      int max_context_len, int chunk_tokens, void* workspace,
+                      size_t workspace_bytes, int32_t* device_errors, void* stream) {
+  if (!supported_shape(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
+  if (num_seqs > 0 && (num_groups < 1 || num_groups > num_seqs || !group_start || !shared_lens))
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0) return PA_OK;
+  return decode_common(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
+                       num_seqs, num_q_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_context_len, PA_BF16, false, nullptr, nullptr, 1,
+                       chunk_tokens, workspace, workspace_bytes, device_errors, stream,
+                       group_start, shared_lens, num_groups);
 }
 
 int pa_reshape_and_cache_fp8(const void* k, const void* v, void* k_cache, void* v_cache,

@@ -126,7 +126,9 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(
         const int mid = (lo + hi + 1) >> 1;
         if (first_s[mid] <= e) lo = mid; else hi = mid - 1;
       }
-      work[carry + e] = make_int4(base + lo, e - first_s[lo], len_s[lo], carry + e);
+      const int single = len_s[lo] <= chunk_tokens ? kSingleChunk : 0;
+      work[carry + e] =
+          make_int4(base + lo, (e - first_s[lo]) * chunk_tokens, len_s[lo], (carry + e) | single);
     }
     __syncthreads();
     if (threadIdx.x == 0) carry_s = carry + tile_total;
@@ -140,6 +142,13 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(
 }
 
 constexpr int kMergeWarps = 8;
+
+// Partials a sequence can have: its chunks, plus (cascade) its prefix chunks.
+int64_t cascade_parts_per_seq(int max_context_len, int chunk_tokens, bool cascade) {
+  if (max_context_len <= 0) return 0;
+  const int64_t L = max_context_len;
+  return (L + chunk_tokens - 1) / chunk_tokens + (cascade ? (L + kPrefixChunk - 1) / kPrefixChunk : 0);
+}
 constexpr int kWideMergeWarps = 16;
 
 // Running log-sum-exp state of one output row over some chunks (base 2):
@@ -189,7 +198,9 @@ __device__ __forceinline__ void store_row(void* out, int64_t o, const float* r) 
   }
 }
 
-// Split-K merge (log-sum-exp): for sequence b, query head i with n >= 2 chunks,
+// Split-K merge (log-sum-exp): for sequence b, query head i with n >= min_chunks
+// chunks (2 for pa_decode, whose single chunks write the output directly; 1 for
+// the cascade, where every chunk is a partial),
 //   out = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M),  M = max_c lse_c,
 // where o_c is chunk c's normalised output and lse_c its base-2 log-sum-exp.
 // One warp per (b, i) row, each lane owning head_dim / 32 columns; one pass with
@@ -197,7 +208,8 @@ __device__ __forceinline__ void store_row(void* out, int64_t o, const float* r) 
 template <bool BF16, int CPL>
 __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(
     const int32_t* __restrict__ chunk_base, const float* __restrict__ part_lse,
-    const float* __restrict__ part_out, void* __restrict__ out, int num_q_heads, int64_t rows) {
+    const float* __restrict__ part_out, void* __restrict__ out, int num_q_heads, int64_t rows,
+    int min_chunks) {
   constexpr int D = CPL * 32;
   wait_prior_grids();                     // the decode kernel's partials
   const int lane = threadIdx.x & 31;
@@ -207,7 +219,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(
   const int i = static_cast<int>(row - static_cast<int64_t>(b) * num_q_heads);
   const int c0 = chunk_base[b];
   const int n = chunk_base[b + 1] - c0;
-  if (n < 2) return;
+  if (n < min_chunks) return;             // one chunk: the decode kernel wrote the row
   const int64_t prow0 = static_cast<int64_t>(c0) * num_q_heads + i;
   LseAcc<CPL> st;
 #pragma unroll 8
@@ -230,7 +242,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(
 template <bool BF16, int CPL>
 __global__ void __launch_bounds__(kWideMergeWarps * 32) decode_merge_wide_kernel(
     const int32_t* __restrict__ chunk_base, const float* __restrict__ part_lse,
-    const float* __restrict__ part_out, void* __restrict__ out, int num_q_heads) {
+    const float* __restrict__ part_out, void* __restrict__ out, int num_q_heads, int min_chunks) {
   constexpr int D = CPL * 32;
   __shared__ float sM[kWideMergeWarps], sS[kWideMergeWarps];
   __shared__ float sacc[kWideMergeWarps][D];
@@ -242,7 +254,7 @@ __global__ void __launch_bounds__(kWideMergeWarps * 32) decode_merge_wide_kernel
   const int i = static_cast<int>(row - static_cast<int64_t>(b) * num_q_heads);
   const int c0 = chunk_base[b];
   const int n = chunk_base[b + 1] - c0;
-  if (n < 2) return;                      // uniform over the block
+  if (n < min_chunks) return;             // uniform over the block
   const int64_t prow0 = static_cast<int64_t>(c0) * num_q_heads + i;
   LseAcc<CPL> st;
 #pragma unroll 8
@@ -299,19 +311,22 @@ template <bool BF16, int CPL>
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream) {
   const int rows_q = a.q_len * a.num_q_heads;         // query rows per sequence
   const int64_t rows = static_cast<int64_t>(a.num_seqs) * rows_q;
-  const int64_t max_chunks_per_seq = (static_cast<int64_t>(a.max_context_len) + a.chunk_tokens - 1) /
-                                     a.chunk_tokens;
+  const bool cascade = a.num_groups > 0;
+  const int64_t max_chunks_per_seq = cascade_parts_per_seq(a.max_context_len, a.chunk_tokens,
+                                                           cascade);
+  const int min_chunks = cascade ? 1 : 2;
   if (max_chunks_per_seq >= 32)
     return launch_dependent(decode_merge_wide_kernel<BF16, CPL>, static_cast<unsigned>(rows),
                             kWideMergeWarps * 32, stream,
                             static_cast<const int32_t*>(a.ws.chunk_base),
                             static_cast<const float*>(a.ws.part_lse),
-                            static_cast<const float*>(a.ws.part_out), a.out, rows_q);
+                            static_cast<const float*>(a.ws.part_out), a.out, rows_q, min_chunks);
   const unsigned blocks = static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps);
   return launch_dependent(decode_merge_kernel<BF16, CPL>, blocks, kMergeWarps * 32, stream,
                           static_cast<const int32_t*>(a.ws.chunk_base),
                           static_cast<const float*>(a.ws.part_lse),
-                          static_cast<const float*>(a.ws.part_out), a.out, rows_q, rows);
+                          static_cast<const float*>(a.ws.part_out), a.out, rows_q, rows,
+                          min_chunks);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -359,11 +374,9 @@ cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int head_dim, int6
 }  // namespace
 
 WorkspaceLayout decode_workspace_layout(int num_seqs, int num_q_heads, int head_dim,
-                                        int max_context_len, int chunk_tokens) {
+                                        int max_context_len, int chunk_tokens, int num_groups) {
   WorkspaceLayout w{};
-  const int64_t per_seq =
-      max_context_len > 0 ? (static_cast<int64_t>(max_context_len) + chunk_tokens - 1) / chunk_tokens
-                          : 0;
+  const int64_t per_seq = cascade_parts_per_seq(max_context_len, chunk_tokens, num_groups > 0);
   w.max_chunks = static_cast<int64_t>(num_seqs) * per_seq;
   size_t off = 256;  // header
   w.chunk_base = off;
@@ -376,6 +389,14 @@ WorkspaceLayout decode_workspace_layout(int num_seqs, int num_q_heads, int head_
   off += align256(static_cast<size_t>(w.max_chunks) * num_q_heads * head_dim * 4);
   w.q8 = off;                             // the fp8-cache path's prepared q rows
   off += align256(static_cast<size_t>(num_seqs) * num_q_heads * (2 * head_dim + 16));
+  w.prefix_parts = off;                   // the cascade's per-sequence prefix partials
+  w.prefix_items = off;
+  if (num_groups > 0) {
+    off += align256(static_cast<size_t>(num_seqs) * 4);
+    w.prefix_items = off;                 // (group, prefix chunk) items
+    const int64_t per_group = (static_cast<int64_t>(max_context_len) + kPrefixChunk - 1) / kPrefixChunk;
+    off += align256(static_cast<size_t>(num_groups) * per_group * 8);
+  }
   w.total = off;
   return w;
 }
@@ -392,11 +413,17 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     const cudaError_t qe = cudaGetLastError();
     if (qe != cudaSuccess) return qe;
   }
+  const bool cascade = a.num_groups > 0;
   const int64_t row_chunks = static_cast<int64_t>(rows_q) * a.head_dim * elt / 16;
-  decode_plan_kernel<<<1, kPlanThreads, 0, stream>>>(
-      a.context_lens, a.num_seqs, a.chunk_tokens, a.max_context_len, a.q_len, a.ws.header,
-      a.ws.chunk_base, a.ws.work, static_cast<uint4*>(a.out), row_chunks, a.device_errors);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  if (cascade) {
+    e = launch_cascade_plan(a, stream);
+  } else {
+    decode_plan_kernel<<<1, kPlanThreads, 0, stream>>>(
+        a.context_lens, a.num_seqs, a.chunk_tokens, a.max_context_len, a.q_len, a.ws.header,
+        a.ws.chunk_base, a.ws.work, static_cast<uint4*>(a.out), row_chunks, a.device_errors);
+    e = cudaGetLastError();
+  }
   if (e != cudaSuccess) return e;
   if (a.ws.max_chunks == 0) return cudaSuccess;  // every length is zero
 
@@ -405,7 +432,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   const int group = a.num_q_heads / a.num_kv_heads;
   const int rows = a.q_len * group;                   // rows per (sequence, kv head) item
   // the kernel instance is chosen by the rows of an item, and so is its consumer
-  if (a.kv8 || decode_uses_tensor_cores(a.bf16 != 0, rows)) {
+  // (the cascade's prefix kernel reads through the maps too)
+  if (a.kv8 || cascade || decode_uses_tensor_cores(a.bf16 != 0, rows)) {
     const int64_t rows = static_cast<int64_t>(a.num_blocks) * a.num_kv_heads * a.block_size;
     const int kv_elt = a.kv8 ? 1 : 2;
     // one box per page a unit touches: min(page, unit) rows
@@ -445,11 +473,17 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   int device = 0;
   e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
+  if (cascade) {
+    // the shared prefixes first (an ordinary launch after the plan), then the
+    // decode kernel over each sequence's own tokens
+    e = launch_cascade_prefix(a, kp, device, stream);
+    if (e != cudaSuccess) return e;
+  }
   e = a.kv8    ? run_decode_fp8(a.head_dim, rows, kp, grid, device, stream)
       : a.bf16 ? run_decode_bf16(a.head_dim, rows, kp, grid, device, stream)
                : run_decode_f32(a.head_dim, rows, kp, grid, device, stream);
   if (e != cudaSuccess) return e;
-  if (a.max_context_len > a.chunk_tokens) {
+  if (cascade || a.max_context_len > a.chunk_tokens) {
     if (a.bf16 && a.head_dim == 128) e = launch_merge<true, 4>(a, stream);
     else if (a.bf16) e = launch_merge<true, 2>(a, stream);
     else if (a.head_dim == 128) e = launch_merge<false, 4>(a, stream);

@@ -9,24 +9,32 @@
 
 namespace pa {
 
+// Tokens of a group's shared prefix per item of the cascade prefix kernel.
+constexpr int kPrefixChunk = 128;
+
 // Workspace of one pa_decode call, carved from the caller's buffer.
 struct DecodeWorkspace {
   int32_t* header;       // [0] work counter, [1] total chunks, rest reserved
   int32_t* chunk_base;   // [num_seqs + 1] first global chunk of each sequence
-  int4* work;            // [max_chunks] {b, chunk index, length, global chunk}
+  int4* work;            // [max_chunks] {b, first token, length, global chunk | single flag}
   float* part_lse;       // [max_chunks][num_q_heads] base-2 log-sum-exp of a chunk
   float* part_out;       // [max_chunks][num_q_heads][head_dim] chunk output, normalised
   unsigned char* q8;     // fp8 caches: [num_seqs * num_q_heads][2 * head_dim + 16] prepared q
+  int32_t* prefix_parts; // cascade: [num_seqs] prefix partials of each sequence
+  int2* prefix_items;    // cascade: [groups * max prefix chunks] (group, prefix chunk)
   int64_t max_chunks;
 };
 
 struct WorkspaceLayout {
-  size_t chunk_base, work, part_lse, part_out, q8, total;
+  size_t chunk_base, work, part_lse, part_out, q8, prefix_parts, prefix_items, total;
   int64_t max_chunks;
 };
 
+// num_groups > 0: the cascade layout (partials for each sequence's prefix
+// chunks too, the prefix item list).
 WorkspaceLayout decode_workspace_layout(int num_seqs, int num_q_heads, int head_dim,
-                                        int max_context_len, int chunk_tokens);
+                                        int max_context_len, int chunk_tokens,
+                                        int num_groups = 0);
 
 struct DecodeArgs {
   void* out;
@@ -39,6 +47,11 @@ struct DecodeArgs {
   int num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks;
   int max_blocks_per_seq, max_context_len, chunk_tokens;
   int q_len;  // new tokens per sequence (q and out are [num_seqs][q_len][num_q_heads][head_dim])
+  // cascade (num_groups > 0): sequences group_start[f] .. group_start[f+1]-1 share
+  // their first shared_lens[f] tokens (device arrays)
+  const int32_t* group_start = nullptr;
+  const int32_t* shared_lens = nullptr;
+  int num_groups = 0;
   int bf16;  // q / out element type: 1 bf16, 0 f32 (and the caches' unless kv8)
   int kv8;   // caches hold float8 e4m3 codes (q / out bf16)
   const float* k_scale;  // kv8: dequantisation scale per kv head, device memory
@@ -50,6 +63,7 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
+cudaError_t launch_cascade_plan(const DecodeArgs& a, cudaStream_t stream);
 
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
                                      const int64_t* slot_mapping, int num_tokens,

@@ -74,8 +74,13 @@ constexpr unsigned kFull = 0xffffffffu;
 constexpr float kNoScore = -3.0e38f;
 
 struct ItemDesc {
-  int b, h, chunk, len, gchunk, n_units, n_tokens, single, rot;
+  int b, h, tok0, len, gchunk, n_units, n_tokens, single, rot;
 };
+
+// Work entry of a (sequence, chunk): {sequence, first token of the chunk, sequence
+// length, global chunk index | kSingleChunk when the sequence is this one chunk
+// (its rows go straight to `out`)}.
+constexpr int kSingleChunk = 1 << 30;
 
 // Tensor-core consumer: bf16 with a group of 2..8 query heads per kv head.
 constexpr bool decode_uses_tensor_cores(bool bf16, int group) { return bf16 && group >= 2; }
@@ -965,7 +970,7 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
       const int j = i / Hkv;
       const int h = i - j * Hkv;
       const int4 w = p.work[j];                  // {b, chunk, length, global chunk}
-      const int tok0 = w.y * p.chunk_tokens;
+      const int tok0 = w.y;
       const int ntok = min(p.chunk_tokens, w.z - tok0);
       const int n_units = (ntok + Tr::UT - 1) / Tr::UT;
       const int page0 = tok0 / bs;
@@ -981,8 +986,8 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
       tbl_s[slot * 32 + lane] = phys;
       if (lane == 0) {
         ItemDesc d;
-        d.b = w.x; d.h = h; d.chunk = w.y; d.len = w.z; d.gchunk = w.w;
-        d.n_units = n_units; d.n_tokens = ntok; d.single = (w.z <= p.chunk_tokens);
+        d.b = w.x; d.h = h; d.tok0 = w.y; d.len = w.z; d.gchunk = w.w & (kSingleChunk - 1);
+        d.n_units = n_units; d.n_tokens = ntok; d.single = (w.w & kSingleChunk) != 0;
         d.rot = i % CW;
         desc[slot] = d;
       }
@@ -1121,7 +1126,7 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
     cs.begin(qbuf + slot * Tr::Q_BYTES, item_scale, kv_v);
     // row j may see positions up to L - q_len + j: relative to the item's first
     // token, the last visible token of this lane's row
-    const int qlim0 = d.len - p.q_len - d.chunk * p.chunk_tokens + cs.row_token(p.group_log2);
+    const int qlim0 = d.len - p.q_len - d.tok0 + cs.row_token(p.group_log2);
     __syncwarp();
     if (lane == 0) mbar_arrive(&item_empty[slot]);
 
