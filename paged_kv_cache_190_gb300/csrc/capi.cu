@@ -233,7 +233,8 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   a.ws.part_out = reinterpret_cast<float*>(ws + lay.part_out);
   a.ws.q8 = reinterpret_cast<unsigned char*>(ws + lay.q8);
   a.ws.prefix_parts = reinterpret_cast<int32_t*>(ws + lay.prefix_parts);
-  a.ws.prefix_items = reinterpret_cast<int2*>(ws + lay.prefix_items);
+  a.ws.prefix_items = reinterpret_cast<int4*>(ws + lay.prefix_items);
+  a.ws.inline_start = reinterpret_cast<int32_t*>(ws + lay.inline_start);
   a.group_start = group_start;
   a.shared_lens = shared_lens;
   a.num_groups = num_groups;

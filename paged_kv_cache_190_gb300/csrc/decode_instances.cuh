@@ -57,5 +57,7 @@ cudaError_t run_decode_fp8(int head_dim, int group, const DecodeKernelParams& kp
                            int device, cudaStream_t stream);
 cudaError_t launch_cascade_prefix(const DecodeArgs& a, const DecodeKernelParams& kp, int device,
                                   cudaStream_t stream);
+cudaError_t launch_cascade_merge(const DecodeArgs& a, const DecodeKernelParams& kp,
+                                 cudaStream_t stream);
 
 }  // namespace pa

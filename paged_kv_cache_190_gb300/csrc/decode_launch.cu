@@ -147,7 +147,7 @@ constexpr int kMergeWarps = 8;
 int64_t cascade_parts_per_seq(int max_context_len, int chunk_tokens, bool cascade) {
   if (max_context_len <= 0) return 0;
   const int64_t L = max_context_len;
-  return (L + chunk_tokens - 1) / chunk_tokens + (cascade ? (L + kPrefixChunk - 1) / kPrefixChunk : 0);
+  return (L + chunk_tokens - 1) / chunk_tokens + (cascade ? kMaxPrefixPieces : 0);
 }
 constexpr int kWideMergeWarps = 16;
 
@@ -198,9 +198,7 @@ __device__ __forceinline__ void store_row(void* out, int64_t o, const float* r) 
   }
 }
 
-// Split-K merge (log-sum-exp): for sequence b, query head i with n >= min_chunks
-// chunks (2 for pa_decode, whose single chunks write the output directly; 1 for
-// the cascade, where every chunk is a partial),
+// Split-K merge (log-sum-exp): for sequence b, query head i with n >= 2 chunks,
 //   out = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M),  M = max_c lse_c,
 // where o_c is chunk c's normalised output and lse_c its base-2 log-sum-exp.
 // One warp per (b, i) row, each lane owning head_dim / 32 columns; one pass with
@@ -208,8 +206,7 @@ __device__ __forceinline__ void store_row(void* out, int64_t o, const float* r) 
 template <bool BF16, int CPL>
 __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(
     const int32_t* __restrict__ chunk_base, const float* __restrict__ part_lse,
-    const float* __restrict__ part_out, void* __restrict__ out, int num_q_heads, int64_t rows,
-    int min_chunks) {
+    const float* __restrict__ part_out, void* __restrict__ out, int num_q_heads, int64_t rows) {
   constexpr int D = CPL * 32;
   wait_prior_grids();                     // the decode kernel's partials
   const int lane = threadIdx.x & 31;
@@ -219,7 +216,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(
   const int i = static_cast<int>(row - static_cast<int64_t>(b) * num_q_heads);
   const int c0 = chunk_base[b];
   const int n = chunk_base[b + 1] - c0;
-  if (n < min_chunks) return;             // one chunk: the decode kernel wrote the row
+  if (n < 2) return;                      // one chunk: the decode kernel wrote the row
   const int64_t prow0 = static_cast<int64_t>(c0) * num_q_heads + i;
   LseAcc<CPL> st;
 #pragma unroll 8
@@ -242,7 +239,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(
 template <bool BF16, int CPL>
 __global__ void __launch_bounds__(kWideMergeWarps * 32) decode_merge_wide_kernel(
     const int32_t* __restrict__ chunk_base, const float* __restrict__ part_lse,
-    const float* __restrict__ part_out, void* __restrict__ out, int num_q_heads, int min_chunks) {
+    const float* __restrict__ part_out, void* __restrict__ out, int num_q_heads) {
   constexpr int D = CPL * 32;
   __shared__ float sM[kWideMergeWarps], sS[kWideMergeWarps];
   __shared__ float sacc[kWideMergeWarps][D];
@@ -254,7 +251,7 @@ __global__ void __launch_bounds__(kWideMergeWarps * 32) decode_merge_wide_kernel
   const int i = static_cast<int>(row - static_cast<int64_t>(b) * num_q_heads);
   const int c0 = chunk_base[b];
   const int n = chunk_base[b + 1] - c0;
-  if (n < min_chunks) return;             // uniform over the block
+  if (n < 2) return;                      // uniform over the block
   const int64_t prow0 = static_cast<int64_t>(c0) * num_q_heads + i;
   LseAcc<CPL> st;
 #pragma unroll 8
@@ -311,22 +308,19 @@ template <bool BF16, int CPL>
 cudaError_t launch_merge(const DecodeArgs& a, cudaStream_t stream) {
   const int rows_q = a.q_len * a.num_q_heads;         // query rows per sequence
   const int64_t rows = static_cast<int64_t>(a.num_seqs) * rows_q;
-  const bool cascade = a.num_groups > 0;
   const int64_t max_chunks_per_seq = cascade_parts_per_seq(a.max_context_len, a.chunk_tokens,
-                                                           cascade);
-  const int min_chunks = cascade ? 1 : 2;
+                                                           false);
   if (max_chunks_per_seq >= 32)
     return launch_dependent(decode_merge_wide_kernel<BF16, CPL>, static_cast<unsigned>(rows),
                             kWideMergeWarps * 32, stream,
                             static_cast<const int32_t*>(a.ws.chunk_base),
                             static_cast<const float*>(a.ws.part_lse),
-                            static_cast<const float*>(a.ws.part_out), a.out, rows_q, min_chunks);
+                            static_cast<const float*>(a.ws.part_out), a.out, rows_q);
   const unsigned blocks = static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps);
   return launch_dependent(decode_merge_kernel<BF16, CPL>, blocks, kMergeWarps * 32, stream,
                           static_cast<const int32_t*>(a.ws.chunk_base),
                           static_cast<const float*>(a.ws.part_lse),
-                          static_cast<const float*>(a.ws.part_out), a.out, rows_q, rows,
-                          min_chunks);
+                          static_cast<const float*>(a.ws.part_out), a.out, rows_q, rows);
 }
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -391,11 +385,15 @@ WorkspaceLayout decode_workspace_layout(int num_seqs, int num_q_heads, int head_
   off += align256(static_cast<size_t>(num_seqs) * num_q_heads * (2 * head_dim + 16));
   w.prefix_parts = off;                   // the cascade's per-sequence prefix partials
   w.prefix_items = off;
+  w.inline_start = off;
   if (num_groups > 0) {
     off += align256(static_cast<size_t>(num_seqs) * 4);
-    w.prefix_items = off;                 // (group, prefix chunk) items
-    const int64_t per_group = (static_cast<int64_t>(max_context_len) + kPrefixChunk - 1) / kPrefixChunk;
-    off += align256(static_cast<size_t>(num_groups) * per_group * 8);
+    w.prefix_items = off;                 // (group, row set, piece, span) items
+    // row sets: one per group plus one per 64 rows (8 query heads per kv head at most)
+    const int64_t rowsets = num_groups + (static_cast<int64_t>(num_seqs) * 8 + 63) / 64;
+    off += align256(static_cast<size_t>(rowsets) * kMaxPrefixPieces * 16);
+    w.inline_start = off;
+    off += align256(static_cast<size_t>(num_seqs) * 4);
   }
   w.total = off;
   return w;
@@ -474,8 +472,9 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
   if (cascade) {
-    // the shared prefixes first (an ordinary launch after the plan), then the
-    // decode kernel over each sequence's own tokens
+    // the shared prefixes first, then the decode kernel over the sequences' long
+    // own suffixes, then the merge (which also attends to the short suffixes);
+    // each a programmatic dependent of the one before
     e = launch_cascade_prefix(a, kp, device, stream);
     if (e != cudaSuccess) return e;
   }
@@ -483,7 +482,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
       : a.bf16 ? run_decode_bf16(a.head_dim, rows, kp, grid, device, stream)
                : run_decode_f32(a.head_dim, rows, kp, grid, device, stream);
   if (e != cudaSuccess) return e;
-  if (cascade || a.max_context_len > a.chunk_tokens) {
+  if (cascade) return launch_cascade_merge(a, kp, stream);
+  if (a.max_context_len > a.chunk_tokens) {
     if (a.bf16 && a.head_dim == 128) e = launch_merge<true, 4>(a, stream);
     else if (a.bf16) e = launch_merge<true, 2>(a, stream);
     else if (a.head_dim == 128) e = launch_merge<false, 4>(a, stream);

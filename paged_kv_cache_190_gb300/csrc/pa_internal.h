@@ -10,7 +10,12 @@
 namespace pa {
 
 // Tokens of a group's shared prefix per item of the cascade prefix kernel.
-constexpr int kPrefixChunk = 128;
+// Shared-prefix decode: tokens per pipeline stage of the prefix kernel, most
+// prefix partials (pieces) per row, and the longest own suffix a sequence may
+// have for the merge kernel to attend to it directly.
+constexpr int kPrefixStageTokens = 64;
+constexpr int kMaxPrefixPieces = 32;
+constexpr int kInlineSuffixTokens = 32;
 
 // Workspace of one pa_decode call, carved from the caller's buffer.
 struct DecodeWorkspace {
@@ -21,12 +26,13 @@ struct DecodeWorkspace {
   float* part_out;       // [max_chunks][num_q_heads][head_dim] chunk output, normalised
   unsigned char* q8;     // fp8 caches: [num_seqs * num_q_heads][2 * head_dim + 16] prepared q
   int32_t* prefix_parts; // cascade: [num_seqs] prefix partials of each sequence
-  int2* prefix_items;    // cascade: [groups * max prefix chunks] (group, prefix chunk)
+  int4* prefix_items;    // cascade: (group, row set, piece, stages per piece)
+  int32_t* inline_start; // cascade: [num_seqs] first own token the merge attends to, or -1
   int64_t max_chunks;
 };
 
 struct WorkspaceLayout {
-  size_t chunk_base, work, part_lse, part_out, q8, prefix_parts, prefix_items, total;
+  size_t chunk_base, work, part_lse, part_out, q8, prefix_parts, prefix_items, inline_start, total;
   int64_t max_chunks;
 };
 
@@ -64,6 +70,7 @@ struct DecodeArgs {
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_cascade_plan(const DecodeArgs& a, cudaStream_t stream);
+int prefix_grid(int num_sms);   // CTAs of the shared-prefix kernel
 
 cudaError_t launch_reshape_and_cache(const void* k, const void* v, void* k_cache, void* v_cache,
                                      const int64_t* slot_mapping, int num_tokens,
