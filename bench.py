@@ -38,8 +38,8 @@ import pa_inputs  # noqa: E402
 METRIC = "paged decode KV-read GB/s (% of GB300 HBM peak); decode steps/s, µs/step"
 FALLBACK_HBM_GBS = 6800.0
 DEFAULT_WORKLOAD = "mha_bf16"   # Llama-2-7B-shaped MHA decode, bf16, batch 64
-DECODE_SOURCES = ["paged_decode.cuh", "decode_launch.cu", "decode_instances.cuh", "pa_device.cuh",
-                  "cascade.cu"]
+DECODE_SOURCES = ["paged_decode.cuh", "decode_launch.cu", "decode_instances.cuh", "pa_device.cuh"]
+CASCADE_SOURCES = DECODE_SOURCES + ["cascade.cu"]
 
 
 # ------------------------------------------------------------------ helpers
@@ -96,8 +96,9 @@ def source_digest(names) -> str:
 
 
 def ncu_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, or None when
-    the decode sources changed since it was captured."""
+    """DRAM bytes per decode call (the decode kernel's launch; for the cascade
+    the prefix and merge kernels') from the committed ncu summary, or None when
+    the kernel sources changed since it was captured."""
     path = os.path.join(ROOT, "profiles", f"decode_{workload}_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -106,7 +107,8 @@ def ncu_traffic(workload: str):
         if ":" in line and not line.startswith("#"):
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
-    if fields.get("source_digest") != source_digest(DECODE_SOURCES):
+    sources = CASCADE_SOURCES if "cascade" in workload else DECODE_SOURCES
+    if fields.get("source_digest") != source_digest(sources):
         return None
     try:
         return int(float(fields["dram_bytes_per_launch"]))

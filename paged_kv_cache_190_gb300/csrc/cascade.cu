@@ -273,7 +273,7 @@ __device__ __forceinline__ uint32_t prefix_swz(int row, int chunk) {
 // NG (1 or 2) consecutive 16-token groups of a stage, for one warp's 16 rows
 // (g and g + 8 of lane g * 4 + c): the scores of all 16 NG tokens first (2 NG
 // independent accumulation chains over head_dim), one online-softmax update
-// of the rows' maximum and sum (base 2), then O = O alpha + P V with NG k-steps.
+// of the rows' reference maximum and sum (base 2), then O += P V with NG k-steps.
 template <int D, int NG>
 __device__ __forceinline__ void prefix_step(uint32_t kg, uint32_t vg,
                                             const uint32_t (&qa)[D / 16][4],
@@ -309,10 +309,20 @@ __device__ __forceinline__ void prefix_step(uint32_t kg, uint32_t vg,
   x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, 2));
   x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, 1));
   x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, 2));
-  const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-  const float a0 = fast_exp2(m0 - n0), a1 = fast_exp2(m1 - n1);
-  m0 = n0;
-  m1 = n1;
+  // The reference maximum of a row only moves when a score exceeds it by more
+  // than 8 (every probability stays <= 2^8, exact in fp32 and bf16), and then
+  // for the whole warp: most steps rescale nothing.
+  const bool grow = x0 > m0 + 8.f || x1 > m1 + 8.f;
+  const bool rescale = __any_sync(kFull, grow);
+  float a0 = 1.f, a1 = 1.f;
+  if (rescale) {
+    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
+    a0 = fast_exp2(m0 - n0);
+    a1 = fast_exp2(m1 - n1);
+    m0 = n0;
+    m1 = n1;
+  }
+  const float n0 = m0, n1 = m1;
   float sum0 = 0.f, sum1 = 0.f;
   uint32_t pa[NG][4];
 #pragma unroll
@@ -335,17 +345,18 @@ __device__ __forceinline__ void prefix_step(uint32_t kg, uint32_t vg,
   }
   l0 = l0 * a0 + sum0;
   l1 = l1 * a1 + sum1;
-  // ---- O = O alpha + P V; V^T fragments for n-tiles 2j, 2j + 1
+  if (rescale) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      o[t][0] *= a0;
+      o[t][1] *= a0;
+      o[t][2] *= a1;
+      o[t][3] *= a1;
+    }
+  }
+  // ---- O = O + P V; V^T fragments for n-tiles 2j, 2j + 1
 #pragma unroll
   for (int j = 0; j < NT / 2; ++j) {
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      float(&od)[4] = o[2 * j + e];
-      od[0] *= a0;
-      od[1] *= a0;
-      od[2] *= a1;
-      od[3] *= a1;
-    }
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {
       uint32_t v00, v01, v10, v11;
