@@ -276,9 +276,11 @@ int pa_cascade_groups(const int32_t* block_tables, const int32_t* context_lens, 
  *
  * pa_decode_fp8: pa_decode over such pools, with the same arguments and
  * workspace (pa_decode_workspace_size with the same sizes).  The kernel uses
- * the codes as they are and applies K's scale to the logits and V's to the
- * output; products are computed with q and the probabilities rounded to f16
- * (every e4m3 value is exactly an f16) and fp32 accumulation.
+ * the codes as they are (e4m3 tensor-core products, fp32 accumulation) and
+ * applies K's scale to the logits and V's to the output.  The other operand of
+ * each product is carried as two e4m3 parts: q scaled per row by a power of
+ * two and split into hi + lo codes, and the probabilities (times 2^8) split
+ * the same way, so the result carries about the precision of bf16 operands.
  */
 int pa_reshape_and_cache_fp8(const void* k, const void* v, void* k_cache, void* v_cache,
                              const int64_t* slot_mapping, const float* k_scale,

@@ -96,8 +96,11 @@ struct DecodeTraits {
   static constexpr bool TC = KV8 || decode_uses_tensor_cores(BF16, G);
   // Consumer warps: the fp8 kernel keeps 6 so that the CTA's 8 warps get up to
   // 255 registers each (9 or more warps put 3 on some SM sub-partitions, which
-  // caps a thread at 168).
-  static constexpr int CW = KV8 ? 6 : kConsumerWarps;
+  // caps a thread at 168).  So does the 8-row kernel: its per-warp merge
+  // buffers (rows x head_dim floats each) are half its shared memory's fixed
+  // part, and with 6 warps 18 stages fit instead of 16 (measured on 2 draft
+  // tokens x GQA-4: 336 -> 314 us).
+  static constexpr int CW = (KV8 || G == 8) ? 6 : kConsumerWarps;
   static constexpr int THREADS = (CW + 2) * 32;                // + producer + scheduler
   static constexpr int ELT = KV8 ? 1 : (BF16 ? 2 : 4);         // cache element bytes
   static constexpr int QELT = BF16 ? 2 : 4;                    // q element bytes
@@ -1189,37 +1192,43 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
     last = __shfl_sync(kFull, last, 0);
     if (last) {
       if (lane == 0) *merge_cnt = 0;
-      // out[g] = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w over the 8 warps
-#pragma unroll 1
+      // out[g] = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w over the CW warps.
+      // The weights of every row first, then all rows' columns together, so
+      // that the merging warp has every row's loads in flight at once.
+      float f[G][CW], inv[G], lse[G];
+#pragma unroll
       for (int g = 0; g < G; ++g) {
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < CW; ++w) M = fmaxf(M, mml[(w * G + g) * 2]);
-        float f[CW];
         float lam = 0.f;
 #pragma unroll
         for (int w = 0; w < CW; ++w) {
           // a row with no visible token in this item (a new token before the
           // item's first position) has M = -inf: it contributes nothing
-          f[w] = M == -INFINITY ? 0.f : fast_exp2(mml[(w * G + g) * 2] - M);
-          lam = fmaf(f[w], mml[(w * G + g) * 2 + 1], lam);
+          f[g][w] = M == -INFINITY ? 0.f : fast_exp2(mml[(w * G + g) * 2] - M);
+          lam = fmaf(f[g][w], mml[(w * G + g) * 2 + 1], lam);
         }
-        const float inv = lam > 0.f ? 1.f / lam : 0.f;
-        // row g = (new token j, head gi of the group): query row j * Hq + h * group + gi
-        const int qh = (g >> p.group_log2) * p.num_q_heads + d.h * p.group + (g & (p.group - 1));
-        const int64_t rows_per_seq = static_cast<int64_t>(p.q_len) * p.num_q_heads;
+        inv[g] = lam > 0.f ? 1.f / lam : 0.f;
+        lse[g] = lam > 0.f ? M + __log2f(lam) : -INFINITY;
+      }
+      const int64_t rows_per_seq = static_cast<int64_t>(p.q_len) * p.num_q_heads;
 #pragma unroll
-        for (int cp = lane; cp < D / 2; cp += 32) {
-          const int dcol = 2 * cp;
+      for (int cp = lane; cp < D / 2; cp += 32) {
+        const int dcol = 2 * cp;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
           float o0 = 0.f, o1 = 0.f;
 #pragma unroll
           for (int w = 0; w < CW; ++w) {
             const float2 a = *reinterpret_cast<const float2*>(macc + (w * G + g) * D + dcol);
-            o0 = fmaf(f[w], a.x, o0);
-            o1 = fmaf(f[w], a.y, o1);
+            o0 = fmaf(f[g][w], a.x, o0);
+            o1 = fmaf(f[g][w], a.y, o1);
           }
-          o0 *= inv;
-          o1 *= inv;
+          o0 *= inv[g];
+          o1 *= inv[g];
+          // row g = (new token j, head gi of the group): query row j * Hq + h * group + gi
+          const int qh = (g >> p.group_log2) * p.num_q_heads + d.h * p.group + (g & (p.group - 1));
           if (d.single) {
             const int64_t o = (static_cast<int64_t>(d.b) * rows_per_seq + qh) * D + dcol;
             if constexpr (BF16) {
@@ -1231,7 +1240,7 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
           } else {
             const int64_t row = static_cast<int64_t>(d.gchunk) * rows_per_seq + qh;
             *reinterpret_cast<float2*>(p.part_out + row * D + dcol) = make_float2(o0, o1);
-            if (dcol == 0) p.part_lse[row] = lam > 0.f ? M + __log2f(lam) : -INFINITY;
+            if (dcol == 0) p.part_lse[row] = lse[g];
           }
         }
       }
