@@ -11,11 +11,11 @@
 //   * plan: per group, the prefix items (row set x piece of the shared tokens);
 //     per sequence, its prefix partials, then its own ("suffix") tokens: a short
 //     suffix is left to the merge, a long one becomes decode-kernel chunks;
+//   * the decode kernel over the long suffixes (chunks, as pa_decode);
 //   * prefix kernel: per (item, kv head) the shared K/V pages stream through
 //     shared memory once (TMA, a 3-stage pipeline) while every row of the group
 //     (members x query heads of the kv head) attends to them on the tensor
 //     cores; one partial per row and piece;
-//   * the decode kernel over the long suffixes (chunks, as pa_decode);
 //   * merge: per row, the partials (log-sum-exp) and, for a short suffix, the
 //     attention over its few tokens, computed in the same pass.
 #include <cuda.h>
@@ -34,6 +34,7 @@ namespace pa {
 namespace {
 
 constexpr int kCascadePlanThreads = 1024;
+constexpr int kPlanGroupCache = 2048;                   // groups the plan keeps in shared memory
 constexpr int kPrefixConsumerWarps = 4;                 // one 16-row tile each
 constexpr int kPrefixThreads = (kPrefixConsumerWarps + 1) * 32;   // + the producer warp
 constexpr int kPrefixRows = 16 * kPrefixConsumerWarps;  // rows of one item (a row set)
@@ -127,8 +128,8 @@ __device__ __forceinline__ PrefixShape prefix_shape(int sl, int members, int gro
 //     below a member's length sets PA_DEVERR_BAD_LENGTH, and that member is
 //     decoded without the sharing.
 __global__ void __launch_bounds__(kCascadePlanThreads) cascade_plan_kernel(
-    const int32_t* __restrict__ context_lens, const int32_t* __restrict__ group_start,
-    const int32_t* __restrict__ shared_lens, int num_groups, int num_seqs, int chunk_tokens,
+    const int32_t* __restrict__ context_lens, const int32_t* group_start,
+    const int32_t* shared_lens, int num_groups, int num_seqs, int chunk_tokens,
     int max_len, int block_size, int max_blocks_per_seq, int group, int num_kv_heads,
     int prefix_ctas, int32_t* __restrict__ header, int32_t* __restrict__ chunk_base,
     int32_t* __restrict__ prefix_parts, int32_t* __restrict__ inline_start,
@@ -137,8 +138,18 @@ __global__ void __launch_bounds__(kCascadePlanThreads) cascade_plan_kernel(
   __shared__ int warp_sums[kCascadePlanThreads / 32];
   __shared__ int total_s;
   __shared__ int carry_parts, carry_work, carry_items, units_s;
-  allow_next_grid();                      // the prefix kernel may start its prologue
+  __shared__ int32_t gs_cache[kPlanGroupCache + 1], sl_cache[kPlanGroupCache];
+  allow_next_grid();                      // the next kernel may start its prologue
   if (threadIdx.x == 0) carry_parts = carry_work = carry_items = units_s = 0;
+  // the group arrays are read many times (a binary search per sequence): keep
+  // them in shared memory when they fit
+  const bool cached = num_groups <= kPlanGroupCache;
+  if (cached) {
+    for (int i = threadIdx.x; i <= num_groups; i += kCascadePlanThreads) gs_cache[i] = group_start[i];
+    for (int i = threadIdx.x; i < num_groups; i += kCascadePlanThreads) sl_cache[i] = shared_lens[i];
+    group_start = gs_cache;
+    shared_lens = sl_cache;
+  }
   __syncthreads();
   // ---- 1a. total prefix work in stages (x kv heads)
   for (int base = 0; base < num_groups; base += kCascadePlanThreads) {
@@ -785,8 +796,8 @@ cudaError_t run_prefix(const DecodeArgs& a, const DecodeKernelParams& kp, int de
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  // a dependent of the plan kernel: its blocks start their prologue early and
-  // wait on the device for the item list
+  // a dependent of the decode kernel (itself one of the plan kernel): its
+  // blocks wait on the device for both, i.e. for the item list
   return launch_pdl(prefix_attention_kernel<D>, static_cast<unsigned>(prefix_grid(a.num_sms)),
                     kPrefixThreads, Ly::SMEM, stream, kp,
                     static_cast<const int32_t*>(a.group_start),

@@ -471,18 +471,19 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   int device = 0;
   e = cudaGetDevice(&device);
   if (e != cudaSuccess) return e;
-  if (cascade) {
-    // the shared prefixes first, then the decode kernel over the sequences' long
-    // own suffixes, then the merge (which also attends to the short suffixes);
-    // each a programmatic dependent of the one before
-    e = launch_cascade_prefix(a, kp, device, stream);
-    if (e != cudaSuccess) return e;
-  }
   e = a.kv8    ? run_decode_fp8(a.head_dim, rows, kp, grid, device, stream)
       : a.bf16 ? run_decode_bf16(a.head_dim, rows, kp, grid, device, stream)
                : run_decode_f32(a.head_dim, rows, kp, grid, device, stream);
   if (e != cudaSuccess) return e;
-  if (cascade) return launch_cascade_merge(a, kp, stream);
+  if (cascade) {
+    // after the decode kernel over the sequences' long own suffixes (often none,
+    // and then it ends right after the plan) come the shared prefixes and the
+    // merge, which also attends to the short suffixes; each launch is a
+    // programmatic dependent of the one before
+    e = launch_cascade_prefix(a, kp, device, stream);
+    if (e != cudaSuccess) return e;
+    return launch_cascade_merge(a, kp, stream);
+  }
   if (a.max_context_len > a.chunk_tokens) {
     if (a.bf16 && a.head_dim == 128) e = launch_merge<true, 4>(a, stream);
     else if (a.bf16) e = launch_merge<true, 2>(a, stream);
