@@ -44,9 +44,10 @@ def _oracle(case, write=True):
                              case.num_kv_heads, "bf16")
 
 
-# groups of 5, 1, 3 and 4 sequences sharing 160 tokens (one full prefix chunk of
-# 128 and a ragged one), nothing, 384 (three full chunks) and 64; the suffixes
-# run from one token (L = shared + 1) to several chunks
+# groups of 5, 1, 3 and 4 sequences sharing 160 tokens (two full 64-token
+# stages of the prefix kernel and a ragged one), nothing, 384 (six full stages)
+# and 64; the own suffixes run from one token (L = shared + 1, attended to in
+# the merge) to several decode-kernel chunks
 LENS = [161, 300, 200, 225, 500, 77, 385, 700, 390, 65, 90, 1000, 66]
 GROUPS = [5, 1, 3, 4]
 SHARED = [160, 0, 384, 64]
@@ -79,9 +80,10 @@ def test_cascade_close_to_plain_decode():
     assert diff.max() <= 2e-2 and diff.mean() <= 1e-3
 
 
-def test_long_prefix_goes_through_the_wide_merge():
-    """A 4096-token shared prefix with 64-token chunks: 32 prefix partials plus the
-    suffix chunks per row (the merge for long partial lists)."""
+def test_long_prefix_with_the_most_pieces():
+    """A 4096-token shared prefix (64 stages) cut into the most pieces a group
+    may have (32), then 64-token decode chunks of the own suffixes: up to 47
+    partials per row."""
     lens = [4096 + 70, 4096 + 1, 4096 + 300, 5000]
     case, starts, shared = _grouped_case("cascade-long", 1260, 16, 4, 128, 16, lens, [4],
                                          [4096])
@@ -181,3 +183,33 @@ def test_host_refusals():
     with pytest.raises(ValueError):                       # group_start must have G + 1 entries
         pa.pa_decode_cascade(out, q, kc, kc, *args, to_dev(shared), to_dev(shared), case.scale,
                              1, 40)
+
+
+@pytest.mark.parametrize("Hq,Hkv,members", [(16, 4, 24), (16, 2, 17), (8, 8, 70)])
+def test_groups_wider_than_one_row_set(Hq, Hkv, members):
+    """More than 64 rows in a group (members x query heads per kv head): the
+    prefix work is split into several row sets (96, 136 and 70 rows here),
+    the last one partial."""
+    rng = np.random.default_rng(1310 + members)
+    shared = 320                                          # 5 stages of 64 tokens
+    lens = [shared + int(x) for x in rng.integers(1, 90, size=members)] + [150, 60]
+    case, starts, shared_lens = _grouped_case(f"cascade-wide-{Hq}-{Hkv}-{members}", 1310 + members,
+                                              Hq, Hkv, 128, 16, lens, [members, 2], [shared, 48])
+    out, flags, _ = _cascade(case, starts, shared_lens)
+    assert flags == 0
+    check_tolerance(out_as_f64(out), _oracle(case), "bf16", case.name)
+
+
+def test_more_groups_than_the_plan_caches():
+    """2100 groups (the plan keeps at most 2048 in shared memory): pairs of
+    sequences sharing one page, and singles."""
+    rng = np.random.default_rng(1320)
+    sizes = [2 if i % 3 == 0 else 1 for i in range(2100)]
+    lens = []
+    for s in sizes:
+        lens += [16 + int(x) for x in rng.integers(1, 40, size=s)]
+    case, starts, shared = _grouped_case("cascade-many-groups", 1320, 8, 8, 64, 16, lens, sizes,
+                                         [16 if s == 2 else 0 for s in sizes])
+    out, flags, _ = _cascade(case, starts, shared)
+    assert flags == 0
+    check_tolerance(out_as_f64(out), _oracle(case), "bf16", case.name)
