@@ -428,7 +428,11 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   DecodeKernelParams kp;
   std::memset(&kp, 0, sizeof(kp));
   const int group = a.num_q_heads / a.num_kv_heads;
-  const int rows = a.q_len * group;                   // rows per (sequence, kv head) item
+  // fp8 pools with 16-token pages: items over kv-head pairs, so that one copy
+  // takes both heads' rows of a page (4 KiB instead of two of 2 KiB)
+  const bool paired = a.kv8 && a.block_size == 16 && a.q_len == 1 && a.num_kv_heads % 2 == 0 &&
+                      group <= 4;
+  const int rows = (paired ? 2 : 1) * a.q_len * group;   // rows per item
   // the kernel instance is chosen by the rows of an item, and so is its consumer
   // (the cascade's prefix kernel reads through the maps too)
   if (a.kv8 || cascade || decode_uses_tensor_cores(a.bf16 != 0, rows)) {
@@ -437,7 +441,8 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
     // one box per page a unit touches: min(page, unit) rows
     const int unit_tokens =
         a.kv8 ? DecodeTraits<true, 128, 4, true>::UT : DecodeTraits<true, 128, 4, false>::UT;
-    const int box_rows = a.block_size < unit_tokens ? a.block_size : unit_tokens;
+    const int box_rows = paired ? 2 * a.block_size
+                                : (a.block_size < unit_tokens ? a.block_size : unit_tokens);
     e = make_pool_map(&kp.tmap_k, a.k_cache, a.head_dim, rows, kv_elt, box_rows);
     if (e == cudaSuccess)
       e = make_pool_map(&kp.tmap_v, a.v_cache, a.head_dim, rows, kv_elt, box_rows);
@@ -450,7 +455,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   kp.block_tables = a.block_tables;
   kp.scale_log2 = static_cast<float>(static_cast<double>(a.scale) * 1.4426950408889634);
   kp.num_q_heads = a.num_q_heads;
-  kp.num_kv_heads = a.num_kv_heads;
+  kp.num_kv_heads = paired ? a.num_kv_heads / 2 : a.num_kv_heads;   // item heads
+  kp.pool_heads = a.num_kv_heads;
+  kp.head_pairs = paired ? 1 : 0;
+  kp.pair_shift = group >= 4 ? 2 : (group >= 2 ? 1 : 0);
   kp.block_size = a.block_size;
   kp.num_blocks = a.num_blocks;
   kp.max_blocks_per_seq = a.max_blocks_per_seq;
@@ -464,9 +472,10 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   kp.k_scale = a.k_scale;
   kp.v_scale = a.v_scale;
   kp.q_len = a.q_len;
-  kp.group = group;
-  kp.group_log2 = group >= 8 ? 3 : (group >= 4 ? 2 : (group >= 2 ? 1 : 0));
-  const int64_t items_upper = a.ws.max_chunks * a.num_kv_heads;
+  const int item_group = paired ? 2 * group : group;   // query heads of an item
+  kp.group = item_group;
+  kp.group_log2 = item_group >= 8 ? 3 : (item_group >= 4 ? 2 : (item_group >= 2 ? 1 : 0));
+  const int64_t items_upper = a.ws.max_chunks * kp.num_kv_heads;
   const int grid = static_cast<int>(items_upper < a.num_sms ? items_upper : a.num_sms);
   int device = 0;
   e = cudaGetDevice(&device);

@@ -188,6 +188,12 @@ struct DecodeKernelParams {
   // head (a power of two, as log2): an item's G rows are (token j, head g) =
   // row j * group + g
   int q_len, group, group_log2;
+  // fp8 pools with 16-token pages: items over kv-head pairs (head_pairs = 1).
+  // num_kv_heads and group then count pairs and the pair's query rows; a stage
+  // holds 16 positions of both heads (one 32-row box per pool: the two heads'
+  // rows of a page are adjacent), and row g belongs to head 2 h + (g >> pair_shift).
+  int head_pairs, pair_shift;
+  int pool_heads;                   // kv heads of the pools (the row stride of a page)
 };
 
 // Butterfly step over lane bit `mask` (within 8-lane groups): lanes with the
@@ -711,6 +717,10 @@ struct Fp8TensorConsumer {
   float o[MT][4];
   float m, l, sc, vscale;
   int lane;
+  // head pair (pshift >= 0): row g belongs to head g >> pshift of the pair, and
+  // tokens 0-15 / 16-31 of a block are the 16 positions of head 0 / head 1
+  int pshift = -1, rsub = 0;
+  float sc1 = 0.f, vscale1 = 0.f;
 
   __device__ __forceinline__ void init(int lane_, float*) { lane = lane_; }
 
@@ -718,10 +728,19 @@ struct Fp8TensorConsumer {
     return (lane >> 2) >> group_log2;
   }
 
+  // The second head's scales when the items are head pairs (shift >= 0).
+  __device__ __forceinline__ void set_pair(int shift, float score_scale1, float v_scale1) {
+    pshift = shift;
+    sc1 = score_scale1;
+    vscale1 = v_scale1 * (1.f / kPScale);
+  }
+
   __device__ __forceinline__ void begin(const char* qs, float score_scale, float v_scale) {
     const int g = lane >> 2, c = lane & 3;
     float qinv = 0.f;
     qrow = g < G;
+    rsub = pshift >= 0 ? (g >> pshift) & 1 : 0;
+    if (rsub) score_scale = sc1;
     // the q' fragments are read from shared memory in every unit (the slot
     // stays valid for the whole item), which keeps 16 registers free
     qaddr = smem_addr(qs + (qrow ? g : 0) * Tr::QROW_BYTES + 4 * c);
@@ -782,8 +801,10 @@ struct Fp8TensorConsumer {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
         const int tk = 8 * n + 2 * c + e;
+        // a head pair: this row sees only its own head's half, positions tk % 16
+        const bool seen = pshift < 0 ? tk <= lim : ((tk >> 4) == rsub && (tk & 15) <= lim);
         const float v = (sh[n][e] + sh[n][e + 2]) * sc;
-        sv[2 * n + e] = tk <= lim ? v : -INFINITY;
+        sv[2 * n + e] = seen ? v : -INFINITY;
         mx = fmaxf(mx, sv[2 * n + e]);
       }
     mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, 1));
@@ -849,6 +870,9 @@ struct Fp8TensorConsumer {
       mml_w[g * 2 + 1] = lt;
     }
     const int h0 = 2 * c, h1 = 2 * c + 1;
+    // V's scale of each column's row (its head of the pair)
+    const float vs0 = pshift >= 0 && ((h0 >> pshift) & 1) ? vscale1 : vscale;
+    const float vs1 = pshift >= 0 && ((h1 >> pshift) & 1) ? vscale1 : vscale;
 #pragma unroll
     for (int mt = 0; mt < MT; ++mt) {
       if constexpr (kPackPV) {             // add the lo columns (lane c + 2) to the hi ones
@@ -857,12 +881,12 @@ struct Fp8TensorConsumer {
       }
       const int d0 = 16 * mt + 2 * g, d1 = d0 + 1;     // O^T rows g and g + 8
       if (h0 < G) {
-        macc_w[h0 * D + d0] = o[mt][0] * vscale;
-        macc_w[h0 * D + d1] = o[mt][2] * vscale;
+        macc_w[h0 * D + d0] = o[mt][0] * vs0;
+        macc_w[h0 * D + d1] = o[mt][2] * vs0;
       }
       if (h1 < G) {
-        macc_w[h1 * D + d0] = o[mt][1] * vscale;
-        macc_w[h1 * D + d1] = o[mt][3] * vscale;
+        macc_w[h1 * D + d0] = o[mt][1] * vs1;
+        macc_w[h1 * D + d1] = o[mt][3] * vs1;
       }
     }
   }
@@ -928,6 +952,9 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
 
   const int Hkv = p.num_kv_heads;
   const int bs = p.block_size;
+  // positions per unit: a head-pair stage holds half as many of each head
+  const bool paired = KV8 && p.head_pairs != 0;
+  const int PU = paired ? Tr::UT / 2 : Tr::UT;
 
   if (warp == CW + 1) {
     // ----------------------------------------------------------- scheduler
@@ -975,7 +1002,7 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
       const int4 w = p.work[j];                  // {b, chunk, length, global chunk}
       const int tok0 = w.y;
       const int ntok = min(p.chunk_tokens, w.z - tok0);
-      const int n_units = (ntok + Tr::UT - 1) / Tr::UT;
+      const int n_units = (ntok + PU - 1) / PU;
       const int page0 = tok0 / bs;
       const int npages = (ntok + bs - 1) / bs;
       int phys = -1;
@@ -1049,10 +1076,22 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
             ok = false;
             break;
           }
-          const int tok = u * Tr::UT;
+          const int tok = u * PU;
           char* dst = stages + s * Tr::STAGE_BYTES;
           const int pp = tbl_s[slot * 32 + tok / bs];
-          if constexpr (Tr::TC) {
+          if (paired) {
+            // one box per pool: the page's 16 rows of head 2h, then of head 2h + 1
+            if (pp >= 0) {
+              stage_bad[s] = 0;
+              mbar_arrive_expect_tx(&full[s], Tr::STAGE_BYTES);
+              const int row = (pp * p.pool_heads + 2 * d.h) * bs;
+              tma_rows<Tr>(dst, &p.tmap_k, row, &full[s]);
+              tma_rows<Tr>(dst + Tr::TILE_BYTES, &p.tmap_v, row, &full[s]);
+            } else {
+              stage_bad[s] = 1;
+              mbar_arrive(&full[s]);
+            }
+          } else if constexpr (Tr::TC) {
             // one tensor-map box per page the unit touches (a unit longer than
             // a page takes several; the last unit of an item only those it
             // needs) and pool, each taking all 128-byte slabs of its rows
@@ -1070,7 +1109,7 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
               for (int j = 0; j < n_op; ++j) {
                 const int t = tok + j * rows_op;
                 const int pj = j == 0 ? pp : tbl_s[slot * 32 + t / bs];
-                const int row = (pj * Hkv + d.h) * bs + t % bs;
+                const int row = (pj * p.pool_heads + d.h) * bs + t % bs;
                 tma_rows<Tr>(dst + j * rows_op * 128, &p.tmap_k, row, &full[s]);
                 tma_rows<Tr>(dst + Tr::TILE_BYTES + j * rows_op * 128, &p.tmap_v, row, &full[s]);
               }
@@ -1082,7 +1121,7 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
             stage_bad[s] = 0;
             mbar_arrive_expect_tx(&full[s], Tr::STAGE_BYTES);
             const int64_t off =
-                ((static_cast<int64_t>(pp) * Hkv + d.h) * bs + (tok % bs)) * Tr::ROW_BYTES;
+                ((static_cast<int64_t>(pp) * p.pool_heads + d.h) * bs + (tok % bs)) * Tr::ROW_BYTES;
             bulk_g2s(dst, p.k_cache + off, Tr::TILE_BYTES, &full[s]);
             bulk_g2s(dst + Tr::TILE_BYTES, p.v_cache + off, Tr::TILE_BYTES, &full[s]);
           } else {
@@ -1124,8 +1163,16 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
     const ItemDesc d = desc[slot];
     if (d.b < 0 || *abort_flag) break;
     // fp8 caches: K's head scale folds into the score scale, V's into the output
-    const float kv_k = KV8 ? p.k_scale[d.h] : 1.f, kv_v = KV8 ? p.v_scale[d.h] : 1.f;
+    const int kvh = paired ? 2 * d.h : d.h;       // (first) kv head of the item
+    const float kv_k = KV8 ? p.k_scale[kvh] : 1.f, kv_v = KV8 ? p.v_scale[kvh] : 1.f;
     const float item_scale = p.scale_log2 * kv_k;
+    if constexpr (KV8) {
+      // a head pair: rows of the second head take its own scales
+      if (paired)
+        cs.set_pair(p.pair_shift, p.scale_log2 * p.k_scale[kvh + 1], p.v_scale[kvh + 1]);
+      else
+        cs.set_pair(-1, 0.f, 0.f);
+    }
     cs.begin(qbuf + slot * Tr::Q_BYTES, item_scale, kv_v);
     // row j may see positions up to L - q_len + j: relative to the item's first
     // token, the last visible token of this lane's row
@@ -1143,27 +1190,32 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
         aborted = true;
         break;
       }
-      const int nt = min(Tr::UT, d.n_tokens - u * Tr::UT);
+      const int nt = min(PU, d.n_tokens - u * PU);     // positions of the unit
       if (!stage_bad[s]) {
         char* kt = stages + s * Tr::STAGE_BYTES;
         char* vt = kt + Tr::TILE_BYTES;
         if constexpr (Tr::TC) {
           // The tensor cores multiply every row of the tile, so value rows past
           // the sequence (stale or never-written slots) must not hold NaN or Inf.
-          if (nt < Tr::UT) {
-            for (int i = lane; i < (Tr::UT - nt) * Tr::BOXES * 8; i += 32) {
-              const int row = nt + i / (Tr::BOXES * 8);
+          if (nt < PU) {
+            // (a head-pair stage: positions nt.. of both halves)
+            const int per_half = PU - nt;
+            const int nzero = paired ? 2 * per_half : Tr::UT - nt;
+            for (int i = lane; i < nzero * Tr::BOXES * 8; i += 32) {
+              const int k = i / (Tr::BOXES * 8);
+              const int row = paired ? (k < per_half ? nt + k : PU + nt + (k - per_half)) : nt + k;
               const int rest = i % (Tr::BOXES * 8);
-              *reinterpret_cast<uint4*>(vt + (rest >> 3) * Tr::BOX_BYTES + row * 128 +
-                                        (rest & 7) * 16) = make_uint4(0, 0, 0, 0);
+              if (row < Tr::UT)
+                *reinterpret_cast<uint4*>(vt + (rest >> 3) * Tr::BOX_BYTES + row * 128 +
+                                          (rest & 7) * 16) = make_uint4(0, 0, 0, 0);
             }
             __syncwarp();
           }
         }
-        cs.unit(kt, vt, nt, qlim0 - u * Tr::UT, item_scale, [&] {
+        cs.unit(kt, vt, nt, qlim0 - u * PU, item_scale, [&] {
           if constexpr (Tr::TC) {
             // order this warp's generic-proxy writes before the next tensor copy here
-            if (nt < Tr::UT) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            if (nt < PU) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(&empty[s]);

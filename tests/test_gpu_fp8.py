@@ -121,6 +121,21 @@ def test_decode_fp8_every_group(G, bs):
     check_tolerance(got, oracle_step(case), "fp8", case.name)
 
 
+@pytest.mark.parametrize("Hkv,G", [(3, 2), (6, 1), (4, 4)])
+def test_decode_fp8_head_pairs_and_odd_head_counts(Hkv, G):
+    """16-token pages: an even number of kv heads runs items over head pairs
+    (one 32-row copy per page and pool, each row masked to its own head, each
+    head with its own scales); an odd number runs single-head items."""
+    case = pa_inputs.make_decode_case(
+        f"fp8-pairs-{Hkv}-{G}", seed=540 + Hkv + G, dtype="fp8", num_seqs=4,
+        num_q_heads=Hkv * G, num_kv_heads=Hkv, head_dim=128, block_size=16,
+        lens=("list", [2, 31, 48, 333]))
+    dc = DeviceCase(case)
+    got = out_as_f64(dc.step(chunk_tokens=64))
+    assert dc.device_errors() == 0
+    check_tolerance(got, oracle_step(case), "fp8", case.name)
+
+
 def test_decode_fp8_split_sizes_agree():
     case = pa_inputs.make_decode_case("fp8-split", seed=51, dtype="fp8", num_seqs=3,
                                       num_q_heads=8, num_kv_heads=2, head_dim=128,
