@@ -90,3 +90,29 @@ def test_workspace_size_with_explicit_chunk_is_monotone():
     # chunk must be a multiple of 16 and of the block size, at most 32 pages
     assert pa.pa_decode_workspace_size(4, 32, 8, 128, 32, 2000, 48) == 0
     assert pa.pa_decode_workspace_size(4, 32, 8, 128, 16, 2000, 1024) == 0
+
+
+def test_cascade_host_checks():
+    """pa_decode_cascade refuses bad group arguments on the host; its workspace
+    covers the decode's and grows with the groups."""
+    lib = pa.library()
+    buf = (ctypes.c_uint8 * 4096)()
+    p = (ctypes.addressof(buf) + 255) & ~255
+
+    def call(num_groups=2, gs=p, sl=p, hq=32, b=4, d=128, bs=16):
+        return lib.pa_decode_cascade(p, p, p, p, p, p, gs, sl, num_groups, 1.0, 8, b, hq, d, bs,
+                                     64, 8, 100, 64, p, 1 << 30, None, None)
+    assert call(num_groups=0) == -1                 # at least one group
+    assert call(num_groups=5) == -1                 # more groups than sequences
+    assert call(gs=None) == -1
+    assert call(sl=None) == -1
+    assert call(d=96) == -2
+    assert call(bs=8) == -2
+    assert call(hq=16 * 8) == -2                    # 16 query heads per kv head
+    assert call(b=0, num_groups=0) == 0             # nothing to do
+    dec = pa.pa_decode_workspace_size(4, 32, 8, 128, 16, 2000, 64)
+    c1 = pa.pa_decode_cascade_workspace_size(4, 1, 32, 8, 128, 16, 2000, 64)
+    c2 = pa.pa_decode_cascade_workspace_size(4, 3, 32, 8, 128, 16, 2000, 64)
+    assert dec < c1 <= c2
+    assert lib.pa_decode_cascade_workspace_size(4, 0, 32, 8, 128, 16, 2000, 64) == 0
+    assert lib.pa_decode_cascade_workspace_size(4, 1, 32, 8, 128, 32, 2000, 48) == 0  # 1.5 pages
