@@ -587,10 +587,12 @@ __global__ void __launch_bounds__(kPrefixThreads) prefix_attention_kernel(
 //   out = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M),  M = max_c lse_c,
 // each lane owning CPL = head_dim / 32 columns.  A short own suffix
 // [inline_start[b], L_b) (at most 32 tokens) is one more term per row, computed
-// here: lane j takes token inline_start[b] + j (its page and whole K row) and
-// forms the G scores q_g.k_j (q rows from shared memory); the base-2 softmax of
-// each row runs over the lanes; the weighted sum of V uses every token's V
-// columns of this lane, all loaded up front.  Every load of the warp (pages,
+// here: the suffix's tokens share the warp, LPT = 32 / (its length rounded up to
+// a power of two) lanes each (at most one 16-byte piece of the row per lane
+// and token fewer), every lane forming the G partial scores of its part of its
+// token's K row (q rows as fp32 in shared memory), summed over the token's
+// lanes; the base-2 softmax of each row runs over the tokens; the weighted sum
+// of V uses every token's V columns of this lane, all loaded up front.  Every load of the warp (pages,
 // then K, V and the partials) is issued before the arithmetic that needs it.
 // Rows with neither (L_b = 0) were zeroed by the plan.
 template <int CPL, int G>
@@ -600,7 +602,7 @@ __global__ void __launch_bounds__(kCascadeMergeWarps * 32) cascade_merge_kernel(
     int max_len, int num_seqs) {
   constexpr int D = CPL * 32;
   constexpr int KV = D / 8;                     // 16-byte pieces of a row
-  __shared__ __align__(16) uint16_t q_s[kCascadeMergeWarps][G * D];
+  __shared__ __align__(16) float q_s[kCascadeMergeWarps][G * D];
   wait_prior_grids();                           // every partial is written
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
@@ -616,34 +618,45 @@ __global__ void __launch_bounds__(kCascadeMergeWarps * 32) cascade_merge_kernel(
   const int L = s0 >= 0 ? min(max(context_lens[b], 0), max_len) : 0;
   const int nsuf = s0 >= 0 ? min(L - s0, 32) : 0;
   const int64_t row0 = static_cast<int64_t>(b) * Hq + h * G;   // first output row
-  // ---- the G q rows -> shared memory; this lane's token and its page
+  // ---- the G q rows -> shared memory as fp32
   if (nsuf > 0) {
     const uint4* qsrc = reinterpret_cast<const uint4*>(p.q) + row0 * KV;
-    uint4* qdst = reinterpret_cast<uint4*>(q_s[warp]);
-    for (int e = lane; e < G * KV; e += 32) qdst[e] = qsrc[e];
+    float4* qdst = reinterpret_cast<float4*>(q_s[warp]);
+    for (int e = lane; e < G * KV; e += 32) {
+      const uint4 w = qsrc[e];
+      qdst[2 * e] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+      qdst[2 * e + 1] = make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+    }
   }
+  // ---- this lane's token (LPT lanes per token), its page and its part of the K row
+  int p2 = 1;
+  while (p2 < nsuf) p2 <<= 1;
+  const int lpt = min(32 / p2, KV);              // lanes per token
+  const int per = KV / lpt;                      // 16-byte pieces per lane
+  const int tok = lane / lpt, part = lane - tok * lpt;
   int page = -1;
-  if (lane < nsuf) {
-    const int t = s0 + lane;
+  if (tok < nsuf) {
+    const int t = s0 + tok;
     page = p.block_tables[static_cast<int64_t>(b) * p.max_blocks_per_seq + t / bs];
     if (page < 0 || page >= p.num_blocks) {
-      report(p.device_errors, PA_DEVERR_BAD_BLOCK);
+      if (part == 0) report(p.device_errors, PA_DEVERR_BAD_BLOCK);
       page = -1;
     }
   }
   const int64_t kv_row =
-      page >= 0 ? ((static_cast<int64_t>(page) * Hkv + h) * bs + (s0 + lane) % bs) * D : 0;
-  // ---- K row of this lane's token; this lane's V columns of every token
+      page >= 0 ? ((static_cast<int64_t>(page) * Hkv + h) * bs + (s0 + tok) % bs) * D : 0;
   uint4 kr[KV];
 #pragma unroll
   for (int e = 0; e < KV; ++e)
-    kr[e] = page >= 0 ? reinterpret_cast<const uint4*>(p.k_cache + kv_row * 2)[e]
-                      : make_uint4(0, 0, 0, 0);
+    kr[e] = page >= 0 && e < per
+                ? reinterpret_cast<const uint4*>(p.k_cache + kv_row * 2)[part * per + e]
+                : make_uint4(0, 0, 0, 0);
+  // ---- this lane's V columns of every token (token j's row from its first lane)
   using VCols = typename std::conditional<CPL == 4, uint2, uint32_t>::type;
   VCols vr[32];
 #pragma unroll
   for (int j = 0; j < 32; ++j) {
-    const int64_t rj = __shfl_sync(kFull, kv_row, j);   // token j's row (0 when unreadable)
+    const int64_t rj = __shfl_sync(kFull, kv_row, j < nsuf ? j * lpt : 0);
     vr[j] = j < nsuf ? *reinterpret_cast<const VCols*>(p.v_cache + (rj + lane * CPL) * 2)
                      : VCols{};
   }
@@ -665,21 +678,35 @@ __global__ void __launch_bounds__(kCascadeMergeWarps * 32) cascade_merge_kernel(
     for (int k = 0; k < CPL; ++k) acc[g][k] = fmaf(acc[g][k], sc, w * v[k]);
     M[g] = Mn;
   };
-#pragma unroll 2
-  for (int cc = 0; cc < n; ++cc) {
-    const int64_t prow = (static_cast<int64_t>(c0) + cc) * Hq + h * G;
+  // Each row's largest log-sum-exp first (lane i takes the (partial, row)
+  // entries i, i + 32, ...: row i % G, as 32 is a multiple of G), so that the
+  // weighted sum below has no chain from one partial to the next.
+  if (n > 0) {
+    float mloc = kNoScore;
+    for (int i = lane; i < n * G; i += 32)
+      mloc = fmaxf(mloc, p.part_lse[(static_cast<int64_t>(c0) + i / G) * Hq + h * G + i % G]);
+    for (int o2 = 16; o2 >= G; o2 >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, o2));
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float* src = p.part_out + (prow + g) * D + lane * CPL;
-      float v[CPL];
-      if constexpr (CPL == 4) {
-        const float4 t4 = *reinterpret_cast<const float4*>(src);
-        v[0] = t4.x; v[1] = t4.y; v[2] = t4.z; v[3] = t4.w;
-      } else {
-        const float2 t2 = *reinterpret_cast<const float2*>(src);
-        v[0] = t2.x; v[1] = t2.y;
+    for (int g = 0; g < G; ++g) M[g] = __shfl_sync(kFull, mloc, g);   // lane g holds row g's
+#pragma unroll 4
+    for (int cc = 0; cc < n; ++cc) {
+      const int64_t prow = (static_cast<int64_t>(c0) + cc) * Hq + h * G;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float* src = p.part_out + (prow + g) * D + lane * CPL;
+        const float w = fast_exp2(p.part_lse[prow + g] - M[g]);   // 0 for an empty partial
+        float v[CPL];
+        if constexpr (CPL == 4) {
+          const float4 t4 = *reinterpret_cast<const float4*>(src);
+          v[0] = t4.x; v[1] = t4.y; v[2] = t4.z; v[3] = t4.w;
+        } else {
+          const float2 t2 = *reinterpret_cast<const float2*>(src);
+          v[0] = t2.x; v[1] = t2.y;
+        }
+        S[g] += w;
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) acc[g][k] = fmaf(w, v[k], acc[g][k]);
       }
-      add(g, p.part_lse[prow + g], v);
     }
   }
   // ---- the suffix term of each row
@@ -688,27 +715,34 @@ __global__ void __launch_bounds__(kCascadeMergeWarps * 32) cascade_merge_kernel(
     float s[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) s[g] = 0.f;
-    const uint4* qv = reinterpret_cast<const uint4*>(q_s[warp]);
+    const float4* qv = reinterpret_cast<const float4*>(q_s[warp]);
 #pragma unroll
     for (int e = 0; e < KV; ++e) {
-      const uint4 kk = kr[e];
-      const float k0 = bf16_lo(kk.x), k1 = bf16_hi(kk.x), k2 = bf16_lo(kk.y), k3 = bf16_hi(kk.y);
-      const float k4 = bf16_lo(kk.z), k5 = bf16_hi(kk.z), k6 = bf16_lo(kk.w), k7 = bf16_hi(kk.w);
+      if (e < per) {                              // uniform over the warp
+        const uint4 kk = kr[e];
+        const float k0 = bf16_lo(kk.x), k1 = bf16_hi(kk.x), k2 = bf16_lo(kk.y), k3 = bf16_hi(kk.y);
+        const float k4 = bf16_lo(kk.z), k5 = bf16_hi(kk.z), k6 = bf16_lo(kk.w), k7 = bf16_hi(kk.w);
+        const int ci = part * per + e;            // 16-byte piece of the row: 8 columns
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const uint4 qq = qv[g * KV + e];
-        float d = s[g];
-        d = fmaf(bf16_lo(qq.x), k0, d);
-        d = fmaf(bf16_hi(qq.x), k1, d);
-        d = fmaf(bf16_lo(qq.y), k2, d);
-        d = fmaf(bf16_hi(qq.y), k3, d);
-        d = fmaf(bf16_lo(qq.z), k4, d);
-        d = fmaf(bf16_hi(qq.z), k5, d);
-        d = fmaf(bf16_lo(qq.w), k6, d);
-        d = fmaf(bf16_hi(qq.w), k7, d);
-        s[g] = d;
+        for (int g = 0; g < G; ++g) {
+          const float4 qa = qv[(g * D) / 4 + 2 * ci], qb = qv[(g * D) / 4 + 2 * ci + 1];
+          float d = s[g];
+          d = fmaf(qa.x, k0, d);
+          d = fmaf(qa.y, k1, d);
+          d = fmaf(qa.z, k2, d);
+          d = fmaf(qa.w, k3, d);
+          d = fmaf(qb.x, k4, d);
+          d = fmaf(qb.y, k5, d);
+          d = fmaf(qb.z, k6, d);
+          d = fmaf(qb.w, k7, d);
+          s[g] = d;
+        }
       }
     }
+    // the token's score: the sum over its lanes
+    for (int o2 = 1; o2 < lpt; o2 <<= 1)
+#pragma unroll
+      for (int g = 0; g < G; ++g) s[g] += __shfl_xor_sync(kFull, s[g], o2);
     float pj[G], mx[G], l[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -718,7 +752,7 @@ __global__ void __launch_bounds__(kCascadeMergeWarps * 32) cascade_merge_kernel(
       for (int o2 = 16; o2 > 0; o2 >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o2));
       mx[g] = m;
       pj[g] = m > -INFINITY ? fast_exp2(sg - m) : 0.f;
-      float t = pj[g];
+      float t = part == 0 ? pj[g] : 0.f;          // each token once
 #pragma unroll
       for (int o2 = 16; o2 > 0; o2 >>= 1) t += __shfl_xor_sync(kFull, t, o2);
       l[g] = t;
@@ -740,7 +774,7 @@ __global__ void __launch_bounds__(kCascadeMergeWarps * 32) cascade_merge_kernel(
         }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float w = __shfl_sync(kFull, pj[g], j);   // 0 for an unreadable token
+          const float w = __shfl_sync(kFull, pj[g], j * lpt);   // 0 for an unreadable token
 #pragma unroll
           for (int k = 0; k < CPL; ++k) o[g][k] = fmaf(w, w != 0.f ? v[k] : 0.f, o[g][k]);
         }
