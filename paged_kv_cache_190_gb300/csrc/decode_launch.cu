@@ -143,8 +143,7 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(
 
 constexpr int kMergeWarps = 8;
 
-// Partials a sequence can have: its chunks, plus (shared-prefix decode) its
-// prefix pieces.
+// Partials a sequence can have: its chunks, plus (cascade) its prefix chunks.
 int64_t cascade_parts_per_seq(int max_context_len, int chunk_tokens, bool cascade) {
   if (max_context_len <= 0) return 0;
   const int64_t L = max_context_len;
