@@ -211,7 +211,7 @@ class GpuStep:
             t = t.view(self.torch.int16).view(self.torch.bfloat16)
         return t.to(self.device)
 
-    def _init_decode(self, case):
+    def _init_decode(self, case, finish=True):
         torch = self.torch
         self.fp8 = case.dtype == "fp8"            # e4m3 pools; q, new token, out bf16
         bf = case.dtype in ("bf16", "fp8")
@@ -236,7 +236,8 @@ class GpuStep:
                                 slots=case.slot_mapping, tables=case.block_tables,
                                 lens=case.context_lens)
         self.bf16 = bf
-        self._finish_init()
+        if finish:
+            self._finish_init()
 
     def _init_shared_prefix(self):
         """Shared-prefix step: the library's block manager forks each parent's
@@ -261,7 +262,7 @@ class GpuStep:
             block_size=s.block_size, num_blocks=s.num_blocks, scale=s.scale, context_lens=lens,
             block_tables=tables, slot_mapping=slots, k_cache=kc, v_cache=vc, k_new=s.k_new,
             v_new=s.v_new, q=s.q)
-        self._init_decode(case)
+        self._init_decode(case, finish=False)
         self.pairs = self._t(pairs)
         self.host_inputs["pairs"] = pairs
         elt = 2
@@ -281,12 +282,12 @@ class GpuStep:
             self.bytes["step"] += unique - self.bytes["kv"]
             self.bytes["kv"] = unique
             self.groups = len(shared)
-            self._finish_init()
+        self._finish_init()
 
     def _finish_init(self):
         torch, pa = self.torch, self.pa
         c = self.case
-        if getattr(self, "cascade", False) and hasattr(self, "groups"):
+        if self.cascade:
             self.ws_bytes = pa.pa_decode_cascade_workspace_size(
                 c.num_seqs, self.groups, c.num_q_heads, c.num_kv_heads, c.head_dim,
                 c.block_size, self.max_len, self.chunk_tokens)
@@ -304,7 +305,7 @@ class GpuStep:
         # the cascade adds the prefix kernel and always merges
         self.launches_per_step = (1 if self.pairs is not None else 0) + 3 + (
             1 if self.max_len > self.chunk else 0)
-        if getattr(self, "cascade", False):
+        if self.cascade:
             self.launches_per_step = (1 if self.pairs is not None else 0) + 5
 
     def write(self):
