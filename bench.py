@@ -65,6 +65,32 @@ def algorithmic_bytes(case) -> dict:
     return dict(kv=kv, decode=decode, write=write, step=decode + write)
 
 
+def unique_kv_bytes(case, group_start, shared_lens) -> int:
+    """K/V bytes a shared-prefix decode must read: each group's shared tokens
+    once, every sequence's own tokens once."""
+    kv_elt, _ = element_sizes(case)
+    sizes = np.diff(np.asarray(group_start, np.int64))
+    shared = np.asarray(shared_lens, np.int64)
+    own = int(case.context_lens.astype(np.int64).sum() - np.repeat(shared, sizes).sum())
+    return (int(shared.sum()) + own) * 2 * case.num_kv_heads * case.head_dim * kv_elt
+
+
+def shared_prefix_bytes(case, pairs, group_start=None, shared_lens=None) -> dict:
+    """algorithmic_bytes of the shared-prefix step: plus the copy-on-write page
+    copies; with groups (the cascade decode), K/V counted once per group."""
+    b = algorithmic_bytes(case)
+    kv_elt, _ = element_sizes(case)
+    b["copy"] = 2 * 2 * len(pairs) * case.num_kv_heads * case.block_size * case.head_dim * kv_elt
+    b["step"] += b["copy"]
+    if group_start is not None:
+        unique = unique_kv_bytes(case, group_start, shared_lens)
+        b["kv_logical"] = b["kv"]
+        b["decode"] += unique - b["kv"]
+        b["step"] += unique - b["kv"]
+        b["kv"] = unique
+    return b
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -265,23 +291,16 @@ class GpuStep:
         self._init_decode(case, finish=False)
         self.pairs = self._t(pairs)
         self.host_inputs["pairs"] = pairs
-        elt = 2
-        self.bytes["copy"] = 2 * 2 * len(pairs) * s.num_kv_heads * s.block_size * s.head_dim * elt
-        self.bytes["step"] += self.bytes["copy"]
         if self.cascade:
             # groups from the host tables (the library's grouping); the decode then
             # needs each family's shared pages once, each child's own tokens once
             starts, shared = pa.pa_cascade_groups(tables, lens, s.block_size)
             self.group_start, self.shared_lens = self._t(starts), self._t(shared)
             self.host_inputs["group_start"], self.host_inputs["shared_lens"] = starts, shared
-            sizes = np.diff(starts)
-            own = int(lens.astype(np.int64).sum() - (np.repeat(shared, sizes)).sum())
-            unique = (int(shared.astype(np.int64).sum()) + own) * 2 * s.num_kv_heads * s.head_dim * elt
-            self.bytes["kv_logical"] = self.bytes["kv"]
-            self.bytes["decode"] += unique - self.bytes["kv"]
-            self.bytes["step"] += unique - self.bytes["kv"]
-            self.bytes["kv"] = unique
+            self.bytes = shared_prefix_bytes(case, pairs, starts, shared)
             self.groups = len(shared)
+        else:
+            self.bytes = shared_prefix_bytes(case, pairs)
         self._finish_init()
 
     def _finish_init(self):
@@ -461,7 +480,8 @@ def run_gpu(args, world, rank, local):
         result["roofline"]["kernel"] = ("pa_decode_cascade call (plan + prefix kernel + "
                                         "paged_decode_kernel + merge), CUDA events")
     if not args.no_cpu_baseline and world == 1:
-        result["cpu_baseline"] = cpu_baseline(ws.case, budget_s=args.cpu_budget)
+        result["cpu_baseline"] = cpu_baseline(ws.case, budget_s=args.cpu_budget,
+                                              step_bytes=b["step"])
     return result
 
 
@@ -700,11 +720,12 @@ def _oracle_decode(case, kc, vc, rows=None):
                              case.num_kv_heads, case.dtype, rows=rows)
 
 
-def cpu_baseline(case, budget_s=15.0, kind="oracle"):
+def cpu_baseline(case, budget_s=15.0, kind="oracle", step_bytes=None):
     """The oracle, as it stands, on the host cores: whole decode steps of the
     workload (cache write + every (sequence, query head) row) repeated until
     about `budget_s` seconds have passed, or a random subset of rows when one
-    step alone would take longer."""
+    step alone would take longer.  The rate counts the GPU arm's algorithmic
+    bytes of a step (`step_bytes`), pro rata for a subset of rows."""
     import oracle
     kc, vc = case.k_cache.copy(), case.v_cache.copy()
     threads = oracle.max_threads()
@@ -715,7 +736,8 @@ def cpu_baseline(case, budget_s=15.0, kind="oracle"):
     t0 = time.perf_counter()
     _oracle_decode(case, kc, vc, rows=rows)
     per_row = (time.perf_counter() - t0) / 8
-    step_bytes = algorithmic_bytes(case)["step"]
+    if step_bytes is None:
+        step_bytes = algorithmic_bytes(case)["step"]
     if per_row * all_rows <= budget_s:
         steps, elapsed = 0, 0.0
         while steps == 0 or elapsed < budget_s:
@@ -727,10 +749,11 @@ def cpu_baseline(case, budget_s=15.0, kind="oracle"):
         nbytes, sample = steps * step_bytes, f"{steps} whole {case.name} steps"
     else:
         n = int(max(8, budget_s / max(per_row, 1e-9)))
-        rows, nbytes = _oracle_sample(case, n, rng)
+        rows, _ = _oracle_sample(case, n, rng)
         t0 = time.perf_counter()
         _oracle_decode(case, kc, vc, rows=rows)
         elapsed = time.perf_counter() - t0
+        nbytes = step_bytes * n / all_rows
         sample = f"{n} random (sequence, query head) rows of the {case.name} step"
     return {"value": round(nbytes / elapsed / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": kind, "sample": f"{sample}, fp64 gather-then-attend, {elapsed:.1f} s",
@@ -779,10 +802,25 @@ def run_reference(args, world, rank):
     oracle.build()
     if args.workload == "swap_gqa":
         return run_reference_swap(args, world)
+    pairs = None
     if args.workload in ("shared_prefix_bf16", "shared_prefix_cascade_bf16"):
-        case = pa_inputs.workload("gqa_bf16")
+        # the same step the GPU arm times, from the oracle's block manager; the
+        # oracle decodes every child over its whole context (sharing changes only
+        # where the bytes live), the rate counts the GPU arm's bytes
+        s = pa_inputs.shared_prefix_script()
+        case, pairs = pa_inputs.shared_prefix_step(
+            oracle.RefBlockManager(s.num_blocks, s.block_size, s.initial_free_order), s)
+        if args.workload == "shared_prefix_cascade_bf16":
+            C = s.children_per_parent
+            starts = np.arange(0, case.num_seqs + 1, C)
+            shared = (s.prefix_lens.astype(np.int64) // s.block_size) * s.block_size
+            step_bytes = shared_prefix_bytes(case, pairs, starts, shared)["step"]
+        else:
+            step_bytes = shared_prefix_bytes(case, pairs)["step"]
     else:
         case = pa_inputs.workload(args.workload)
+        step_bytes = algorithmic_bytes(case)["step"]
+    all_rows = case.num_seqs * case.q_len * case.num_q_heads
     kc, vc = case.k_cache.copy(), case.v_cache.copy()
     threads = oracle.max_threads()
     rng = np.random.default_rng(11)
@@ -795,21 +833,23 @@ def run_reference(args, world, rank):
     n_rows = int(max(1, min(4 * threads, 120.0 / max(total_steps, 1) / max(per_row, 1e-6))))
     samples = [_oracle_sample(case, n_rows, rng) for _ in range(args.steps + args.warmup)]
     elapsed, nbytes_total = 0.0, 0.0
-    for i, (rows, nbytes) in enumerate(samples):
+    for i, (rows, _) in enumerate(samples):
         t0 = time.perf_counter()
+        if pairs is not None:
+            oracle.copy_blocks(kc, vc, pairs)
         _oracle_write(case, kc, vc)
         _oracle_decode(case, kc, vc, rows=rows)
         dt = time.perf_counter() - t0
         if i >= args.warmup:
             elapsed += dt
-            nbytes_total += nbytes
+            nbytes_total += step_bytes * len(rows) / all_rows
     value = nbytes_total / elapsed / 1e9
     ms = elapsed / args.steps * 1e3
     return {"metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic (seeded pa_inputs)", "impl": "reference",
-            "config": {"workload": case.name, "num_seqs": case.num_seqs,
+            "config": {"workload": args.workload, "num_seqs": case.num_seqs,
                        "rows_per_step": n_rows},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                              "kind": "oracle",

@@ -383,6 +383,42 @@ def shared_prefix_prefill(manager, script: SharedPrefixScript):
     return prefix_slots
 
 
+def shared_prefix_step(manager, script: SharedPrefixScript):
+    """The timed step of the shared-prefix workload, on any block manager with
+    the oracle's method names: the prefill (parents fork their children and
+    leave), then one new token per child in id order (its slot; a copy pair when
+    it writes into a page it still shares).  Returns the DecodeCase (pools holding
+    the prefill, the step's tables and lengths, new tokens and q) and the int64
+    copy pairs [P, 2]."""
+    s = script
+    prefix_slots = shared_prefix_prefill(manager, s)
+    _, children = shared_prefix_ids(s)
+    kc = nan_fill((s.num_blocks, s.num_kv_heads, s.block_size, s.head_dim), s.dtype)
+    vc = nan_fill(kc.shape, s.dtype)
+    for p, sl in enumerate(prefix_slots):
+        place_at_slots(kc, sl, s.prefix_k[p], s.block_size)
+        place_at_slots(vc, sl, s.prefix_v[p], s.block_size)
+    slots, pairs = [], []
+    for c in children:
+        slot, src, dst = manager.append_slot(c)
+        slots.append(slot)
+        if src >= 0:
+            pairs.append((src, dst))
+    rows = [manager.block_table(c) for c in children]
+    mb = max(len(pages) for pages, _ in rows)
+    tables = np.full((len(children), mb), -1, np.int32)
+    for i, (pages, _) in enumerate(rows):
+        tables[i, :len(pages)] = pages
+    lens = np.asarray([length for _, length in rows], np.int32)
+    case = DecodeCase(name="shared_prefix_bf16", dtype=s.dtype, num_seqs=len(children),
+                      num_q_heads=s.num_q_heads, num_kv_heads=s.num_kv_heads, head_dim=s.head_dim,
+                      block_size=s.block_size, num_blocks=s.num_blocks, scale=s.scale,
+                      context_lens=lens, block_tables=tables,
+                      slot_mapping=np.asarray(slots, np.int64), k_cache=kc, v_cache=vc,
+                      k_new=s.k_new, v_new=s.v_new, q=s.q)
+    return case, np.asarray(pairs, np.int64).reshape(-1, 2)
+
+
 def shared_prefix_finish_order(script: SharedPrefixScript):
     """Step at which each child finishes (after its tail) and the order of the
     children finishing at the same step."""
