@@ -165,18 +165,24 @@ int pa_decode(void* out, const void* q, const void* k_cache, const void* v_cache
  *
  * Same arguments and result as pa_decode, minus the workspace: the scratch is a
  * static device array of PA_NOALLOC_SCRATCH_BYTES (96 MiB) inside the library,
- * allocated on every GPU that loads the library's device code and held until
- * the process exits.  The call allocates nothing (no cudaMalloc, no allocating
- * library routine).  Problems whose workspace (pa_decode_workspace_size with
- * the same arguments) exceeds PA_NOALLOC_SCRATCH_BYTES are rejected with
- * PA_ERR_WORKSPACE before anything is enqueued.
+ * held until the process exits on every GPU where it has been used.  The call
+ * itself allocates nothing (no cudaMalloc, no allocating library routine).
+ * Problems whose workspace (pa_decode_workspace_size with the same arguments)
+ * exceeds PA_NOALLOC_SCRATCH_BYTES are rejected with PA_ERR_WORKSPACE before
+ * anything is enqueued.
  *
- * The first call on a device looks the array's device address up
- * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture.  All calls share the one array: calls
- * that may overlap on the GPU (different streams, or host threads enqueueing
- * concurrently) race on it and must be serialised by the caller.  Each call
- * resets what must start at zero, so the previous call's contents do no harm.
+ * Set-up: the first call in a CUDA context looks the array's device address
+ * up (cudaGetSymbolAddress, with the caller's device and context current) and
+ * caches it under the context's unique id, so a non-primary context, or a
+ * primary context created again after cudaDeviceReset, gets its own lookup.
+ * Under CUDA's default lazy module loading that first lookup is also when the
+ * driver loads this part of the library onto the device and reserves the
+ * 96 MiB: make the first call at set-up time, before any stream capture and
+ * before a fixed memory pool takes the device's free memory.  All calls share
+ * the one array: calls that may overlap on the GPU (different streams, or host
+ * threads enqueueing concurrently) race on it and must be serialised by the
+ * caller.  Each call resets what must start at zero, so the previous call's
+ * contents do no harm.
  */
 #define PA_NOALLOC_SCRATCH_BYTES ((size_t)96 << 20)
 int pa_decode_noalloc(void* out, const void* q, const void* k_cache, const void* v_cache,

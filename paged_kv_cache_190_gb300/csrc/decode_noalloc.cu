@@ -5,15 +5,23 @@
 // steps).  Instead of a caller-provided workspace, it uses a fixed-size
 // scratch array that is part of this library's device code.
 //
-// The array is a file-scope __device__ variable: it is allocated when the
-// library's device code is loaded on a GPU and held until the process exits.
-// In host code `g_decode_scratch` is only a host-side stand-in for the symbol,
-// not a device address, so the device address is looked up once per device
-// with cudaGetSymbolAddress (with that device current) and cached.
+// The array is a file-scope __device__ variable.  Under CUDA's default lazy
+// module loading it is reserved on a device when its address is first looked
+// up there (the first call in that CUDA context), and held until the process
+// exits.  In host code `g_decode_scratch` is only a host-side stand-in for the
+// symbol, not a device address, so the device address is looked up with
+// cudaGetSymbolAddress, with the caller's device and context current, and
+// cached.  The cache is keyed by the context's unique id (cuCtxGetId), not by
+// the device ordinal: a symbol's address belongs to a context, so a caller in
+// a non-primary context, or a primary context created again after
+// cudaDeviceReset, gets a lookup of its own rather than another context's
+// address.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
-#include <atomic>
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/pa.h"
 
@@ -22,19 +30,73 @@ namespace {
 constexpr size_t kScratchBytes = PA_NOALLOC_SCRATCH_BYTES;
 __device__ __align__(256) unsigned char g_decode_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_address[kMaxDevices];
+// Driver calls through the runtime's entry-point query (no libcuda link).
+struct CtxCalls {
+  PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+  PFN_cuCtxGetId_v12000 get_id = nullptr;
+};
 
-// Device address of g_decode_scratch on the current device.
+const CtxCalls& ctx_calls() {
+  static const CtxCalls calls = [] {
+    CtxCalls c;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      c.get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    p = nullptr;
+    q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      c.get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    return c;
+  }();
+  return calls;
+}
+
+// Unique id of the current context (0 when there is none yet).
+int current_context_id(unsigned long long* id) {
+  const CtxCalls& c = ctx_calls();
+  if (!c.get_current || !c.get_id) return PA_ERR_CUDA;
+  CUcontext ctx = nullptr;
+  if (c.get_current(&ctx) != CUDA_SUCCESS) return PA_ERR_CUDA;
+  *id = 0;
+  if (ctx != nullptr && c.get_id(ctx, id) != CUDA_SUCCESS) return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+constexpr int kCacheEntries = 16;
+struct Entry {
+  unsigned long long context_id;
+  void* address;
+};
+std::mutex g_cache_lock;
+Entry g_cache[kCacheEntries];
+int g_cache_used = 0;
+
+// Device address of g_decode_scratch in the current context.
 int scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
-  void* p = g_scratch_address[dev].load(std::memory_order_acquire);
-  if (p == nullptr) {
-    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr)
-      return PA_ERR_CUDA;
-    g_scratch_address[dev].store(p, std::memory_order_release);
+  unsigned long long id = 0;
+  int rc = current_context_id(&id);
+  if (rc != PA_OK) return rc;
+  if (id != 0) {
+    std::lock_guard<std::mutex> g(g_cache_lock);
+    for (int i = 0; i < g_cache_used; ++i)
+      if (g_cache[i].context_id == id) {
+        *out = g_cache[i].address;
+        return PA_OK;
+      }
+  }
+  // First call in this context: the lookup loads this file's module on the
+  // device (reserving the array) and, when no context was current yet, makes
+  // the runtime's primary context current.
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || p == nullptr)
+    return PA_ERR_CUDA;
+  if (id == 0 && (rc = current_context_id(&id)) != PA_OK) return rc;
+  {
+    std::lock_guard<std::mutex> g(g_cache_lock);
+    if (id != 0 && g_cache_used < kCacheEntries) g_cache[g_cache_used++] = Entry{id, p};
   }
   *out = p;
   return PA_OK;

@@ -148,7 +148,7 @@ def test_unknown_and_duplicate_ids():
         bm.free(3)
 
 
-def _run_script(bm, script):
+def _run_script(bm, script, after_step=None):
     prefix_slots = pa_inputs.shared_prefix_prefill(bm, script)
     _, children = pa_inputs.shared_prefix_ids(script)
     trace = [[s.tolist() for s in prefix_slots]]
@@ -158,6 +158,8 @@ def _run_script(bm, script):
         slots = [r[0] for r in res]
         pairs = [(r[1], r[2]) for r in res if r[1] >= 0]
     trace.append((list(map(int, slots)), [tuple(map(int, p)) for p in pairs]))
+    if after_step is not None:
+        after_step(bm, children)
     # finish: every child generates its tail, then leaves in the scripted order
     remaining = {c: int(script.tails[c]) for c in children}
     step = 0
@@ -189,6 +191,47 @@ def test_shared_prefix_script_matches_oracle_and_returns_every_page():
     assert prod.num_free() == script.num_blocks
     assert sorted(prod.free_list()) == list(range(script.num_blocks))
     assert all(prod.refcount(p) == 0 for p in range(script.num_blocks))
+
+
+def test_shared_prefix_script_full_size():
+    """The shared-prefix workload at its stated size: 8 parents of 2048 + g_p
+    tokens fork 16 children each, every child writes one token (copy-on-write of
+    its family's partial page), then generates its tail of U{0..512} tokens and
+    leaves in the scripted random order.  Library and oracle managers agree on
+    every slot and copy; right after the step the reference counts are what the
+    sharing implies; at the end every page is back on the free list."""
+    script = pa_inputs.shared_prefix_script()
+    P, C, bs = script.num_parents, script.children_per_parent, script.block_size
+    assert (P, C) == (8, 16) and all(2049 <= n <= 2063 for n in script.prefix_lens)
+
+    def after_step(bm, children):
+        rc = (lambda p: bm.refcount[p]) if isinstance(bm.refcount, list) else bm.refcount
+        for p in range(P):
+            fam = children[p * C:(p + 1) * C]
+            tables = [bm.block_table(c)[0] for c in fam]
+            full = int(script.prefix_lens[p]) // bs
+            shared = tables[-1][:full]
+            for t in tables:                       # the full prompt pages stay shared by all
+                assert t[:full] == shared
+            assert all(rc(page) == C for page in shared)
+            # the partial page: C - 1 children copied it, the last wrote in place
+            last = [t[full] for t in tables]
+            assert len(set(last)) == C and all(rc(page) == 1 for page in last)
+        used = sum(1 for page in range(script.num_blocks) if rc(page) > 0)
+        assert used + bm.num_free() == script.num_blocks
+
+    prod = pa.BlockManager(script.num_blocks, bs, script.initial_free_order)
+    ref = oracle.RefBlockManager(script.num_blocks, bs, script.initial_free_order)
+    t_prod = _run_script(prod, script, after_step)
+    t_ref = _run_script(ref, script, after_step)
+    assert t_prod == t_ref
+    assert len(t_prod[1][1]) == P * (C - 1)
+    assert len(t_prod) - 2 == int(script.tails.max())          # one trace entry per later step
+    for bm in (prod, ref):
+        assert bm.num_free() == script.num_blocks
+        assert sorted(bm.free_list()) == list(range(script.num_blocks))
+    assert all(prod.refcount(p) == 0 for p in range(script.num_blocks))
+    assert all(r == 0 for r in ref.refcount)
 
 
 @pytest.mark.parametrize("seed", range(16))

@@ -90,22 +90,16 @@ def test_decode_fp8_workloads_at_oracle_size(name, B, over):
 
 
 @pytest.mark.parametrize("name", ["mha_fp8", "gqa_fp8", "long128k_fp8"])
-def test_decode_fp8_full_size_sampled_rows(name):
-    """Full-size fp8 workload in the bench's launch configuration, checked on
-    sampled rows the oracle computes one by one."""
+def test_decode_fp8_full_size_every_row(name):
+    """Full-size fp8 workload in the bench's launch configuration, every output
+    row against the oracle (the mean-error bar on the whole output)."""
     case = pa_inputs.workload(name)
     dc = DeviceCase(case)
     got = out_as_f64(dc.step())
     assert dc.device_errors() == 0
-    assert np.all(np.isfinite(got))
-    rng = np.random.default_rng(78)
-    rows = [(int(rng.integers(case.num_seqs)), int(rng.integers(case.num_q_heads)))
-            for _ in range(24)]
-    rows.append((int(np.argmax(case.context_lens)), 0))
-    rows.append((int(np.argmin(case.context_lens)), case.num_q_heads - 1))
-    want = oracle_step(case, rows=rows)
-    sel = np.stack([got[b, i] for b, i in rows])
-    check_tolerance(sel, want, case.dtype, case.name)
+    want = oracle_step(case)
+    assert got.shape == want.shape
+    check_tolerance(got, want, case.dtype, case.name)
 
 
 @pytest.mark.parametrize("G", [1, 2, 4, 8])

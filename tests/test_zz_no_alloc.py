@@ -1,8 +1,10 @@
 """The allocation-free decode entry point, for callers that cannot allocate
 device memory (code inside a runtime that owns every device allocation, or a
-decode loop that must not allocate between steps): through the C ABI it must
-give the same output as pa_decode with a caller workspace, call after call,
-and refuse problems bigger than its static scratch before enqueueing anything.
+decode loop that must not allocate between steps).  Through the C ABI it must
+match the oracle within the decode tolerance and give bit for bit the output of
+pa_decode with a caller workspace, call after call; it must not allocate on the
+device once set up; and it must refuse problems bigger than its static scratch
+before enqueueing anything.
 
 Kept in a file that runs last so a failure here cannot hide any other test.
 """
@@ -12,7 +14,7 @@ import torch
 
 import pa_inputs
 import paged_kv_cache_190_gb300 as pa
-from gpu_helpers import DEV, DeviceCase, check_tolerance, out_as_f64
+from gpu_helpers import DEV, DeviceCase, check_tolerance, oracle_step, out_as_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -23,18 +25,36 @@ def _noalloc(dc, out):
                          c.num_kv_heads, c.max_context_len, device_errors=dc.errs)
 
 
-def test_noalloc_matches_pa_decode_on_two_calls_in_a_row():
-    # several chunks per sequence, so the split partials and the merge use the scratch
-    case = pa_inputs.scaled_workload("gqa_bf16", 16)
+CASES = [
+    # several chunks per sequence of the GQA workload's length mix
+    ("gqa_bf16", 16, {}),
+    # the long-context workload cut to 20 000 tokens: a dozen chunks per
+    # sequence and a ragged tail, so the split partials and the merge use the scratch
+    ("long128k_bf16", 2, dict(lens=("fixed", 20000))),
+]
+
+
+@pytest.mark.parametrize("name,B,over", CASES)
+def test_noalloc_matches_oracle_and_pa_decode_on_two_calls_in_a_row(name, B, over):
+    case = pa_inputs.scaled_workload(name, B, **over)
     dc = DeviceCase(case)
-    want = out_as_f64(dc.step())                 # cache write + pa_decode with its own workspace
-    for _ in range(2):
-        out = torch.full(dc.q.shape, float("nan"), dtype=dc.tdt, device=DEV)
+    ref = dc.step()                          # cache write + pa_decode with its own workspace
+    want = oracle_step(case)
+    outs = [torch.full(dc.q.shape, float("nan"), dtype=dc.tdt, device=DEV) for _ in range(3)]
+    _noalloc(dc, outs[0])                    # set-up call (looks the scratch address up)
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    alloc_before = torch.cuda.memory_allocated()
+    for out in outs[1:]:                     # two more calls in a row
         _noalloc(dc, out)
-        torch.cuda.synchronize()
-        got = out_as_f64(out)
-        check_tolerance(got, want, case.dtype, "pa_decode_noalloc vs pa_decode")
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] == free_before, "device memory changed across calls"
+    assert torch.cuda.memory_allocated() == alloc_before
     assert dc.device_errors() == 0
+    for k, out in enumerate(outs):
+        check_tolerance(out_as_f64(out), want, case.dtype, f"{case.name} call {k}")
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16)), \
+            f"{case.name} call {k}: differs from pa_decode"
 
 
 def test_noalloc_after_a_different_problem():
@@ -42,12 +62,14 @@ def test_noalloc_after_a_different_problem():
     # shape must not be affected by them
     small = DeviceCase(pa_inputs.workload("tiny_fp32"))
     big = DeviceCase(pa_inputs.scaled_workload("mha_bf16", 4))
-    want_small = out_as_f64(small.step())
-    want_big = out_as_f64(big.step())
-    for dc, want in ((big, want_big), (small, want_small), (big, want_big)):
+    ref_small, ref_big = small.step(), big.step()
+    want_small, want_big = oracle_step(small.case), oracle_step(big.case)
+    for dc, ref, want in ((big, ref_big, want_big), (small, ref_small, want_small),
+                          (big, ref_big, want_big)):
         out = torch.empty(dc.q.shape, dtype=dc.tdt, device=DEV)
         _noalloc(dc, out)
         check_tolerance(out_as_f64(out), want, dc.case.dtype, dc.case.name)
+        assert torch.equal(out, ref)
     assert small.device_errors() == 0 and big.device_errors() == 0
 
 
