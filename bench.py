@@ -221,13 +221,16 @@ def dist_env():
 class GpuStep:
     """Device-resident inputs of one workload and the step that runs on them."""
 
-    def __init__(self, name: str, device, torch, pa, chunk_tokens: int = 0):
+    def __init__(self, name: str, device, torch, pa, chunk_tokens: int = 0, num_seqs: int = 0):
         self.torch, self.pa, self.device = torch, pa, device
         self.chunk_tokens = chunk_tokens
         self.name = name
+        self.reduced = bool(num_seqs)
         self.cascade = name == "shared_prefix_cascade_bf16"
         if name in ("shared_prefix_bf16", "shared_prefix_cascade_bf16"):
-            self._init_shared_prefix()
+            self._init_shared_prefix(num_seqs)
+        elif num_seqs:
+            self._init_decode(pa_inputs.scaled_workload(name, num_seqs))
         else:
             self._init_decode(pa_inputs.workload(name))
 
@@ -265,12 +268,12 @@ class GpuStep:
         if finish:
             self._finish_init()
 
-    def _init_shared_prefix(self):
+    def _init_shared_prefix(self, num_parents=0):
         """Shared-prefix step: the library's block manager forks each parent's
         pages to its children; the step copies the partial shared page for all
         but the last child of each family, writes the new tokens, decodes."""
         pa = self.pa
-        s = pa_inputs.shared_prefix_script()
+        s = pa_inputs.shared_prefix_script(scale_parents=num_parents or None)
         bm = pa.BlockManager(s.num_blocks, s.block_size, s.initial_free_order)
         prefix_slots = pa_inputs.shared_prefix_prefill(bm, s)
         _, children = pa_inputs.shared_prefix_ids(s)
@@ -327,71 +330,92 @@ class GpuStep:
         if self.cascade:
             self.launches_per_step = (1 if self.pairs is not None else 0) + 5
 
-    def write(self):
-        pa = self.pa
+    def write(self, prepare=False):
+        """Enqueue the step's page copies and cache write; with ``prepare`` return
+        them as prepared C-ABI calls instead."""
+        pa, calls = self.pa, []
         if self.pairs is not None:
-            pa.pa_copy_blocks(self.k_cache, self.v_cache, self.pairs, device_errors=self.errs)
+            calls.append(pa.pa_copy_blocks(self.k_cache, self.v_cache, self.pairs,
+                                           device_errors=self.errs, prepare=prepare))
         if self.fp8:
-            pa.pa_reshape_and_cache_fp8(self.k_new, self.v_new, self.k_cache, self.v_cache,
-                                        self.slots, self.k_scale, self.v_scale,
-                                        device_errors=self.errs)
-            return
-        pa.pa_reshape_and_cache(self.k_new, self.v_new, self.k_cache, self.v_cache, self.slots,
-                                device_errors=self.errs)
+            calls.append(pa.pa_reshape_and_cache_fp8(self.k_new, self.v_new, self.k_cache,
+                                                     self.v_cache, self.slots, self.k_scale,
+                                                     self.v_scale, device_errors=self.errs,
+                                                     prepare=prepare))
+        else:
+            calls.append(pa.pa_reshape_and_cache(self.k_new, self.v_new, self.k_cache,
+                                                 self.v_cache, self.slots, device_errors=self.errs,
+                                                 prepare=prepare))
+        return calls
 
-    def decode(self):
+    def decode(self, prepare=False):
+        """Enqueue the step's decode call (or return it prepared)."""
+        pa = self.pa
+        common = dict(workspace=self.workspace, chunk_tokens=self.chunk_tokens,
+                      device_errors=self.errs, prepare=prepare)
         if self.cascade:
-            self.pa.pa_decode_cascade(self.out, self.q, self.k_cache, self.v_cache, self.tables,
-                                      self.lens, self.group_start, self.shared_lens, self.scale,
-                                      self.Hkv, self.max_len, workspace=self.workspace,
-                                      chunk_tokens=self.chunk_tokens, device_errors=self.errs)
-            return
+            return [pa.pa_decode_cascade(self.out, self.q, self.k_cache, self.v_cache, self.tables,
+                                         self.lens, self.group_start, self.shared_lens,
+                                         self.scale, self.Hkv, self.max_len, **common)]
         if self.case.q_len > 1:
-            self.pa.pa_decode_multi(self.out, self.q, self.k_cache, self.v_cache, self.tables,
-                                    self.lens, self.scale, self.Hkv, self.max_len,
-                                    workspace=self.workspace, chunk_tokens=self.chunk_tokens,
-                                    device_errors=self.errs)
-            return
+            return [pa.pa_decode_multi(self.out, self.q, self.k_cache, self.v_cache, self.tables,
+                                       self.lens, self.scale, self.Hkv, self.max_len, **common)]
         if self.fp8:
-            self.pa.pa_decode_fp8(self.out, self.q, self.k_cache, self.v_cache, self.tables,
-                                  self.lens, self.scale, self.k_scale, self.v_scale, self.Hkv,
-                                  self.max_len, workspace=self.workspace,
-                                  chunk_tokens=self.chunk_tokens, device_errors=self.errs)
-            return
-        self.pa.pa_decode(self.out, self.q, self.k_cache, self.v_cache, self.tables, self.lens,
-                          self.scale, self.Hkv, self.max_len, workspace=self.workspace,
-                          chunk_tokens=self.chunk_tokens, device_errors=self.errs)
+            return [pa.pa_decode_fp8(self.out, self.q, self.k_cache, self.v_cache, self.tables,
+                                     self.lens, self.scale, self.k_scale, self.v_scale, self.Hkv,
+                                     self.max_len, **common)]
+        return [pa.pa_decode(self.out, self.q, self.k_cache, self.v_cache, self.tables, self.lens,
+                             self.scale, self.Hkv, self.max_len, **common)]
+
+    def dtype_text(self):
+        if self.fp8:
+            return ("e4m3 K/V codes (e4m3 tensor-core products, q and P split into e4m3 hi + lo, "
+                    "fp32 accumulate), bf16 q/out")
+        return "bf16" if self.bf16 else "f32"
+
+    def unique_kv_bytes(self):
+        """K/V bytes of the distinct physical pages the step's tables touch."""
+        c = self.case
+        pages = set()
+        for b in range(c.num_seqs):
+            n = (int(c.context_lens[b]) + c.block_size - 1) // c.block_size
+            pages.update(c.block_tables[b, :n].tolist())
+        kv_elt, _ = element_sizes(c)
+        return len(pages) * 2 * c.num_kv_heads * c.block_size * c.head_dim * kv_elt
+
+    def cascade_summary(self, dec_ms):
+        b = self.bytes
+        return {"unique_kv_bytes": b["kv"], "logical_kv_bytes": b["kv_logical"],
+                "logical_decode_gbs": round((b["decode"] - b["kv"] + b["kv_logical"])
+                                            / (dec_ms * 1e-3) / 1e9, 1)}
 
     def step(self):
         self.write()
         self.decode()
 
+    def prepared_step(self):
+        """The whole step as prepared C-ABI calls, in order."""
+        return self.write(prepare=True) + self.decode(prepare=True)
 
-def run_gpu(args, world, rank, local):
-    import torch
-    import paged_kv_cache_190_gb300 as pa
-    pa.library()
-    device = torch.device(f"cuda:{local}")
-    torch.cuda.set_device(device)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=device)
-    ws = GpuStep(args.workload, device, torch, pa, args.chunk_tokens)
-    stream = torch.cuda.current_stream(device)
 
-    def barrier():
-        if world > 1:
-            torch.distributed.barrier()
+# Measured after the headline workload in a default single-GPU run, each with its
+# own timing, roofline and clocks: the GQA batch and the 128K-context decode,
+# the shared-prefix step (with pa_decode, and with the shared-prefix decode), and
+# the float8 pools.
+EXTRA_WORKLOADS = ("gqa_bf16", "long128k_bf16", "shared_prefix_bf16",
+                   "shared_prefix_cascade_bf16", "mha_fp8", "gqa_fp8", "long128k_fp8")
 
-    # warm-up
-    for _ in range(args.warmup):
+
+def time_steps(ws, K, warmup, torch, pa, device, stream, barrier):
+    """W untimed steps, then K steps timed with CUDA events on the launching
+    stream (around the whole region and around each step's write and decode),
+    clocks sampled meanwhile."""
+    for _ in range(warmup):
         ws.step()
     torch.cuda.synchronize(device)
     flags = pa.pa_read_device_errors(ws.errs)
     if flags:
-        raise RuntimeError(f"device error bits {flags} during warm-up")
-
-    K = args.steps
+        raise RuntimeError(f"{ws.name}: device error bits {flags} during warm-up")
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     barrier()
     torch.cuda.synchronize(device)
@@ -411,25 +435,106 @@ def run_gpu(args, world, rank, local):
         if K * 0.5e-3 < 0.3:
             time.sleep(0.3)
     barrier()
-    total_ms = t_start.elapsed_time(t_end)
-    decode_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
-    write_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    ms_per_step = max_over_ranks(total_ms / K, device, world)
     flags = pa.pa_read_device_errors(ws.errs)
     if flags:
-        raise RuntimeError(f"device error bits {flags} during the timed steps")
+        raise RuntimeError(f"{ws.name}: device error bits {flags} during the timed steps")
+    return {"total_ms": t_start.elapsed_time(t_end),
+            "decode_ms": [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)],
+            "write_ms": [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)],
+            "clocks": clocks.summary()}
 
-    # end to end through the public API with host buffers
-    e2e = run_e2e(ws, args, torch, pa, device, stream, barrier, world)
 
+def roofline(ws, dec_avg_ms, peak, peak_src):
+    b = ws.bytes
+    achieved = b["decode"] / (dec_avg_ms * 1e-3) / 1e9
+    kernel = ("pa_decode_cascade call (plan + prefix kernel + paged_decode_kernel + merge)"
+              if ws.cascade else "pa_decode call (plan + paged_decode_kernel + merge)")
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": None if ws.reduced else ncu_traffic(ws.name),
+            "kernel": kernel + ", CUDA events", "algorithmic_bytes_per_launch": b["decode"],
+            "avg_launch_us": round(dec_avg_ms * 1e3, 2),
+            "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json hbm_gbs' if peak_src == 'measured' else 'profiling recipe fallback 6.8 TB/s'})"}
+
+
+def l2_note(ws):
+    kv = ws.bytes["kv"]
+    if kv > 1e9:
+        return "no flush: the step reads %.2f GB of K/V, far above the 129 MB L2" % (kv / 1e9)
+    return ("no flush: the step's %.0f MB of distinct K/V pages can sit in the 129 MB L2, so its "
+            "GB/s is not a DRAM rate" % (ws.unique_kv_bytes() / 1e6))
+
+
+def workload_entry(ws, m, e2e, world, peak, peak_src):
+    """Summary of one extra workload for the JSON line."""
+    K = len(m["decode_ms"])
+    ms_per_step = m["total_ms"] / K
+    dec_ms = statistics.mean(m["decode_ms"])
+    c = ws.case
+    entry = {
+        "value": round(whole_job_gbs(ws.bytes["step"], world, ms_per_step * 1e-3), 2),
+        "unit": "GB/s", "steps": K, "us_per_step": round(ms_per_step * 1e3, 2),
+        "steps_per_s": round(1e3 / ms_per_step, 1),
+        "dtype": ws.dtype_text(),
+        "config": {"num_seqs": c.num_seqs, "num_q_heads": c.num_q_heads,
+                   "num_kv_heads": c.num_kv_heads, "head_dim": c.head_dim,
+                   "block_size": c.block_size, "mean_context": float(c.context_lens.mean()),
+                   "max_context": ws.max_len, "chunk_tokens": ws.chunk, "l2": l2_note(ws),
+                   "algorithmic_bytes_per_step": ws.bytes["step"]},
+        "roofline": roofline(ws, dec_ms, peak, peak_src),
+        "write_avg_us": round(statistics.mean(m["write_ms"]) * 1e3, 2),
+        "e2e": e2e, "gpu_launches": ws.launches_per_step * K, "clocks": m["clocks"],
+    }
+    if ws.cascade:
+        entry["config"]["groups"] = ws.groups
+        entry["cascade"] = ws.cascade_summary(dec_ms)
+    return entry
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+    import paged_kv_cache_190_gb300 as pa
+    pa.library()
+    device = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    ws = GpuStep(args.workload, device, torch, pa, args.chunk_tokens, args.num_seqs)
+    stream = torch.cuda.current_stream(device)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    K = args.steps
+    m = time_steps(ws, K, args.warmup, torch, pa, device, stream, barrier)
+    ms_per_step = max_over_ranks(m["total_ms"] / K, device, world)
+
+    # end to end through the C ABI with host buffers
+    e2e = run_e2e(ws, K, args.warmup, torch, device, stream, barrier, world)
+
+    peak, peak_src = hbm_peak()
+    extras = {}
+    if world == 1 and args.extra_workloads and not args.num_seqs:
+        # the other configurations the target is stated on, measured the same way
+        names = [w for w in args.extra_workloads.split(",") if w and w != args.workload]
+        host_ms = {}
+        for name in names:
+            t0 = time.perf_counter()
+            xs = GpuStep(name, device, torch, pa, 0)
+            xK, xW = max(K, args.extra_steps), max(args.warmup, 5)
+            xm = time_steps(xs, xK, xW, torch, pa, device, stream, barrier)
+            xe = run_e2e(xs, xK, xW, torch, device, stream, barrier, world)
+            extras[name] = workload_entry(xs, xm, xe, world, peak, peak_src)
+            host_ms[name] = round((time.perf_counter() - t0) * 1e3, 1)
+            del xs
+            torch.cuda.empty_cache()
     if rank != 0:
         return None
-    peak, peak_src = hbm_peak()
     b = ws.bytes
     value = whole_job_gbs(b["step"], world, ms_per_step * 1e-3)
-    dec_avg_ms = statistics.mean(decode_ms)
-    achieved = b["decode"] / (dec_avg_ms * 1e-3) / 1e9
-    traffic = ncu_traffic(args.workload)
+    dec_avg_ms = statistics.mean(m["decode_ms"])
     result = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
@@ -437,33 +542,26 @@ def run_gpu(args, world, rank, local):
         "steps_per_s": round(world * 1e3 / ms_per_step, 1),
         "hbm_frac_step": round(value / world / peak, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": ("e4m3 K/V (f16 MMA, fp32 accumulate), bf16 q/out" if ws.fp8
-                  else "bf16" if ws.bf16 else "f32"), "data": "synthetic (seeded pa_inputs; no dataset or weights)",
+        "dtype": ws.dtype_text(), "data": "synthetic (seeded pa_inputs; no dataset or weights)",
         "config": {
-            "workload": args.workload, "num_seqs": ws.case.num_seqs,
+            "workload": args.workload + (f"[reduced: {args.num_seqs}]" if args.num_seqs else ""),
+            "num_seqs": ws.case.num_seqs,
             "num_q_heads": ws.case.num_q_heads, "num_kv_heads": ws.case.num_kv_heads,
             "head_dim": ws.case.head_dim, "block_size": ws.case.block_size,
             "num_blocks": ws.case.num_blocks, "mean_context": float(ws.case.context_lens.mean()),
             "max_context": ws.max_len, "chunk_tokens": ws.chunk,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "l2": "no flush: the step reads %.2f GB of K/V, far above the 129 MB L2"
-                  % (b["kv"] / 1e9) if b["kv"] > 1e9 else "working set may sit in L2",
+            "l2": l2_note(ws),
             "step": ("copy_blocks + " if ws.pairs is not None else "")
             + "reshape_and_cache + decode (plan, persistent decode, split-K merge)",
             "algorithmic_bytes_per_step": b["step"],
         },
-        "roofline": {
-            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": traffic,
-            "kernel": "pa_decode call (plan + paged_decode_kernel + merge), CUDA events",
-            "algorithmic_bytes_per_launch": b["decode"], "avg_launch_us": round(dec_avg_ms * 1e3, 2),
-            "peak_source": f"{peak_src} ({'MEASURED_PEAKS.json hbm' if peak_src == 'measured' else 'profiling recipe fallback 6.8 TB/s'})",
-        },
-        "write_avg_us": round(statistics.mean(write_ms) * 1e3, 2),
+        "roofline": roofline(ws, dec_avg_ms, peak, peak_src),
+        "write_avg_us": round(statistics.mean(m["write_ms"]) * 1e3, 2),
         "host_block_manager": host_block_manager_time(ws.case, pa),
         "e2e": e2e,
         "gpu_launches": ws.launches_per_step * K,
-        "clocks": clocks.summary(),
+        "clocks": m["clocks"],
     }
     if ws.cascade:
         # algorithmic bytes above count each family's shared pages once; the same
@@ -473,12 +571,14 @@ def run_gpu(args, world, rank, local):
                                     "shared-prefix kernel, persistent decode over each "
                                     "sequence's own pages, merge)")
         result["config"]["groups"] = ws.groups
-        result["cascade"] = {
-            "unique_kv_bytes": b["kv"], "logical_kv_bytes": b["kv_logical"],
-            "logical_decode_gbs": round((b["decode"] - b["kv"] + b["kv_logical"])
-                                        / (dec_avg_ms * 1e-3) / 1e9, 1)}
-        result["roofline"]["kernel"] = ("pa_decode_cascade call (plan + prefix kernel + "
-                                        "paged_decode_kernel + merge), CUDA events")
+        result["cascade"] = ws.cascade_summary(dec_avg_ms)
+    if extras:
+        result["workloads"] = extras
+        result["workloads_note"] = (
+            "each measured after the headline in the same process: its own warm-up, "
+            f"max(steps, {args.extra_steps}) timed steps, CUDA-event decode time, roofline "
+            "against the same peak, clocks and e2e; host seconds to build each: "
+            + ", ".join(f"{k} {v / 1e3:.1f}" for k, v in host_ms.items()))
     if not args.no_cpu_baseline and world == 1:
         result["cpu_baseline"] = cpu_baseline(ws.case, budget_s=args.cpu_budget,
                                               step_bytes=b["step"])
@@ -636,37 +736,40 @@ def host_block_manager_time(case, pa, repeats: int = 100):
             "num_seqs": B, "note": "host C++ block manager via ctypes; outside the device timing"}
 
 
-def run_e2e(ws, args, torch, pa, device, stream, barrier, world):
-    """Every step: pinned host inputs copied to the device, the step through the
-    C ABI, the output copied back to pinned host memory, stream synchronised."""
-    def pinned(a):
-        a = np.ascontiguousarray(a)
-        if a.dtype == np.uint16:
-            a = a.view(np.int16)
-        return torch.from_numpy(a).pin_memory()
-
-    host = {k: pinned(v) for k, v in ws.host_inputs.items()}
-    dev = dict(q=ws.q, k_new=ws.k_new, v_new=ws.v_new, slots=ws.slots, tables=ws.tables,
-               lens=ws.lens)
-    if "pairs" in host:
-        dev["pairs"] = ws.pairs
-    if "group_start" in host:
-        dev["group_start"], dev["shared_lens"] = ws.group_start, ws.shared_lens
+def run_e2e(ws, steps, warmup, torch, device, stream, barrier, world):
+    """End to end through the C ABI with host buffers.  The step's inputs (q,
+    new k/v, slots, tables, lengths, and the copy pairs or groups where the
+    workload has them) sit packed in one pinned host buffer; every step copies
+    it into one device buffer whose views are the step's device inputs, runs the
+    step's C-ABI calls (prepared once: the same pointers every step), copies the
+    output back into pinned host memory and synchronises the stream."""
+    spans, off = {}, 0
+    for name, a in ws.host_inputs.items():
+        nbytes = np.ascontiguousarray(a).nbytes
+        spans[name] = (off, nbytes)
+        off += (nbytes + 255) // 256 * 256
+    host = torch.empty(off, dtype=torch.uint8).pin_memory()
+    dev = torch.empty(off, dtype=torch.uint8, device=device)
+    host_np = host.numpy()
+    for name, a in ws.host_inputs.items():
+        o, nbytes = spans[name]
+        host_np[o:o + nbytes] = np.ascontiguousarray(a).view(np.uint8).reshape(-1)
+        old = getattr(ws, name)                       # rebind the input as a view of `dev`
+        setattr(ws, name, dev[o:o + nbytes].view(old.dtype).view(old.shape))
+    calls = ws.prepared_step()
     out_host = torch.empty(ws.out.shape, dtype=ws.out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_host.numel() * out_host.element_size()
 
     def one():
-        for k, h in host.items():
-            d = dev[k]
-            d.view(torch.uint8).view(-1).copy_(h.view(torch.uint8).view(-1), non_blocking=True)
-        ws.step()
+        dev.copy_(host, non_blocking=True)
+        for call in calls:
+            call()
         out_host.copy_(ws.out, non_blocking=True)
         stream.synchronize()
 
-    for _ in range(max(3, args.warmup // 4)):
+    for _ in range(max(3, warmup // 4)):
         one()
-    n = max(10, min(args.steps, 500))
+    n = max(10, min(steps, 500))
     barrier()
     t0 = time.perf_counter()
     for _ in range(n):
@@ -675,8 +778,9 @@ def run_e2e(ws, args, torch, pa, device, stream, barrier, world):
     barrier()
     sec = max_over_ranks((t1 - t0) / n, device, world)
     return {"value": round(whole_job_gbs(ws.bytes["step"], world, sec), 2), "unit": "GB/s",
-            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "us_per_step": round(sec * 1e6, 2), "steps": n}
+            "h2d_bytes_per_step": int(off), "d2h_bytes_per_step": int(d2h),
+            "us_per_step": round(sec * 1e6, 2), "steps": n,
+            "copies_per_step": "1 H2D (packed inputs) + 1 D2H (out), stream synchronised"}
 
 
 # -------------------------------------------------------------- CPU oracle
@@ -858,6 +962,23 @@ def run_reference(args, world, rank):
                     "d2h_bytes_per_step": 0}}
 
 
+def replica_command(n, argv, port):
+    """The command that runs this benchmark as n ranks, one process per GPU."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+            f"--nproc-per-node={n}", "--master-addr=127.0.0.1", f"--master-port={port}",
+            os.path.abspath(__file__), *argv]
+
+
+def launch_replicas(n, argv) -> int:
+    """`--gpus N` without a launcher: start N ranks (one per GPU) and pass their
+    output through; rank 0 prints the JSON line.  Returns the launcher's status."""
+    import socket
+    with socket.socket() as sock:
+        sock.bind(("127.0.0.1", 0))
+        port = sock.getsockname()[1]
+    return subprocess.call(replica_command(n, argv, port))
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -871,11 +992,22 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--chunk-tokens", type=int, default=0,
                     help="split size for pa_decode (0: the library's automatic choice)")
+    ap.add_argument("--num-seqs", type=int, default=0,
+                    help="a reduced case: the workload's shapes and draws with this many "
+                         "sequences (parents for the shared-prefix workloads); 0: full size")
+    ap.add_argument("--extra-workloads", default=",".join(EXTRA_WORKLOADS),
+                    help="comma-separated workloads measured after the headline one in a "
+                         "single-GPU run (empty: none)")
+    ap.add_argument("--extra-steps", type=int, default=300,
+                    help="at least this many timed steps for each extra workload")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("at least 3 warm-up steps")
     world, rank, local = dist_env()
-    if args.gpus != world and world > 1:
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # one process per GPU: relaunch this command under torch.distributed.run
+        sys.exit(launch_replicas(args.gpus, sys.argv[1:] if argv is None else list(argv)))
+    if args.gpus != world:
         ap.error(f"--gpus {args.gpus} but WORLD_SIZE {world}")
     if args.impl == "reference":
         res = run_reference(args, world, rank)

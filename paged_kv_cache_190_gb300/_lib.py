@@ -161,8 +161,27 @@ def _need_cuda_contig(name, t):
         raise ValueError(f"{name} must be a contiguous CUDA tensor")
 
 
+class PreparedCall:
+    """One C-ABI call with its arguments marshalled once.  Calling it enqueues
+    the same call again -- same pointers, sizes and stream -- so the tensors it
+    was made from must stay alive and in place.  The device-op wrappers below
+    return one instead of calling when given ``prepare=True``: for loops that
+    issue the same step over and over with no per-call argument checks."""
+
+    __slots__ = ("name", "fn", "args")
+
+    def __init__(self, name, args):
+        self.name, self.fn, self.args = name, getattr(library(), name), args
+
+    def __call__(self):
+        rc = self.fn(*self.args)
+        if rc != PA_OK:
+            _check(rc, self.name)
+
+
 # ----------------------------------------------------------------- device ops
-def pa_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, device_errors=None, stream=None):
+def pa_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, device_errors=None, stream=None,
+                         prepare=False):
     """k, v [T, Hkv, D]; caches [NB, Hkv, bs, D]; slot_mapping int64 [T] (see pa.h)."""
     import torch
     for n, t in (("k", k), ("v", v), ("k_cache", k_cache), ("v_cache", v_cache),
@@ -171,14 +190,17 @@ def pa_reshape_and_cache(k, v, k_cache, v_cache, slot_mapping, device_errors=Non
     if slot_mapping.dtype != torch.int64:
         raise TypeError("slot_mapping must be int64")
     NB, Hkv, bs, D = k_cache.shape
-    rc = library().pa_reshape_and_cache(
+    call = PreparedCall("pa_reshape_and_cache", (
         _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), int(k.shape[0]),
         int(Hkv), int(D), int(bs), int(NB), _dtype_code(k_cache), _ptr(device_errors),
-        _stream(stream, k_cache.device))
-    _check(rc, "pa_reshape_and_cache")
+        _stream(stream, k_cache.device)))
+    if prepare:
+        return call
+    call()
 
 
-def pa_copy_blocks(k_cache, v_cache, src_dst_pairs, device_errors=None, stream=None):
+def pa_copy_blocks(k_cache, v_cache, src_dst_pairs, device_errors=None, stream=None,
+                   prepare=False):
     """src_dst_pairs int64 [P, 2] on the device (see pa.h)."""
     import torch
     for n, t in (("k_cache", k_cache), ("v_cache", v_cache), ("src_dst_pairs", src_dst_pairs)):
@@ -187,10 +209,12 @@ def pa_copy_blocks(k_cache, v_cache, src_dst_pairs, device_errors=None, stream=N
         raise TypeError("src_dst_pairs must be int64")
     NB = k_cache.shape[0]
     block_bytes = k_cache[0].numel() * k_cache.element_size()
-    rc = library().pa_copy_blocks(_ptr(k_cache), _ptr(v_cache), _ptr(src_dst_pairs),
+    call = PreparedCall("pa_copy_blocks", (_ptr(k_cache), _ptr(v_cache), _ptr(src_dst_pairs),
                                   int(src_dst_pairs.shape[0]), block_bytes, int(NB),
-                                  _ptr(device_errors), _stream(stream, k_cache.device))
-    _check(rc, "pa_copy_blocks")
+                                  _ptr(device_errors), _stream(stream, k_cache.device)))
+    if prepare:
+        return call
+    call()
 
 
 def pa_swap_blocks(src_k, src_v, dst_k, dst_v, src_dst_pairs, device_errors=None, stream=None):
@@ -232,7 +256,8 @@ def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, bloc
 
 
 def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
-              max_context_len, workspace=None, chunk_tokens=0, device_errors=None, stream=None):
+              max_context_len, workspace=None, chunk_tokens=0, device_errors=None, stream=None,
+              prepare=False):
     """out, q [B, Hq, D]; caches [NB, Hkv, bs, D]; block_tables int32 [B, max_blocks];
     context_lens int32 [B] (see pa.h).  ``workspace``: a uint8 CUDA tensor of at
     least pa_decode_workspace_size() bytes; allocated here when None."""
@@ -249,19 +274,21 @@ def pa_decode(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_k
     if workspace is None:
         nbytes = pa_decode_workspace_size(B, Hq, Hkv, D, bs, max_context_len, chunk_tokens)
         workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
-    rc = library().pa_decode(
+    call = PreparedCall("pa_decode", (
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         float(scale), int(num_kv_heads), int(B), int(Hq), int(D), int(bs), int(NB),
         int(block_tables.shape[1]), int(max_context_len), _dtype_code(q), int(chunk_tokens),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(device_errors),
-        _stream(stream, q.device))
-    _check(rc, "pa_decode")
+        _stream(stream, q.device)))
+    if prepare:
+        return call
+    call()
     return out
 
 
 def pa_decode_multi(out, q, k_cache, v_cache, block_tables, context_lens, scale, num_kv_heads,
                     max_context_len, workspace=None, chunk_tokens=0, device_errors=None,
-                    stream=None):
+                    stream=None, prepare=False):
     """Causal paged attention for q_len new tokens per sequence: out, q
     [B, q_len, Hq, D]; the rest as pa_decode (see pa.h)."""
     import torch
@@ -277,13 +304,15 @@ def pa_decode_multi(out, q, k_cache, v_cache, block_tables, context_lens, scale,
     if workspace is None:
         nbytes = pa_decode_workspace_size(B, q_len * Hq, Hkv, D, bs, max_context_len, chunk_tokens)
         workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
-    rc = library().pa_decode_multi(
+    call = PreparedCall("pa_decode_multi", (
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         float(scale), int(num_kv_heads), int(B), int(Hq), int(q_len), int(D), int(bs), int(NB),
         int(block_tables.shape[1]), int(max_context_len), _dtype_code(q), int(chunk_tokens),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(device_errors),
-        _stream(stream, q.device))
-    _check(rc, "pa_decode_multi")
+        _stream(stream, q.device)))
+    if prepare:
+        return call
+    call()
     return out
 
 
@@ -320,7 +349,7 @@ def pa_cascade_groups(block_tables, context_lens, block_size):
 
 def pa_decode_cascade(out, q, k_cache, v_cache, block_tables, context_lens, group_start,
                       shared_lens, scale, num_kv_heads, max_context_len, workspace=None,
-                      chunk_tokens=0, device_errors=None, stream=None):
+                      chunk_tokens=0, device_errors=None, stream=None, prepare=False):
     """Shared-prefix decode (see pa.h): pa_decode's arguments plus group_start
     int32 [groups + 1] and shared_lens int32 [groups] (device tensors); bf16."""
     import torch
@@ -343,13 +372,15 @@ def pa_decode_cascade(out, q, k_cache, v_cache, block_tables, context_lens, grou
         nbytes = pa_decode_cascade_workspace_size(B, G, Hq, Hkv, D, bs, max_context_len,
                                                   chunk_tokens)
         workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
-    rc = library().pa_decode_cascade(
+    call = PreparedCall("pa_decode_cascade", (
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         _ptr(group_start), _ptr(shared_lens), int(G), float(scale), int(num_kv_heads), int(B),
         int(Hq), int(D), int(bs), int(NB), int(block_tables.shape[1]), int(max_context_len),
         int(chunk_tokens), _ptr(workspace), workspace.numel() * workspace.element_size(),
-        _ptr(device_errors), _stream(stream, q.device))
-    _check(rc, "pa_decode_cascade")
+        _ptr(device_errors), _stream(stream, q.device)))
+    if prepare:
+        return call
+    call()
     return out
 
 
@@ -397,7 +428,7 @@ def _need_scales(k_scale, v_scale, num_kv_heads):
 
 
 def pa_reshape_and_cache_fp8(k, v, k_cache, v_cache, slot_mapping, k_scale, v_scale,
-                             device_errors=None, stream=None):
+                             device_errors=None, stream=None, prepare=False):
     """k, v bf16 [T, Hkv, 128]; caches one-byte e4m3 [NB, Hkv, bs, 128];
     k_scale, v_scale float32 [Hkv] (see pa.h)."""
     import torch
@@ -411,16 +442,18 @@ def pa_reshape_and_cache_fp8(k, v, k_cache, v_cache, slot_mapping, k_scale, v_sc
         raise TypeError("k and v must be bf16")
     NB, Hkv, bs, D = k_cache.shape
     _need_scales(k_scale, v_scale, Hkv)
-    rc = library().pa_reshape_and_cache_fp8(
+    call = PreparedCall("pa_reshape_and_cache_fp8", (
         _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(slot_mapping), _ptr(k_scale),
         _ptr(v_scale), int(k.shape[0]), int(Hkv), int(D), int(bs), int(NB), _ptr(device_errors),
-        _stream(stream, k_cache.device))
-    _check(rc, "pa_reshape_and_cache_fp8")
+        _stream(stream, k_cache.device)))
+    if prepare:
+        return call
+    call()
 
 
 def pa_decode_fp8(out, q, k_cache, v_cache, block_tables, context_lens, scale, k_scale, v_scale,
                   num_kv_heads, max_context_len, workspace=None, chunk_tokens=0,
-                  device_errors=None, stream=None):
+                  device_errors=None, stream=None, prepare=False):
     """pa_decode over e4m3 pools: out, q bf16 [B, Hq, 128]; caches one-byte
     [NB, Hkv, bs, 128]; k_scale, v_scale float32 [Hkv] (see pa.h)."""
     import torch
@@ -441,13 +474,15 @@ def pa_decode_fp8(out, q, k_cache, v_cache, block_tables, context_lens, scale, k
     if workspace is None:
         nbytes = pa_decode_workspace_size(B, Hq, Hkv, D, bs, max_context_len, chunk_tokens)
         workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
-    rc = library().pa_decode_fp8(
+    call = PreparedCall("pa_decode_fp8", (
         _ptr(out), _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         float(scale), _ptr(k_scale), _ptr(v_scale), int(num_kv_heads), int(B), int(Hq), int(D),
         int(bs), int(NB), int(block_tables.shape[1]), int(max_context_len), int(chunk_tokens),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _ptr(device_errors),
-        _stream(stream, q.device))
-    _check(rc, "pa_decode_fp8")
+        _stream(stream, q.device)))
+    if prepare:
+        return call
+    call()
     return out
 
 
