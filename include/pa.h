@@ -143,7 +143,7 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
  * block_size (it sizes the launch and the workspace); a length outside
  * [0, max_context_len] sets PA_DEVERR_BAD_LENGTH and is clamped.
  * chunk_tokens: 0 chooses automatically (pa_decode_chunk_tokens); otherwise a
- * multiple of 16 and of block_size, at most 32 * block_size.  Contexts longer
+ * multiple of 16 and of block_size, at most 64 * block_size.  Contexts longer
  * than one chunk are split and merged by a second kernel (log-sum-exp).
  * workspace: caller-owned device scratch of at least pa_decode_workspace_size()
  * bytes with the same arguments, 256-byte aligned; it carries no state between

@@ -39,16 +39,16 @@ int current_sm_count() {
 // Split size: halve 512 until the (sequence, kv head, chunk) items give every
 // SM a few, but never below 64 tokens; at most 32 pages per chunk.
 int choose_chunk(int num_seqs, int num_kv_heads, int block_size, int max_context_len, int sms) {
-  int c = 512;
+  int c = pa::kItemPages * block_size;
   const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads;
   const int64_t target = 4 * static_cast<int64_t>(sms > 0 ? sms : 1);
   while (c > 64 && units * ((static_cast<int64_t>(max_context_len) + c - 1) / c) < target) c /= 2;
-  if (c > 32 * block_size) c = 32 * block_size;
   return c;
 }
 
 bool valid_chunk(int chunk, int block_size) {
-  return chunk >= 16 && chunk % 16 == 0 && chunk % block_size == 0 && chunk <= 32 * block_size;
+  return chunk >= 16 && chunk % 16 == 0 && chunk % block_size == 0 &&
+         chunk <= pa::kItemPages * block_size;
 }
 
 }  // namespace

@@ -14,6 +14,9 @@ namespace pa {
 // prefix partials (pieces) per row, and the longest own suffix a sequence may
 // have for the merge kernel to attend to it directly.
 constexpr int kPrefixStageTokens = 64;
+// Pages of one decode work item (its slice of the block table, staged in shared
+// memory): a chunk holds at most kItemPages * block_size tokens.
+constexpr int kItemPages = 64;
 constexpr int kMaxPrefixPieces = 32;
 constexpr int kInlineSuffixTokens = 32;
 

@@ -136,7 +136,7 @@ struct DecodeTraits {
   static constexpr int PS = TC ? 0 : CW * UT * G * 4;   // CUDA-core probabilities
   static constexpr int QBUF = kItemSlots * Q_BYTES;
   static constexpr int DESC = kItemSlots * static_cast<int>(sizeof(ItemDesc));
-  static constexpr int TBL = kItemSlots * 32 * 4;              // block-table slice per item
+  static constexpr int TBL = kItemSlots * kItemPages * 4;      // block-table slice per item
   static constexpr int FIXED = MERGE_ACC + MERGE_ML + PS + QBUF + DESC + TBL + 64 /*flags*/ +
                                (3 * kItemSlots + 4) * 8 + 1024 /*alignment slack*/;
   static constexpr int S_RAW = (kSmemBudget - FIXED) / (STAGE_BYTES + 2 * 8 + 4);
@@ -1005,15 +1005,17 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
       const int n_units = (ntok + PU - 1) / PU;
       const int page0 = tok0 / bs;
       const int npages = (ntok + bs - 1) / bs;
-      int phys = -1;
-      if (lane < npages) {
-        phys = p.block_tables[static_cast<int64_t>(w.x) * p.max_blocks_per_seq + page0 + lane];
-        if (phys < 0 || phys >= p.num_blocks) {
-          report(p.device_errors, PA_DEVERR_BAD_BLOCK);
-          phys = -1;
+      for (int pg = lane; pg < kItemPages; pg += 32) {
+        int phys = -1;
+        if (pg < npages) {
+          phys = p.block_tables[static_cast<int64_t>(w.x) * p.max_blocks_per_seq + page0 + pg];
+          if (phys < 0 || phys >= p.num_blocks) {
+            report(p.device_errors, PA_DEVERR_BAD_BLOCK);
+            phys = -1;
+          }
         }
+        tbl_s[slot * kItemPages + pg] = phys;
       }
-      tbl_s[slot * 32 + lane] = phys;
       if (lane == 0) {
         ItemDesc d;
         d.b = w.x; d.h = h; d.tok0 = w.y; d.len = w.z; d.gchunk = w.w & (kSingleChunk - 1);
@@ -1078,7 +1080,7 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
           }
           const int tok = u * PU;
           char* dst = stages + s * Tr::STAGE_BYTES;
-          const int pp = tbl_s[slot * 32 + tok / bs];
+          const int pp = tbl_s[slot * kItemPages + tok / bs];
           if (paired) {
             // one box per pool: the page's 16 rows of head 2h, then of head 2h + 1
             if (pp >= 0) {
@@ -1101,14 +1103,14 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
             if (rows_op < Tr::UT) {
               n_op = (min(Tr::UT, d.n_tokens - tok) + rows_op - 1) / rows_op;
               for (int j = 1; j < n_op; ++j)
-                pages_ok &= tbl_s[slot * 32 + (tok + j * rows_op) / bs] >= 0;
+                pages_ok &= tbl_s[slot * kItemPages + (tok + j * rows_op) / bs] >= 0;
             }
             if (pages_ok) {
               stage_bad[s] = 0;
               mbar_arrive_expect_tx(&full[s], n_op * rows_op * Tr::ROW_BYTES * 2);
               for (int j = 0; j < n_op; ++j) {
                 const int t = tok + j * rows_op;
-                const int pj = j == 0 ? pp : tbl_s[slot * 32 + t / bs];
+                const int pj = j == 0 ? pp : tbl_s[slot * kItemPages + t / bs];
                 const int row = (pj * p.pool_heads + d.h) * bs + t % bs;
                 tma_rows<Tr>(dst + j * rows_op * 128, &p.tmap_k, row, &full[s]);
                 tma_rows<Tr>(dst + Tr::TILE_BYTES + j * rows_op * 128, &p.tmap_v, row, &full[s]);
