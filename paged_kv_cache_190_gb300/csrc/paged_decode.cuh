@@ -63,7 +63,7 @@
 
 namespace pa {
 
-constexpr int kConsumerWarps = 8;    // consumer warps of the bf16 / fp32 kernels
+constexpr int kConsumerWarps = 8;    // consumer warps (the bf16 8-row kernel: 6)
 constexpr int kItemSlots = 8;        // items the producer may run ahead
 constexpr int kUnitsAhead = 32;      // claimed-but-unissued units a CTA may hold
 constexpr int kSmemBudget = 227 * 1024;
@@ -94,13 +94,15 @@ struct DecodeTraits {
   static constexpr int G_ = G;
   static constexpr bool KV8_ = KV8;
   static constexpr bool TC = KV8 || decode_uses_tensor_cores(BF16, G);
-  // Consumer warps: the fp8 kernel keeps 6 so that the CTA's 8 warps get up to
-  // 255 registers each (9 or more warps put 3 on some SM sub-partitions, which
-  // caps a thread at 168).  So does the 8-row kernel: its per-warp merge
-  // buffers (rows x head_dim floats each) are half its shared memory's fixed
-  // part, and with 6 warps 18 stages fit instead of 16 (measured on 2 draft
-  // tokens x GQA-4: 336 -> 314 us).
-  static constexpr int CW = (KV8 || G == 8) ? 6 : kConsumerWarps;
+  // Consumer warps: 8, which with the producer and the scheduler puts three
+  // warps on two of the SM's four sub-partitions and so caps a thread at 168
+  // registers; every consumer fits that without spilling (the fp8 one too:
+  // 8 warps against 6 measured 206 -> 187 us on the 128K workload, 212 -> 193
+  // on MHA).  The bf16 8-row kernel keeps 6: its per-warp merge buffers (rows x
+  // head_dim floats each) are half its shared memory's fixed part, and with 6
+  // warps 18 stages fit instead of 16 (measured on 2 draft tokens x GQA-4:
+  // 336 -> 314 us).
+  static constexpr int CW = (!KV8 && G == 8) ? 6 : kConsumerWarps;
   static constexpr int THREADS = (CW + 2) * 32;                // + producer + scheduler
   static constexpr int ELT = KV8 ? 1 : (BF16 ? 2 : 4);         // cache element bytes
   static constexpr int QELT = BF16 ? 2 : 4;                    // q element bytes
