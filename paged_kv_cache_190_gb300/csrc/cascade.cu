@@ -35,11 +35,29 @@ namespace {
 
 constexpr int kCascadePlanThreads = 1024;
 constexpr int kPlanGroupCache = 2048;                   // groups the plan keeps in shared memory
-constexpr int kPrefixConsumerWarps = 4;                 // one 16-row tile each
-constexpr int kPrefixThreads = (kPrefixConsumerWarps + 1) * 32;   // + the producer warp
-constexpr int kPrefixRows = 16 * kPrefixConsumerWarps;  // rows of one item (a row set)
-constexpr int kPrefixStages = 3;
-constexpr int kPrefixCtasPerSm = 2;
+constexpr int kPrefixSoftmaxWarps = 4;                  // one TMEM lane quadrant each
+// softmax warps, as many epilogue warps, two producer warps (K, V) and two MMA
+// warps (one issues the scores, one the value products)
+constexpr int kPrefixThreads = (2 * kPrefixSoftmaxWarps + 4) * 32;
+constexpr int kPrefixRows = 64;                         // query rows of one item (a row set)
+constexpr int kMmaRows = 128;                           // the MMA's M: every row twice
+constexpr int kPrefixKStages = 3;                       // K ring of the prefix kernel
+constexpr int kPrefixVStages = 4;                       // V ring
+constexpr int kPrefixMetaSlots = 4;                     // item descriptions in flight
+constexpr int kPrefixCtasPerSm = 1;
+// Longest piece (in stages) the plan considers, and the fixed cost of an item
+// of the prefix kernel (q rows, first scores, last products, hand-over) in
+// stage times, as measured on the kernel's timeline.
+constexpr int kMaxPieceSpan = 32;
+constexpr int kPieceOverheadStages = 3;
+static_assert(kMaxPieceSpan == 32, "the plan scores one candidate span per lane of a warp");
+
+// Tensor maps of the prefix kernel: the K and V pools as 2-D {head_dim, rows}
+// with 16-row x 128-byte boxes, and q as 4-D {head_dim, group, kv heads,
+// sequences} with boxes of one kv head's 128 / group members.
+struct PrefixMaps {
+  CUtensorMap k, v, q;
+};
 constexpr int kCascadeMergeWarps = 8;
 static_assert(kInlineSuffixTokens <= 32, "the merge attends to a short suffix one token per lane");
 
@@ -138,6 +156,7 @@ __global__ void __launch_bounds__(kCascadePlanThreads) cascade_plan_kernel(
   __shared__ int warp_sums[kCascadePlanThreads / 32];
   __shared__ int total_s;
   __shared__ int carry_parts, carry_work, carry_items, units_s;
+  __shared__ unsigned span_items[kMaxPieceSpan + 1];
   __shared__ int32_t gs_cache[kPlanGroupCache + 1], sl_cache[kPlanGroupCache];
   allow_next_grid();                      // the next kernel may start its prologue
   if (threadIdx.x == 0) carry_parts = carry_work = carry_items = units_s = 0;
@@ -151,24 +170,49 @@ __global__ void __launch_bounds__(kCascadePlanThreads) cascade_plan_kernel(
     shared_lens = sl_cache;
   }
   __syncthreads();
-  // ---- 1a. total prefix work in stages (x kv heads)
-  for (int base = 0; base < num_groups; base += kCascadePlanThreads) {
-    const int f = base + threadIdx.x;
-    int units = 0;
-    if (f < num_groups) {
+  // ---- 1a. the piece length: for every candidate span (stages per piece) the
+  // items it makes, then the span whose busiest CTA (items per CTA x (span +
+  // the per-item overhead, in stages)) finishes first
+  for (int i = threadIdx.x; i <= kMaxPieceSpan; i += kCascadePlanThreads) span_items[i] = 0;
+  __syncthreads();
+  {
+    // warp w takes groups w, w + 32, ...; lane c - 1 counts candidate c's items
+    const int c = (threadIdx.x & 31) + 1;
+    unsigned acc = 0;
+    for (int f = threadIdx.x >> 5; f < num_groups; f += kCascadePlanThreads / 32) {
       const int sl = usable_shared(shared_lens, f, block_size, max_blocks_per_seq, max_len);
       const int2 m = members_of(group_start, f, num_seqs);
-      const PrefixShape s = prefix_shape(sl, m.y - m.x, group, 1);
-      units = s.stages * s.rowsets;
+      const PrefixShape s1 = prefix_shape(sl, m.y - m.x, group, 1);
+      if (s1.stages > 0) {
+        // the pieces prefix_shape makes with span c (raised so that a group
+        // has at most kMaxPrefixPieces pieces)
+        const int span_c = max(c, (s1.stages + kMaxPrefixPieces - 1) / kMaxPrefixPieces);
+        acc += static_cast<unsigned>(s1.rowsets * ((s1.stages + span_c - 1) / span_c));
+      }
     }
-    block_scan(units, warp_sums, &total_s);
-    if (threadIdx.x == 0) units_s += total_s;
-    __syncthreads();
+    if (acc) atomicAdd(&span_items[c], acc);
   }
-  const int64_t total_units = static_cast<int64_t>(units_s) * num_kv_heads;
-  const int64_t target = 2 * static_cast<int64_t>(prefix_ctas > 0 ? prefix_ctas : 1);
-  const int64_t want = (total_units + target - 1) / target;
-  const int span = static_cast<int>(want > 1 ? want : 1);
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    // lane c - 1 scores candidate c; the warp keeps the cheapest (shortest on ties)
+    const int c = threadIdx.x + 1;
+    const int64_t ctas = prefix_ctas > 0 ? prefix_ctas : 1;
+    const int64_t items_c = static_cast<int64_t>(span_items[c]) * num_kv_heads;
+    int64_t cost = (items_c + ctas - 1) / ctas * (c + kPieceOverheadStages);
+    int best = c;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const int64_t oc = __shfl_xor_sync(0xffffffffu, cost, o);
+      const int ob = __shfl_xor_sync(0xffffffffu, best, o);
+      if (oc < cost || (oc == cost && ob < best)) {
+        cost = oc;
+        best = ob;
+      }
+    }
+    if (threadIdx.x == 0) units_s = best;
+  }
+  __syncthreads();
+  const int span = units_s;
   // ---- 1b. the item list
   for (int base = 0; base < num_groups; base += kCascadePlanThreads) {
     const int f = base + threadIdx.x;
@@ -250,333 +294,723 @@ __global__ void __launch_bounds__(kCascadePlanThreads) cascade_plan_kernel(
 
 // ------------------------------------------------------------ prefix kernel
 // Item = (group f, row set rs, piece) x kv head h: the piece's stages of the
-// group's shared tokens (kPrefixStageTokens each, read through the group
-// leader's block table) and the row set's 64 rows r = (member, query head of h),
-// member = r / group.  One producer warp streams each stage's K and V into a
-// 3-slot ring (one tensor-map box per 16 tokens and pool, the decode kernel's
-// swizzled layout); four consumer warps own 16 rows each and keep q, the running
-// maximum and sum, and the output in registers for the whole piece:
-//   S = Q K^T per 16 tokens (mma.sync m16n8k16, bf16, fp32 accumulation; Q rows
-//   as A, K via ldmatrix), online softmax per row in base 2, O += P V (P re-packed
-//   from the S fragments as A, V via ldmatrix.trans).
-// Each row's piece ends as one partial (output divided by its sum, base-2
-// log-sum-exp) at chunk_base[member] + piece, written only when the plan gave
-// the member that many prefix partials.  Items of kv head 0 also check that the
-// members hold the leader's pages (PA_DEVERR_BAD_BLOCK).
+// group's shared tokens (kPrefixStageTokens = 64 each, read through the group
+// leader's block table) for the row set's kPrefixRows = 64 query rows
+// rr = (member, query head of h), member = rr / group.  The products run on the
+// fifth-generation tensor cores (tcgen05.mma, M = 128): every row is in the
+// MMA twice, rows 32 quadrant + i and 32 quadrant + 16 + i for rr = 16 quadrant
+// + i, so that the four TMEM lane quadrants (one per softmax warp) hold 16 rows
+// each and a row's 64 scores of a stage split over two threads.  Warp roles:
+//   * items producer: per item, its description into a shared ring and the
+//     row set's q rows into one of two Q buffers (tensor-map boxes of 16 rows x
+//     128 bytes, straight from q viewed as [member][kv head][group][head_dim]);
+//     per stage, the K pages into a ring (one 16-row box per page and 128-byte
+//     column slab: a tile is [slab][64 tokens][128 bytes], 128-byte swizzle);
+//   * V producer: the V pages the same way into a ring of their own;
+//   * scores (one thread): per stage, S = Q K^T with one tcgen05.mma per 16
+//     columns of head_dim (N = the stage's tokens, bf16 operands in shared
+//     memory, fp32 accumulator in tensor memory, two S buffers); a K slot is
+//     released as soon as its product completes (tcgen05.commit on mbarriers);
+//   * values (one thread): once a stage's probabilities are in shared memory,
+//     O += P V with one product per 16 tokens (N = head_dim, V read in its
+//     stored layout as an MN-major operand), into one of two O buffers;
+//   * softmax (four warps): read the row's scores, keep its reference maximum
+//     (moved only when a score passes it by more than 8 in base 2; then the
+//     thread rescales the copy of the row's O in its own TMEM lane) and sum,
+//     write the probabilities as bf16 into both copies of the row in P; at the
+//     item's end hand (max, sum) over;
+//   * epilogue (four warps): read the item's O rows from tensor memory (a
+//     lane: one copy of a row, half of head_dim) and write each row's partial
+//     (output divided by its sum, base-2 log-sum-exp) at chunk_base[member] +
+//     piece, when the plan gave the member that many prefix partials; items of
+//     kv head 0 also check that the members hold the leader's pages
+//     (PA_DEVERR_BAD_BLOCK).
+// S, P, Q and O are double-buffered, so the next stage's scores, and the next
+// item's first stages, run while a stage is in softmax and an item in its
+// epilogue.
 template <int D>
 struct PrefixLayout {
-  static constexpr int ROW_BYTES = D * 2;
-  static constexpr int GROUP_BYTES = 16 * ROW_BYTES;         // 16 tokens, all slabs
-  static constexpr int GROUPS = kPrefixStageTokens / 16;
-  static constexpr int TILE_BYTES = GROUPS * GROUP_BYTES;    // K (or V) of one stage
-  static constexpr int STAGE_BYTES = 2 * TILE_BYTES;
-  static constexpr int SMEM = kPrefixStages * STAGE_BYTES + 1024 + 64;  // + alignment, barriers
+  static constexpr int SLABS = D / 64;                       // 128-byte column slabs of a row
+  static constexpr int SLAB_TILE = kPrefixStageTokens * 128; // one slab of a stage's tile
+  static constexpr int TILE_BYTES = SLABS * SLAB_TILE;       // K (or V) of one stage
+  static constexpr int OFF_V = kPrefixKStages * TILE_BYTES;
+  static constexpr int Q_SLAB = kMmaRows * 128;              // Q: [slab][128 rows][128 B]
+  static constexpr int Q_BYTES = SLABS * Q_SLAB;
+  static constexpr int P_BYTES = kMmaRows * 128;             // P: [128 rows][64 tokens bf16]
+  static constexpr int OFF_Q = OFF_V + kPrefixVStages * TILE_BYTES;
+  static constexpr int OFF_P = OFF_Q + 2 * Q_BYTES;
+  static constexpr int OFF_ML = OFF_P + 2 * P_BYTES;         // (max, sum) of every row, 2 items
+  static constexpr int OFF_META = OFF_ML + 2 * kPrefixRows * 8;
+  static constexpr int OFF_BARS = OFF_META + kPrefixMetaSlots * 32;
+  // k_full/k_empty[NK], v_full/v_empty[NV], s_full/s_free/p_full/p_free[2],
+  // q_full/q_empty/o_full/o_free/ml_full[2], meta_full/meta_empty[slots], mma_done
+  static constexpr int NUM_BARS =
+      2 * (kPrefixKStages + kPrefixVStages) + 18 + 2 * kPrefixMetaSlots + 1;
+  static constexpr int SMEM = OFF_BARS + NUM_BARS * 8 + 16 + 1024;   // + room to align to 1 KiB
   static constexpr int KS = D / 16;                          // k-steps of S
-  static constexpr int NT = D / 8;                           // n-tiles of O
+  static_assert(kPrefixStageTokens == 64, "a P row is one 128-byte swizzle row of 64 tokens");
+  static_assert(SMEM <= 227 * 1024, "shared memory over budget");
 };
 
-// Byte offset of 16-byte chunk `chunk` of token row `row` (0..15) in a 16-token
-// group: slabs of 16 rows x 128 bytes, 128-byte swizzle.
-__device__ __forceinline__ uint32_t prefix_swz(int row, int chunk) {
-  return static_cast<uint32_t>((chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+// Tensor memory: O of two items in columns [0, 128) and [128, 256), the two S
+// buffers of 64 columns at 256 and 320; 512 columns are allocated.
+constexpr uint32_t kPrefixTmemCols = 512;
+constexpr uint32_t kPrefixTmemO = 128;       // column stride of the O buffers
+constexpr uint32_t kPrefixTmemS = 256;
+
+// Shared-memory matrix descriptor of a tcgen05 operand in the 128-byte swizzled
+// layout: start address, leading-dimension byte offset (between 128-byte column
+// slabs, for an MN-major operand wider than one slab), stride byte offset (between
+// groups of 8 rows), descriptor version 1, swizzle mode 2 (128 bytes).
+__device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
-// NG (1 or 2) consecutive 16-token groups of a stage, for one warp's 16 rows
-// (g and g + 8 of lane g * 4 + c): the scores of all 16 NG tokens first (2 NG
-// independent accumulation chains over head_dim), one online-softmax update
-// of the rows' reference maximum and sum (base 2), then O += P V with NG k-steps.
-template <int D, int NG>
-__device__ __forceinline__ void prefix_step(uint32_t kg, uint32_t vg,
-                                            const uint32_t (&qa)[D / 16][4],
-                                            float (&o)[D / 8][4], float& m0, float& m1,
-                                            float& l0, float& l1, float sc, int lane) {
-  constexpr int KS = D / 16, NT = D / 8, GB = 16 * D * 2;
-  const int mi = lane >> 3, r8 = lane & 7;
-  float s[2 * NG][4];
-#pragma unroll
-  for (int t = 0; t < 2 * NG; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
-  // ---- S = Q K^T: n-tiles 2 gi (tokens 0-7 of group gi) and 2 gi + 1 (8-15)
-#pragma unroll
-  for (int ks = 0; ks < KS; ++ks) {
-#pragma unroll
-    for (int gi = 0; gi < NG; ++gi) {
-      uint32_t b00, b01, b10, b11;
-      ldsm_x4(kg + gi * GB + prefix_swz((mi >> 1) * 8 + r8, 2 * ks + (mi & 1)), b00, b01, b10,
-              b11);
-      mma_bf16_full(s[2 * gi], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b00, b01);
-      mma_bf16_full(s[2 * gi + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b10, b11);
-    }
-  }
-  // ---- online softmax: row g holds elements 0, 1 of each tile, row g + 8 elements 2, 3
-  float x0 = fmaxf(s[0][0], s[0][1]), x1 = fmaxf(s[0][2], s[0][3]);
-#pragma unroll
-  for (int t = 1; t < 2 * NG; ++t) {
-    x0 = fmaxf(x0, fmaxf(s[t][0], s[t][1]));
-    x1 = fmaxf(x1, fmaxf(s[t][2], s[t][3]));
-  }
-  x0 *= sc;
-  x1 *= sc;
-  x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, 1));
-  x0 = fmaxf(x0, __shfl_xor_sync(kFull, x0, 2));
-  x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, 1));
-  x1 = fmaxf(x1, __shfl_xor_sync(kFull, x1, 2));
-  // The reference maximum of a row only moves when a score exceeds it by more
-  // than 8 (every probability stays <= 2^8, exact in fp32 and bf16), and then
-  // for the whole warp: most steps rescale nothing.
-  const bool grow = x0 > m0 + 8.f || x1 > m1 + 8.f;
-  const bool rescale = __any_sync(kFull, grow);
-  float a0 = 1.f, a1 = 1.f;
-  if (rescale) {
-    const float n0 = fmaxf(m0, x0), n1 = fmaxf(m1, x1);
-    a0 = fast_exp2(m0 - n0);
-    a1 = fast_exp2(m1 - n1);
-    m0 = n0;
-    m1 = n1;
-  }
-  const float n0 = m0, n1 = m1;
-  float sum0 = 0.f, sum1 = 0.f;
-  uint32_t pa[NG][4];
-#pragma unroll
-  for (int gi = 0; gi < NG; ++gi) {
-    float pr[2][4];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      pr[u][0] = fast_exp2(s[2 * gi + u][0] * sc - n0);
-      pr[u][1] = fast_exp2(s[2 * gi + u][1] * sc - n0);
-      pr[u][2] = fast_exp2(s[2 * gi + u][2] * sc - n1);
-      pr[u][3] = fast_exp2(s[2 * gi + u][3] * sc - n1);
-      sum0 += pr[u][0] + pr[u][1];
-      sum1 += pr[u][2] + pr[u][3];
-    }
-    // P as the A operand (rows g / g + 8; tokens 2c, 2c + 1 / 8 + 2c, 9 + 2c)
-    pa[gi][0] = pack_bf16x2(pr[0][0], pr[0][1]);
-    pa[gi][1] = pack_bf16x2(pr[0][2], pr[0][3]);
-    pa[gi][2] = pack_bf16x2(pr[1][0], pr[1][1]);
-    pa[gi][3] = pack_bf16x2(pr[1][2], pr[1][3]);
-  }
-  l0 = l0 * a0 + sum0;
-  l1 = l1 * a1 + sum1;
-  if (rescale) {
-#pragma unroll
-    for (int t = 0; t < NT; ++t) {
-      o[t][0] *= a0;
-      o[t][1] *= a0;
-      o[t][2] *= a1;
-      o[t][3] *= a1;
-    }
-  }
-  // ---- O = O + P V; V^T fragments for n-tiles 2j, 2j + 1
-#pragma unroll
-  for (int j = 0; j < NT / 2; ++j) {
-#pragma unroll
-    for (int gi = 0; gi < NG; ++gi) {
-      uint32_t v00, v01, v10, v11;
-      ldsm_x4_trans(vg + gi * GB + prefix_swz((mi & 1) * 8 + r8, 2 * j + (mi >> 1)), v00, v01,
-                    v10, v11);
-      mma_bf16_full(o[2 * j], pa[gi][0], pa[gi][1], pa[gi][2], pa[gi][3], v00, v01);
-      mma_bf16_full(o[2 * j + 1], pa[gi][0], pa[gi][1], pa[gi][2], pa[gi][3], v10, v11);
-    }
-  }
+// Instruction descriptor of a kind::f16 tcgen05.mma: fp32 accumulator, bf16 A
+// and B, A K-major, B K-major or MN-major, N and M.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05 operation this thread issued has completed.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_addr(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane (warp-collective).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, int x, int y,
+                                            int z, int w, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Byte offset of 16-byte chunk c of row r in a 128-byte-wide swizzled tile.
+__device__ __forceinline__ uint32_t sw128(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + (((c ^ r) & 7) << 4));
+}
+
+// Tokens (multiple of 16) of stage st of a shared prefix of sl tokens.
+__device__ __forceinline__ int stage_tokens(int st, int sl) {
+  return min(kPrefixStageTokens, sl - st * kPrefixStageTokens);
+}
+
+// One item as the producer hands it to the other roles.
+struct PrefixMeta {
+  int sl;         // the group's shared tokens
+  int st01;       // first stage | (stages after the last) << 16
+  int rows;       // rows of this row set (<= kPrefixRows)
+  int base;       // first row of the set within the group | kv head << 24
+  int leader;     // the group's first sequence (its table holds the shared pages)
+  int members;    // one past the group's last sequence
+  int piece;
+  int pad;
+};
 
 template <int D>
-__global__ void __launch_bounds__(kPrefixThreads) prefix_attention_kernel(
-    const __grid_constant__ DecodeKernelParams p, const int32_t* __restrict__ group_start,
-    const int32_t* __restrict__ shared_lens, const int32_t* __restrict__ chunk_base,
-    const int32_t* __restrict__ prefix_parts, const int4* __restrict__ items, int num_seqs) {
+__global__ void __launch_bounds__(kPrefixThreads, 1) prefix_attention_kernel(
+    const __grid_constant__ DecodeKernelParams p, const __grid_constant__ PrefixMaps maps,
+    const int32_t* __restrict__ group_start, const int32_t* __restrict__ shared_lens,
+    const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ prefix_parts,
+    const int4* __restrict__ items, int num_seqs) {
   using Ly = PrefixLayout<D>;
-  constexpr int NST = kPrefixStages;
+  constexpr int NK = kPrefixKStages, NV = kPrefixVStages;
+  constexpr int NM = kPrefixMetaSlots;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + NST * Ly::STAGE_BYTES);
-  uint64_t* empty = full + NST;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + NST);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Ly::OFF_BARS);
+  uint64_t* k_full = bars;
+  uint64_t* k_empty = k_full + NK;
+  uint64_t* v_full = k_empty + NK;
+  uint64_t* v_empty = v_full + NV;
+  uint64_t* s_full = v_empty + NV;
+  uint64_t* s_free = s_full + 2;
+  uint64_t* p_full = s_free + 2;
+  uint64_t* p_free = p_full + 2;
+  uint64_t* q_full = p_free + 2;
+  uint64_t* q_empty = q_full + 2;
+  uint64_t* o_full = q_empty + 2;
+  uint64_t* o_free = o_full + 2;
+  uint64_t* ml_full = o_free + 2;
+  uint64_t* meta_full = ml_full + 2;
+  uint64_t* meta_empty = meta_full + NM;
+  uint64_t* mma_done = meta_empty + NM;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Ly::NUM_BARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  PrefixMeta* meta = reinterpret_cast<PrefixMeta*>(smem + Ly::OFF_META);
+  float2* ml = reinterpret_cast<float2*>(smem + Ly::OFF_ML);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int Hkv = p.num_kv_heads, G = p.group, bs = p.block_size;
+  constexpr int kEpiWarp0 = kPrefixSoftmaxWarps;
+  constexpr int kProducerWarp = 2 * kPrefixSoftmaxWarps;    // items, q rows and K
+  constexpr int kMmaWarp = kProducerWarp + 1;                 // scores (and TMEM)
+  constexpr int kVProducerWarp = kMmaWarp + 2;                // V (kMmaWarp + 1: values)
   if (threadIdx.x == 0) {
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kPrefixConsumerWarps);
+    for (int i = 0; i < NK; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
     }
+    for (int i = 0; i < NV; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], kPrefixSoftmaxWarps);
+      mbar_init(&p_full[i], kPrefixSoftmaxWarps);
+      mbar_init(&p_free[i], 1);
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&o_full[i], 1);
+      mbar_init(&o_free[i], kPrefixSoftmaxWarps);
+      mbar_init(&ml_full[i], kPrefixSoftmaxWarps);
+    }
+    for (int i = 0; i < NM; ++i) {
+      mbar_init(&meta_full[i], 1);
+      // released by the two MMA threads, the softmax warps, the epilogue warps
+      // and the V producer
+      mbar_init(&meta_empty[i], 3 + 2 * kPrefixSoftmaxWarps);
+    }
+    mbar_init(mma_done, 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if (warp == kMmaWarp) {
+    // one CTA per SM (its shared memory), so the columns are always free
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(tmem_slot)),
+                 "r"(kPrefixTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tmem_fence_before();
   __syncthreads();
+  tmem_fence_after();
+  const uint32_t tmem = *tmem_slot;
   wait_prior_grids();                     // the plan's item list and partial offsets
   const int n_items = p.header[2] * Hkv;
+  auto fail = [&]() {
+    if (!*abort_flag) {
+      report(p.device_errors, PA_DEVERR_TIMEOUT);
+      *abort_flag = 1;
+    }
+  };
+  // the item's description from the ring slot (every role but the producer)
+  auto take_meta = [&](uint32_t ic, PrefixMeta& mt) -> bool {
+    if (*abort_flag || !mbar_wait(&meta_full[ic % NM], (ic / NM) & 1, p.wait_limit)) return false;
+    mt = meta[ic % NM];
+    return true;
+  };
 
-  if (warp == kPrefixConsumerWarps) {
-    // ---------------- producer: lane 2j (2j + 1) copies K (V) of 16-token group j
-    uint32_t k = 0;
+  // Copies of one pool's pages of a stage into ring slot `dst`: lane (page j,
+  // slab) takes 16 tokens x 128 bytes, the pages of the piece's first 32
+  // 16-token groups fetched once per item (`pre_page`, one per lane).
+  auto stage_copies = [&](const CUtensorMap* map, unsigned char* dst, uint64_t* full, int st,
+                          int st0, int sl, int h, const int32_t* table, int pre_page) {
+    const int t0 = st * kPrefixStageTokens;
+    const int ngrp = stage_tokens(st, sl) / 16;
+    if (lane == 0) mbar_arrive_expect_tx(full, ngrp * Ly::SLABS * 16 * 128);
+    const int j = lane / Ly::SLABS, sl_ = lane % Ly::SLABS;
+    const int gi = (st - st0) * (kPrefixStageTokens / 16) + j;    // page within the piece
+    int page = __shfl_sync(kFull, pre_page, gi < 32 ? gi : 31);
+    if (j < ngrp) {
+      const int t = t0 + 16 * j;
+      if (gi >= 32) {                        // past the prefetched pages
+        page = table[t / bs];
+        if (page < 0 || page >= p.num_blocks) {
+          report(p.device_errors, PA_DEVERR_BAD_BLOCK);
+          page = -1;
+        }
+      }
+      const int row = (page * Hkv + h) * bs + t % bs;
+      tma_load_2d(dst + sl_ * Ly::SLAB_TILE + j * 16 * 128, map, 64 * sl_, row, full);
+    }
+  };
+  auto prefetch_pages = [&](const int32_t* table, int st0, int st1, int sl) {
+    const int ngi = (min(st1 * kPrefixStageTokens, sl) - st0 * kPrefixStageTokens) / 16;
+    int pre_page = -1;
+    if (lane < ngi) {
+      pre_page = table[(st0 * kPrefixStageTokens + 16 * lane) / bs];
+      if (pre_page < 0 || pre_page >= p.num_blocks) {
+        report(p.device_errors, PA_DEVERR_BAD_BLOCK);
+        pre_page = -1;                         // a row outside the pool: the box reads zeros
+      }
+    }
+    return pre_page;
+  };
+
+  if (warp == kProducerWarp) {
+    // ---------------- producer: items, q rows, K pages
+    uint32_t k = 0, ic = 0;
     bool ok = true;
-    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x) {
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++ic) {
       const int4 item = items[it / Hkv];
       const int h = it % Hkv;
       const int sl = shared_lens[item.x];
-      const int leader = members_of(group_start, item.x, num_seqs).x;
-      const int32_t* table = p.block_tables + static_cast<int64_t>(leader) * p.max_blocks_per_seq;
+      const int2 mem = members_of(group_start, item.x, num_seqs);
+      const int32_t* table = p.block_tables + static_cast<int64_t>(mem.x) * p.max_blocks_per_seq;
       const int stages = (sl + kPrefixStageTokens - 1) / kPrefixStageTokens;
       const int st0 = item.z * item.w, st1 = min(st0 + item.w, stages);
-      // the pages of the piece's first 32 16-token groups, one per lane, fetched
-      // while the first slot is awaited
-      const int ngi = (min(st1 * kPrefixStageTokens, sl) - st0 * kPrefixStageTokens) / 16;
-      int pre_page = -1;
-      if (lane < ngi) {
-        pre_page = table[(st0 * kPrefixStageTokens + 16 * lane) / bs];
-        if (pre_page < 0 || pre_page >= p.num_blocks) {
-          report(p.device_errors, PA_DEVERR_BAD_BLOCK);
-          pre_page = -1;                       // a row outside the pool: the box reads zeros
+      // the item's description, then its q rows
+      bool waited = true;
+      if (lane == 0) {
+        waited = !*abort_flag && mbar_wait(&meta_empty[ic % NM], ((ic / NM) & 1) ^ 1, p.wait_limit) &&
+                 mbar_wait(&q_empty[ic & 1], ((ic >> 1) & 1) ^ 1, p.wait_limit);
+        if (waited) {
+          PrefixMeta mt;
+          mt.sl = sl;
+          mt.st01 = st0 | (st1 << 16);
+          mt.rows = min((mem.y - mem.x) * G - item.y * kPrefixRows, kPrefixRows);
+          mt.base = item.y * kPrefixRows | (h << 24);
+          mt.leader = mem.x;
+          mt.members = mem.y;
+          mt.piece = item.z;
+          mt.pad = 0;
+          meta[ic % NM] = mt;
+          mbar_arrive(&meta_full[ic % NM]);
+          uint64_t* qb = &q_full[ic & 1];
+          mbar_arrive_expect_tx(qb, Ly::Q_BYTES);
+          unsigned char* qdst = smem + Ly::OFF_Q + (ic & 1) * Ly::Q_BYTES;
+          const int m0 = mem.x + item.y * kPrefixRows / G;
+          // row set row rr = 16 quadrant + i lands in MMA rows 32 quadrant + i
+          // and 32 quadrant + 16 + i: each a box of the quadrant's 16 / group
+          // members (16 rows x 128 bytes)
+#pragma unroll
+          for (int s = 0; s < Ly::SLABS; ++s)
+#pragma unroll
+            for (int qd = 0; qd < 4; ++qd)
+#pragma unroll
+              for (int c = 0; c < 2; ++c)
+                tma_load_4d(qdst + s * Ly::Q_SLAB + (32 * qd + 16 * c) * 128, &maps.q, 64 * s, 0,
+                            h, m0 + 16 * qd / G, qb);
         }
       }
+      if (!__shfl_sync(kFull, waited, 0)) {
+        if (lane == 0) fail();
+        ok = false;
+        break;
+      }
+      const int pre_page = prefetch_pages(table, st0, st1, sl);
       for (int st = st0; st < st1; ++st, ++k) {
-        const int slot = static_cast<int>(k % NST);
-        bool waited = false;
+        const int slot = static_cast<int>(k % NK);
+        bool w = false;
         if (lane == 0 && !*abort_flag)
-          waited = mbar_wait(&empty[slot], ((k / NST) & 1) ^ 1, p.wait_limit);
-        waited = __shfl_sync(kFull, waited, 0);
-        if (!waited) {
-          if (lane == 0 && !*abort_flag) {
-            report(p.device_errors, PA_DEVERR_TIMEOUT);
-            *abort_flag = 1;
-          }
+          w = mbar_wait(&k_empty[slot], ((k / NK) & 1) ^ 1, p.wait_limit);
+        if (!__shfl_sync(kFull, w, 0)) {
+          if (lane == 0) fail();
           ok = false;
           break;
         }
-        const int t0 = st * kPrefixStageTokens;
-        const int ngrp = min(kPrefixStageTokens, sl - t0) / 16;
-        if (lane == 0) mbar_arrive_expect_tx(&full[slot], ngrp * 2 * Ly::GROUP_BYTES);
-        const int gi = (st - st0) * Ly::GROUPS + (lane >> 1);   // group within the piece
-        int page = __shfl_sync(kFull, pre_page, gi < 32 ? gi : 31);
-        if (lane < 2 * ngrp) {
-          const int j = lane >> 1;
-          const int t = t0 + 16 * j;
-          if (gi >= 32) {                        // past the prefetched pages
-            page = table[t / bs];
-            if (page < 0 || page >= p.num_blocks) {
-              report(p.device_errors, PA_DEVERR_BAD_BLOCK);
-              page = -1;
-            }
-          }
-          const int row = (page * Hkv + h) * bs + t % bs;
-          const bool is_v = lane & 1;
-          unsigned char* dst = smem + slot * Ly::STAGE_BYTES + (is_v ? Ly::TILE_BYTES : 0) +
-                               j * Ly::GROUP_BYTES;
-          if constexpr (Ly::ROW_BYTES == 128)
-            tma_load_2d(dst, is_v ? &p.tmap_v : &p.tmap_k, 0, row, &full[slot]);
-          else
-            tma_load_3d(dst, is_v ? &p.tmap_v : &p.tmap_k, 0, row, 0, &full[slot]);
-        }
+        stage_copies(&maps.k, smem + slot * Ly::TILE_BYTES, &k_full[slot], st, st0, sl, h, table,
+                     pre_page);
       }
     }
-    // the copies of the last stages must land before the shared memory is released
-    if (lane == 0)
-      for (uint32_t j = k > NST ? k - NST : 0; j < k; ++j) mbar_wait(&full[j % NST], (j / NST) & 1);
-    return;
-  }
-
-  // ---------------- consumers
-  const int g = lane >> 2, c = lane & 3;
-  uint32_t k = 0;
-  bool live = true;
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    const int4 item = items[it / Hkv];
-    const int h = it % Hkv;
-    const int sl = shared_lens[item.x];
-    const int2 mem = members_of(group_start, item.x, num_seqs);
-    const int rows = (mem.y - mem.x) * G;
-    const int stages = (sl + kPrefixStageTokens - 1) / kPrefixStageTokens;
-    const int piece = item.z;
-    const int st0 = piece * item.w, st1 = min(st0 + item.w, stages);
-    const int row0 = item.y * kPrefixRows + 16 * warp;      // this warp's first row
-    if (h == 0) {
-      // members of this row set that use this piece hold the leader's pages
-      const int m_lo = mem.x + item.y * kPrefixRows / G;
-      const int m_hi = min(mem.y, mem.x + (item.y + 1) * kPrefixRows / G);
-      const int pg0 = st0 * kPrefixStageTokens / bs;
-      const int np = min(st1 * kPrefixStageTokens, sl) / bs - pg0;
-      const int32_t* lead = p.block_tables + static_cast<int64_t>(mem.x) * p.max_blocks_per_seq;
-      for (int i = threadIdx.x; i < (m_hi - m_lo) * np; i += kPrefixConsumerWarps * 32) {
-        const int m = m_lo + i / np, pg = pg0 + i % np;
-        if (piece < prefix_parts[m] &&
-            p.block_tables[static_cast<int64_t>(m) * p.max_blocks_per_seq + pg] != lead[pg])
-          report(p.device_errors, PA_DEVERR_BAD_BLOCK);
-      }
+    // the copies still in flight must land before the shared memory is released
+    if (lane == 0) {
+      for (uint32_t j = k > NK ? k - NK : 0; j < k; ++j) mbar_wait(&k_full[j % NK], (j / NK) & 1);
+      for (uint32_t j = ic > 2 ? ic - 2 : 0; j < ic; ++j) mbar_wait(&q_full[j & 1], (j >> 1) & 1);
     }
-    // ---- q of rows ra = row0 + g and rb = ra + 8: member r / G, head h G + r % G
-    const int ra = row0 + g, rb = ra + 8;
-    const char* qra = ra < rows ? p.q + ((static_cast<int64_t>(mem.x + ra / G) * p.num_q_heads +
-                                          h * G + ra % G) * D) * 2
-                                : nullptr;
-    const char* qrb = rb < rows ? p.q + ((static_cast<int64_t>(mem.x + rb / G) * p.num_q_heads +
-                                          h * G + rb % G) * D) * 2
-                                : nullptr;
-    uint32_t qa[Ly::KS][4];
-#pragma unroll
-    for (int ks = 0; ks < Ly::KS; ++ks) {
-      const int col = 16 * ks + 2 * c;
-      qa[ks][0] = qra ? *reinterpret_cast<const uint32_t*>(qra + col * 2) : 0u;
-      qa[ks][1] = qrb ? *reinterpret_cast<const uint32_t*>(qrb + col * 2) : 0u;
-      qa[ks][2] = qra ? *reinterpret_cast<const uint32_t*>(qra + (col + 8) * 2) : 0u;
-      qa[ks][3] = qrb ? *reinterpret_cast<const uint32_t*>(qrb + (col + 8) * 2) : 0u;
-    }
-    float o[Ly::NT][4];
-#pragma unroll
-    for (int n = 0; n < Ly::NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m0 = kNoScore, m1 = kNoScore, l0 = 0.f, l1 = 0.f;   // rows g, g + 8
-    const bool has_rows = row0 < rows;
-    for (int st = st0; st < st1; ++st, ++k) {
-      const int slot = static_cast<int>(k % NST);
-      if (live) {
-        bool waited = !*abort_flag && mbar_wait(&full[slot], (k / NST) & 1, p.wait_limit);
-        waited = __all_sync(kFull, waited);
-        if (!waited) {
-          if (lane == 0 && !*abort_flag) {
-            report(p.device_errors, PA_DEVERR_TIMEOUT);
-            *abort_flag = 1;
-          }
-          live = false;
-        }
-      }
-      if (live && has_rows) {
-        const uint32_t kb = smem_addr(smem + slot * Ly::STAGE_BYTES);
-        const uint32_t vb = kb + Ly::TILE_BYTES;
-        const int ngrp = min(kPrefixStageTokens, sl - st * kPrefixStageTokens) / 16;
-        const float sc = p.scale_log2;
-        int grp = 0;
-        for (; grp + 2 <= ngrp; grp += 2)
-          prefix_step<D, 2>(kb + grp * Ly::GROUP_BYTES, vb + grp * Ly::GROUP_BYTES, qa, o, m0, m1,
-                            l0, l1, sc, lane);
-        if (grp < ngrp)
-          prefix_step<D, 1>(kb + grp * Ly::GROUP_BYTES, vb + grp * Ly::GROUP_BYTES, qa, o, m0, m1,
-                            l0, l1, sc, lane);
+  } else if (warp == kVProducerWarp) {
+    // ---------------- producer: V pages
+    uint32_t k = 0, ic = 0;
+    bool ok = true;
+    for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++ic) {
+      PrefixMeta mt;
+      bool got = take_meta(ic, mt);
+      if (!__all_sync(kFull, got)) {
+        if (lane == 0) fail();
+        break;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[slot]);   // the slot may be refilled
-    }
-    if (!live || !has_rows) continue;
-    // ---- partials of rows g and g + 8
-    l0 += __shfl_xor_sync(kFull, l0, 1);
-    l0 += __shfl_xor_sync(kFull, l0, 2);
-    l1 += __shfl_xor_sync(kFull, l1, 1);
-    l1 += __shfl_xor_sync(kFull, l1, 2);
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int r = half ? rb : ra;
-      if (r >= rows) continue;
-      const int b = mem.x + r / G;
-      if (piece >= prefix_parts[b]) continue;      // the plan gave this member no such partial
-      const int qh = h * G + r % G;
-      const int64_t prow = static_cast<int64_t>(chunk_base[b] + piece) * p.num_q_heads + qh;
-      const float l = half ? l1 : l0;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll
-      for (int n = 0; n < Ly::NT; ++n) {
-        const float2 v = half ? make_float2(o[n][2] * inv, o[n][3] * inv)
-                              : make_float2(o[n][0] * inv, o[n][1] * inv);
-        *reinterpret_cast<float2*>(p.part_out + prow * D + 8 * n + 2 * c) = v;
+      if (lane == 0) mbar_arrive(&meta_empty[ic % NM]);
+      const int st0 = mt.st01 & 0xFFFF, st1 = mt.st01 >> 16, sl = mt.sl, h = mt.base >> 24;
+      const int32_t* table = p.block_tables + static_cast<int64_t>(mt.leader) * p.max_blocks_per_seq;
+      const int pre_page = prefetch_pages(table, st0, st1, sl);
+      for (int st = st0; st < st1; ++st, ++k) {
+        const int slot = static_cast<int>(k % NV);
+        bool w = false;
+        if (lane == 0 && !*abort_flag)
+          w = mbar_wait(&v_empty[slot], ((k / NV) & 1) ^ 1, p.wait_limit);
+        if (!__shfl_sync(kFull, w, 0)) {
+          if (lane == 0) fail();
+          ok = false;
+          break;
+        }
+        stage_copies(&maps.v, smem + Ly::OFF_V + slot * Ly::TILE_BYTES, &v_full[slot], st, st0, sl,
+                     h, table, pre_page);
       }
-      if (c == 0) p.part_lse[prow] = l > 0.f ? (half ? m1 : m0) + __log2f(l) : -INFINITY;
     }
+    if (lane == 0)
+      for (uint32_t j = k > NV ? k - NV : 0; j < k; ++j) mbar_wait(&v_full[j % NV], (j / NV) & 1);
+  } else if (warp == kMmaWarp) {
+    // ---------------- S = Q K^T issue: one thread
+    if (lane == 0) {
+      const uint32_t q_base = smem_addr(smem + Ly::OFF_Q);
+      const uint32_t stage_base = smem_addr(smem);
+      uint32_t k = 0, ic = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++ic) {
+        PrefixMeta mt;
+        if (!take_meta(ic, mt)) { ok = false; break; }
+        mbar_arrive(&meta_empty[ic % NM]);
+        const int st0 = mt.st01 & 0xFFFF, st1 = mt.st01 >> 16, sl = mt.sl;
+        if (*abort_flag || !mbar_wait(&q_full[ic & 1], (ic >> 1) & 1, p.wait_limit)) {
+          ok = false;
+          break;
+        }
+        // descriptors advance by (byte offset >> 4) in their address field
+        const uint64_t qd0 = umma_desc(q_base + (ic & 1) * Ly::Q_BYTES, 16, 1024);
+        for (int st = st0; st < st1 && ok; ++st, ++k) {
+          const int slot = static_cast<int>(k % NK), sb = k & 1;
+          if (*abort_flag || !mbar_wait(&k_full[slot], (k / NK) & 1, p.wait_limit) ||
+              !mbar_wait(&s_free[sb], ((k >> 1) & 1) ^ 1, p.wait_limit)) {
+            ok = false;
+            break;
+          }
+          tmem_fence_after();
+          const int tokens = stage_tokens(st, sl);
+          const uint32_t id_s = umma_idesc_bf16(kMmaRows, tokens, false);
+          const uint64_t kd = umma_desc(stage_base + slot * Ly::TILE_BYTES, 16, 1024);
+#pragma unroll
+          for (int ks = 0; ks < Ly::KS; ++ks)
+            umma_bf16(tmem + kPrefixTmemS + 64 * sb,
+                      qd0 + (((ks >> 2) * Ly::Q_SLAB + (ks & 3) * 32) >> 4),
+                      kd + (((ks >> 2) * Ly::SLAB_TILE + (ks & 3) * 32) >> 4), id_s,
+                      ks > 0 ? 1u : 0u);
+          umma_commit(&s_full[sb]);
+          umma_commit(&k_empty[slot]);          // the K slot may be refilled
+          if (st + 1 == st1) umma_commit(&q_empty[ic & 1]);   // the item's q rows are read
+        }
+      }
+      if (!ok) fail();
+      // nothing may be in flight when the columns are released
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp + 1) {
+    // ---------------- O += P V issue: one thread
+    if (lane == 0) {
+      constexpr uint32_t kIdPV = umma_idesc_bf16(kMmaRows, D, true);
+      const uint32_t p_base = smem_addr(smem + Ly::OFF_P);
+      const uint32_t stage_base = smem_addr(smem);
+      uint32_t k = 0, ic = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++ic) {
+        PrefixMeta mt;
+        if (!take_meta(ic, mt)) { ok = false; break; }
+        mbar_arrive(&meta_empty[ic % NM]);
+        const int st0 = mt.st01 & 0xFFFF, st1 = mt.st01 >> 16, sl = mt.sl;
+        const uint32_t o_col = tmem + (ic & 1) * kPrefixTmemO;
+        for (int st = st0; st < st1 && ok; ++st, ++k) {
+          const int pb = k & 1, slot = static_cast<int>(k % NV);
+          const bool first = st == st0;
+          if (*abort_flag || !mbar_wait(&p_full[pb], (k >> 1) & 1, p.wait_limit) ||
+              !mbar_wait(&v_full[slot], (k / NV) & 1, p.wait_limit) ||
+              (first && !mbar_wait(&o_free[ic & 1], ((ic >> 1) & 1) ^ 1, p.wait_limit))) {
+            ok = false;
+            break;
+          }
+          tmem_fence_after();
+          const int tokens = stage_tokens(st, sl);
+          const uint64_t pd = umma_desc(p_base + pb * Ly::P_BYTES, 16, 1024);
+          const uint64_t vd =
+              umma_desc(stage_base + Ly::OFF_V + slot * Ly::TILE_BYTES, Ly::SLAB_TILE, 1024);
+          for (int g = 0; g < tokens / 16; ++g)
+            umma_bf16(o_col, pd + 2 * g, vd + 128 * g, kIdPV, (first && g == 0) ? 0u : 1u);
+          umma_commit(&v_empty[slot]);         // the V slot may be refilled
+          umma_commit(&p_free[pb]);            // the P buffer may be rewritten
+        }
+        if (ok) umma_commit(&o_full[ic & 1]);
+      }
+      if (!ok) fail();
+      umma_commit(mma_done);
+      mbar_wait(mma_done, 0);
+    }
+    __syncwarp();
+  } else if (warp < kPrefixSoftmaxWarps) {
+    // ---------------- softmax warps.  Thread (warp qd, lane l) holds MMA row
+    // 32 qd + l, i.e. row set row rr = 16 qd + l % 16 (every row is in the MMA
+    // twice, rows 32 qd + i and 32 qd + 16 + i), and half h = l / 16 of the
+    // stage's 64 columns; the two halves of a row meet through one shuffle.
+    // Each thread writes its half of the probabilities into both copies of the
+    // row in P, so O holds every row twice as well and each thread rescales the
+    // copy in its own TMEM lane.
+    const int rr = 16 * warp + (lane & 15);
+    const int half = lane >> 4;
+    const int r0 = 32 * warp + (lane & 15);          // the row's two MMA rows: r0, r0 + 16
+    const uint32_t lane_tmem = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const float sc = p.scale_log2;
+    unsigned char* ps = smem + Ly::OFF_P;
+    uint32_t k = 0, ic = 0;
+    bool live = true;
+    for (int it = blockIdx.x; it < n_items && live; it += gridDim.x, ++ic) {
+      PrefixMeta mt;
+      bool got = take_meta(ic, mt);
+      got = __all_sync(kFull, got);
+      if (!got) {
+        if (lane == 0) fail();
+        break;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&meta_empty[ic % NM]);
+      const int st0 = mt.st01 & 0xFFFF, st1 = mt.st01 >> 16, sl = mt.sl;
+      const uint32_t o_col = (ic & 1) * kPrefixTmemO;
+      float m = kNoScore, l = 0.f;                   // l: this half's columns
+      for (int st = st0; st < st1; ++st, ++k) {
+        const int sb = k & 1;
+        bool waited = !*abort_flag && mbar_wait(&s_full[sb], (k >> 1) & 1, p.wait_limit);
+        waited = __all_sync(kFull, waited);
+        if (!waited) {
+          if (lane == 0) fail();
+          live = false;
+          break;
+        }
+        tmem_fence_after();
+        const int tokens = stage_tokens(st, sl);
+        // a TMEM load takes one address for the whole warp: every lane reads
+        // the 64 columns of its row and keeps its half
+        float s[32], t[32];
+        tmem_ld16(lane_tmem + kPrefixTmemS + 64 * sb, s);
+        tmem_ld16(lane_tmem + kPrefixTmemS + 64 * sb + 16, s + 16);
+        tmem_ld16(lane_tmem + kPrefixTmemS + 64 * sb + 32, t);
+        tmem_ld16(lane_tmem + kPrefixTmemS + 64 * sb + 48, t + 16);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) s[c] = half ? t[c] : s[c];
+        tmem_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[sb]);      // the S buffer may be rewritten
+        if (tokens < kPrefixStageTokens) {            // the piece's last, partial stage
+#pragma unroll
+          for (int c = 0; c < 32; ++c)
+            if (32 * half + c >= tokens) s[c] = -INFINITY;
+        }
+        float mx[4] = {s[0], s[1], s[2], s[3]};
+#pragma unroll
+        for (int c = 4; c < 32; ++c) mx[c & 3] = fmaxf(mx[c & 3], s[c]);
+        float x = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        x = fmaxf(x, __shfl_xor_sync(kFull, x, 16)) * sc;
+        // The reference maximum moves only when a score passes it by more than
+        // 8 (every probability stays <= 2^8, exact in fp32 and bf16); then the
+        // row's O, complete up to the previous stage, is rescaled in place.
+        float alpha = 1.f;
+        const bool grow = x > m + 8.f;
+        if (grow) {
+          alpha = fast_exp2(m - x);
+          m = x;
+        }
+        l *= alpha;
+        if (st > st0 && __any_sync(kFull, grow)) {
+          const uint32_t kp = k - 1;
+          bool ok = mbar_wait(&p_free[kp & 1], (kp >> 1) & 1, p.wait_limit);   // PV(kp) done
+          ok = __all_sync(kFull, ok);
+          if (!ok) {
+            if (lane == 0) fail();
+            live = false;
+            break;
+          }
+          tmem_fence_after();
+#pragma unroll
+          for (int c = 0; c < D / 16; ++c) {
+            float o[16];
+            tmem_ld16(lane_tmem + o_col + 16 * c, o);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] *= alpha;
+            tmem_st16(lane_tmem + o_col + 16 * c, o);
+          }
+          tmem_wait_st();
+        }
+        // ---- probabilities into the P buffer of this stage (this half's four
+        // 16-byte chunks of both copies of the row), once the products of two
+        // stages ago have read it
+        bool ok = mbar_wait(&p_free[sb], ((k >> 1) & 1) ^ 1, p.wait_limit);
+        ok = __all_sync(kFull, ok);
+        if (!ok) {
+          if (lane == 0) fail();
+          live = false;
+          break;
+        }
+        float sum[4] = {0.f, 0.f, 0.f, 0.f};
+        unsigned char* prow = ps + sb * Ly::P_BYTES;
+        const float nm = -m;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          float e[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            e[i] = fast_exp2(fmaf(s[8 * c + i], sc, nm));
+            sum[i & 3] += e[i];
+          }
+          uint4 w;
+          w.x = pack_bf16x2(e[0], e[1]);
+          w.y = pack_bf16x2(e[2], e[3]);
+          w.z = pack_bf16x2(e[4], e[5]);
+          w.w = pack_bf16x2(e[6], e[7]);
+          *reinterpret_cast<uint4*>(prow + sw128(r0, 4 * half + c)) = w;
+          *reinterpret_cast<uint4*>(prow + sw128(r0 + 16, 4 * half + c)) = w;
+        }
+        l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tmem_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[sb]);
+      }
+      if (!live) break;
+      // ---- hand the row's (max, sum) to the epilogue, once the epilogue of two
+      // items ago has read this buffer
+      l += __shfl_xor_sync(kFull, l, 16);
+      bool freed = mbar_wait(&o_free[ic & 1], ((ic >> 1) & 1) ^ 1, p.wait_limit);
+      freed = __all_sync(kFull, freed);
+      if (!freed) {
+        if (lane == 0) fail();
+        break;
+      }
+      if (half == 0) ml[(ic & 1) * kPrefixRows + rr] = make_float2(m, l);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ml_full[ic & 1]);
+    }
+  } else {
+    // ---------------- epilogue warps: the lane quadrant of warp % 4
+    const int qd = warp - kEpiWarp0;
+    const int r = qd * 32 + lane;                    // thread index of the epilogue warps
+    const uint32_t lane_tmem = tmem + (static_cast<uint32_t>(qd * 32) << 16);
+    uint32_t ic = 0;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++ic) {
+      PrefixMeta mt;
+      bool got = take_meta(ic, mt);
+      got = __all_sync(kFull, got);
+      if (!got) {
+        if (lane == 0) fail();
+        break;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&meta_empty[ic % NM]);
+      const int h = mt.base >> 24, rs0 = mt.base & 0xFFFFFF;
+      const int2 mem = make_int2(mt.leader, mt.members);
+      const int piece = mt.piece;
+      if (h == 0) {
+        // members of this row set that use this piece hold the leader's pages
+        const int st0 = mt.st01 & 0xFFFF, st1 = mt.st01 >> 16;
+        const int m_lo = mem.x + rs0 / G;
+        const int m_hi = min(mem.y, mem.x + (rs0 + kPrefixRows) / G);
+        const int pg0 = st0 * kPrefixStageTokens / bs;
+        const int np = min(st1 * kPrefixStageTokens, mt.sl) / bs - pg0;
+        const int32_t* lead = p.block_tables + static_cast<int64_t>(mem.x) * p.max_blocks_per_seq;
+        for (int i = r; i < (m_hi - m_lo) * np; i += kPrefixSoftmaxWarps * 32) {
+          const int m = m_lo + i / np, pg = pg0 + i % np;
+          if (piece < prefix_parts[m] &&
+              p.block_tables[static_cast<int64_t>(m) * p.max_blocks_per_seq + pg] != lead[pg])
+            report(p.device_errors, PA_DEVERR_BAD_BLOCK);
+        }
+      }
+      // lane l: row set row rr = 16 qd + l % 16 (its copy in TMEM lane 32 qd + l)
+      // and half l / 16 of head_dim
+      const int rr = 16 * qd + (lane & 15), half = lane >> 4;
+      const bool active = 16 * qd < mt.rows;
+      const bool has_row = rr < mt.rows;
+      const int gr = rs0 + rr;                       // row within the group
+      const int b = has_row ? mem.x + gr / G : mem.x;
+      const bool write = has_row && piece < prefix_parts[b];
+      const int qh = h * G + gr % G;
+      const int64_t prow =
+          write ? static_cast<int64_t>(chunk_base[b] + piece) * p.num_q_heads + qh : 0;
+      bool done = !*abort_flag && mbar_wait(&o_full[ic & 1], (ic >> 1) & 1, p.wait_limit) &&
+                  mbar_wait(&ml_full[ic & 1], (ic >> 1) & 1, p.wait_limit);
+      done = __all_sync(kFull, done);
+      if (!done) {
+        if (lane == 0) fail();
+        break;
+      }
+      tmem_fence_after();
+      if (active) {
+        const float2 st = ml[(ic & 1) * kPrefixRows + rr];
+        const float inv = st.y > 0.f ? 1.f / st.y : 0.f;
+        const uint32_t o_col = (ic & 1) * kPrefixTmemO;
+#pragma unroll
+        for (int c = 0; c < D / 16; ++c) {
+          float o[16];
+          tmem_ld16(lane_tmem + o_col + 16 * c, o);     // one address for the warp
+          tmem_wait_ld();
+          if (write && (c >= D / 32) == (half != 0)) {
+            float4* dst = reinterpret_cast<float4*>(p.part_out + prow * D + 16 * c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
+                                   o[4 * i + 3] * inv);
+          }
+        }
+        if (write && half == 0) p.part_lse[prow] = st.y > 0.f ? st.x + __log2f(st.y) : -INFINITY;
+      }
+      tmem_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&o_free[ic & 1]);
+    }
+  }
+  tmem_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tmem_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kPrefixTmemCols)
+                 : "memory");
   }
 }
 
@@ -830,10 +1264,28 @@ cudaError_t run_prefix(const DecodeArgs& a, const DecodeKernelParams& kp, int de
     if (e != cudaSuccess) return e;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
+  const int group = a.num_q_heads / a.num_kv_heads;
+  PrefixMaps maps;
+  const uint64_t rows = static_cast<uint64_t>(a.num_blocks) * a.num_kv_heads * a.block_size;
+  const uint64_t pool_dims[2] = {static_cast<uint64_t>(D), rows};
+  const uint64_t pool_strides[1] = {static_cast<uint64_t>(D) * 2};
+  const uint32_t pool_box[2] = {64, 16};
+  cudaError_t e = make_bf16_map(&maps.k, a.k_cache, 2, pool_dims, pool_strides, pool_box);
+  if (e == cudaSuccess) e = make_bf16_map(&maps.v, a.v_cache, 2, pool_dims, pool_strides, pool_box);
+  const uint64_t q_dims[4] = {static_cast<uint64_t>(D), static_cast<uint64_t>(group),
+                              static_cast<uint64_t>(a.num_kv_heads),
+                              static_cast<uint64_t>(a.num_seqs)};
+  const uint64_t q_strides[3] = {static_cast<uint64_t>(D) * 2,
+                                 static_cast<uint64_t>(group) * D * 2,
+                                 static_cast<uint64_t>(a.num_q_heads) * D * 2};
+  const uint32_t q_box[4] = {64, static_cast<uint32_t>(group), 1,
+                             static_cast<uint32_t>(16 / group)};
+  if (e == cudaSuccess) e = make_bf16_map(&maps.q, a.q, 4, q_dims, q_strides, q_box);
+  if (e != cudaSuccess) return e;
   // a dependent of the decode kernel (itself one of the plan kernel): its
   // blocks wait on the device for both, i.e. for the item list
   return launch_pdl(prefix_attention_kernel<D>, static_cast<unsigned>(prefix_grid(a.num_sms)),
-                    kPrefixThreads, Ly::SMEM, stream, kp,
+                    kPrefixThreads, Ly::SMEM, stream, kp, maps,
                     static_cast<const int32_t*>(a.group_start),
                     static_cast<const int32_t*>(a.shared_lens),
                     static_cast<const int32_t*>(a.ws.chunk_base),

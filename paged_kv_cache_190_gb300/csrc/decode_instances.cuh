@@ -55,6 +55,10 @@ cudaError_t run_decode_f32(int head_dim, int group, const DecodeKernelParams& kp
                            int device, cudaStream_t stream);
 cudaError_t run_decode_fp8(int head_dim, int group, const DecodeKernelParams& kp, int grid,
                            int device, cudaStream_t stream);
+// A tensor map of bf16 elements with 128-byte swizzle: `rank` dimensions
+// (innermost first), the byte strides of dimensions 1.. and the box.
+cudaError_t make_bf16_map(CUtensorMap* map, const void* base, int rank, const uint64_t* dims,
+                          const uint64_t* strides, const uint32_t* box);
 cudaError_t launch_cascade_prefix(const DecodeArgs& a, const DecodeKernelParams& kp, int device,
                                   cudaStream_t stream);
 cudaError_t launch_cascade_merge(const DecodeArgs& a, const DecodeKernelParams& kp,
