@@ -213,3 +213,25 @@ def test_more_groups_than_the_plan_caches():
     out, flags, _ = _cascade(case, starts, shared)
     assert flags == 0
     check_tolerance(out_as_f64(out), _oracle(case), "bf16", case.name)
+
+
+@pytest.mark.parametrize("limit", [0, 64])
+def test_expired_waits_in_the_prefix_kernel_leave_the_context_usable(limit):
+    """The shared-prefix kernel's pipeline waits (TMA rings, tensor-core
+    completions, tensor-memory hand-overs) are bounded: with the bound cut to
+    `limit` polls they expire, the call reports PA_DEVERR_TIMEOUT and returns
+    (tensor memory released, copies drained), and the next call with the normal
+    bound is exact."""
+    case, starts, shared = _grouped_case("cascade-timeout", 1280, 32, 8, 128, 16, LENS, GROUPS,
+                                         SHARED)
+    try:
+        pa.pa_debug_set_wait_limit(limit)
+        _, flags, _ = _cascade(case, starts, shared)
+    finally:
+        pa.pa_debug_set_wait_limit(-1)
+    assert flags & ~pa.PA_DEVERR_TIMEOUT == 0
+    if limit == 0:
+        assert flags & pa.PA_DEVERR_TIMEOUT
+    out, flags, _ = _cascade(case, starts, shared)
+    assert flags == 0
+    check_tolerance(out_as_f64(out), _oracle(case), "bf16", case.name)
