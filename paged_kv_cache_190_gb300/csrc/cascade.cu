@@ -544,6 +544,7 @@ __global__ void __launch_bounds__(kPrefixThreads, 1) prefix_attention_kernel(
   tmem_fence_after();
   const uint32_t tmem = *tmem_slot;
   wait_prior_grids();                     // the plan's item list and partial offsets
+  allow_next_grid();                      // the merge may start its independent loads
   const int n_items = p.header[2] * Hkv;
   auto fail = [&]() {
     if (!*abort_flag) {
@@ -1037,17 +1038,26 @@ __global__ void __launch_bounds__(kCascadeMergeWarps * 32) cascade_merge_kernel(
   constexpr int D = CPL * 32;
   constexpr int KV = D / 8;                     // 16-byte pieces of a row
   __shared__ __align__(16) float q_s[kCascadeMergeWarps][G * D];
-  wait_prior_grids();                           // every partial is written
+  // Launched as a programmatic dependent of the prefix kernel, which lets it
+  // start early: the plan's arrays, q and the suffix's pages are complete
+  // already (the plan ran before the prefix kernel's own wait returned), so
+  // they are loaded first; only the partials wait for the prefix kernel.
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
   const int64_t item = static_cast<int64_t>(blockIdx.x) * kCascadeMergeWarps + warp;
-  if (item >= static_cast<int64_t>(num_seqs) * Hkv) return;
+  if (item >= static_cast<int64_t>(num_seqs) * Hkv) {
+    wait_prior_grids();
+    return;
+  }
   const int b = static_cast<int>(item / Hkv);
   const int h = static_cast<int>(item - static_cast<int64_t>(b) * Hkv);
   const int c0 = chunk_base[b];
   const int n = chunk_base[b + 1] - c0;
   const int s0 = inline_start[b];
-  if (n <= 0 && s0 < 0) return;                 // uniform over the warp
+  if (n <= 0 && s0 < 0) {                       // uniform over the warp
+    wait_prior_grids();
+    return;
+  }
   const int bs = p.block_size;
   const int L = s0 >= 0 ? min(max(context_lens[b], 0), max_len) : 0;
   const int nsuf = s0 >= 0 ? min(L - s0, 32) : 0;
@@ -1094,6 +1104,7 @@ __global__ void __launch_bounds__(kCascadeMergeWarps * 32) cascade_merge_kernel(
     vr[j] = j < nsuf ? *reinterpret_cast<const VCols*>(p.v_cache + (rj + lane * CPL) * 2)
                      : VCols{};
   }
+  wait_prior_grids();                           // every partial is written
   // ---- the partials of the G rows
   float M[G], S[G], acc[G][CPL];
 #pragma unroll
