@@ -11,9 +11,10 @@
 //   * Work item = (sequence, kv head, chunk of `chunk_tokens` tokens).  A tiny
 //     plan kernel lists the (sequence, chunk) pairs; items are handed out by an
 //     atomic counter, so lognormal lengths balance across SMs.
-//   * One CTA per SM, persistent.  The last warp schedules: it claims items and
+//   * One CTA per SM, persistent.  Behind the consumer warps come the producer,
+//     the scheduler and the merger.  The scheduler claims items and
 //     resolves them (work entry, block-table slice) into shared item slots and
-//     starts the copy of each item's q rows.  The warp before it produces: lane
+//     starts the copy of each item's q rows.  The producer warp: lane
 //     w streams the K and V tiles of consumer warp w's units into that warp's
 //     ring of stages (mbarrier-guarded), with blocking waits of its own, so the
 //     lanes advance independently and several copies are in issue at once (a
@@ -41,8 +42,9 @@
 //       - tensor cores, float8 e4m3 pools (any group): mma.sync m16n8k32 with
 //         e4m3 operands, so the stored codes enter the products unconverted
 //         (see Fp8TensorConsumer).
-//   * At the end of an item the partial states are merged through shared
-//     memory (log-sum-exp) and the item's rows are written either straight to
+//   * At the end of an item the consumer warps hand their partial states to
+//     the merge warp through shared memory and go on with their next item; it
+//     merges them (log-sum-exp) and writes the item's rows either straight to
 //     `out` (single-chunk sequence) or as a normalised partial plus its base-2
 //     log-sum-exp for the split-K merge kernel.
 //   * Every wait is bounded; on expiry the kernel reports PA_DEVERR_TIMEOUT,
@@ -103,7 +105,8 @@ struct DecodeTraits {
   // warps 18 stages fit instead of 16 (measured on 2 draft tokens x GQA-4:
   // 336 -> 314 us).
   static constexpr int CW = (!KV8 && G == 8) ? 6 : kConsumerWarps;
-  static constexpr int THREADS = (CW + 2) * 32;                // + producer + scheduler
+  // + producer + scheduler + merger
+  static constexpr int THREADS = (CW + 3) * 32;
   static constexpr int ELT = KV8 ? 1 : (BF16 ? 2 : 4);         // cache element bytes
   static constexpr int QELT = BF16 ? 2 : 4;                    // q element bytes
   static constexpr int ROW_BYTES = D * ELT;                    // one cache row
@@ -158,11 +161,12 @@ struct DecodeTraits {
   static constexpr int OFF_DESC = OFF_PS + PS;
   static constexpr int OFF_TBL = OFF_DESC + DESC;
   static constexpr int OFF_SFLAG = OFF_TBL + TBL;
-  // abort flag, merge arrival counter, units issued per producer lane [8]
+  // abort flag, a spare word, units issued per producer lane [8]
   static constexpr int OFF_ABORT = OFF_SFLAG + S * 4;
   static constexpr int OFF_BARS = ((OFF_ABORT + 8 + 4 * kConsumerWarps + 7) / 8) * 8;
-  // barriers: full[S], empty[S], item_full[NI], item_empty[NI], sched_full[NI], merge_free
-  static constexpr int NUM_BARS = 2 * S + 3 * kItemSlots + 1;
+  // barriers: full[S], empty[S], item_full[NI], item_empty[NI], sched_full[NI], merge_free,
+  // merge_full
+  static constexpr int NUM_BARS = 2 * S + 3 * kItemSlots + 2;
   static constexpr int SMEM_BYTES = OFF_BARS + NUM_BARS * 8;
   static constexpr int SMEM_ALLOC = SMEM_BYTES + 1024;        // room to align the base to 1 KiB
   static_assert(SMEM_ALLOC <= kSmemBudget, "shared memory over budget");
@@ -915,7 +919,6 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
   volatile int* stage_bad = reinterpret_cast<volatile int*>(smem + Tr::OFF_SFLAG);
   int* tbl_s = reinterpret_cast<int*>(smem + Tr::OFF_TBL);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Tr::OFF_ABORT);
-  int* merge_cnt = reinterpret_cast<int*>(smem + Tr::OFF_ABORT + 4);
   volatile uint32_t* issued_by = reinterpret_cast<volatile uint32_t*>(smem + Tr::OFF_ABORT + 8);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Tr::OFF_BARS);
   uint64_t* full = bars;
@@ -924,6 +927,7 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
   uint64_t* item_empty = item_full + kItemSlots;
   uint64_t* sched_full = item_empty + kItemSlots;
   uint64_t* merge_free = sched_full + kItemSlots;
+  uint64_t* merge_full = merge_free + 1;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -935,14 +939,14 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
     }
     for (int k = 0; k < kItemSlots; ++k) {
       mbar_init(&item_full[k], 1);
-      // released by every consumer warp (q read) and by its producer lane
-      // (done issuing)
-      mbar_init(&item_empty[k], 2 * CW);
+      // released by every consumer warp (q read), by its producer lane (done
+      // issuing) and by the merge warp (descriptor read)
+      mbar_init(&item_empty[k], 2 * CW + 1);
       mbar_init(&sched_full[k], 1);
     }
     mbar_init(merge_free, 1);
+    mbar_init(merge_full, CW);
     *abort_flag = 0;
-    *merge_cnt = 0;
     for (int w = 0; w < CW; ++w) issued_by[w] = 0;
     fence_mbar_init();
   }
@@ -1151,6 +1155,93 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
     return;
   }
 
+  if (warp == CW + 2) {
+    // ---------------------------------------------------------------- merger
+    // Per item, once every consumer warp has deposited its state: the item's
+    // rows out[g] = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w over the CW
+    // warps, written to `out` or as a split-K partial.  A warp of its own, so
+    // that no consumer falls behind the others by the merge.
+    for (uint32_t k = 0;; ++k) {
+      const int slot = k % kItemSlots;
+      if (!mbar_wait(&item_full[slot], (k / kItemSlots) & 1, p.wait_limit)) {
+        report(p.device_errors, PA_DEVERR_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      const ItemDesc d = desc[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[slot]);
+      if (d.b < 0 || *abort_flag) break;
+      bool ok = false;
+      for (uint32_t spin = 0; spin < p.wait_limit && !ok; ++spin) {
+        ok = mbar_try_wait(merge_full, k & 1);
+        if (*abort_flag) break;
+      }
+      if (!ok) {
+        if (!*abort_flag) {
+          report(p.device_errors, PA_DEVERR_TIMEOUT);
+          *abort_flag = 1;
+        }
+        break;
+      }
+      // out[g] = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w over the CW warps.
+      // The weights of every row first, then all rows' columns together, so
+      // that every row's loads are in flight at once.
+      float f[G][CW], inv[G], lse[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < CW; ++w) M = fmaxf(M, mml[(w * G + g) * 2]);
+        float lam = 0.f;
+#pragma unroll
+        for (int w = 0; w < CW; ++w) {
+          // a row with no visible token in this item (a new token before the
+          // item's first position) has M = -inf: it contributes nothing
+          f[g][w] = M == -INFINITY ? 0.f : fast_exp2(mml[(w * G + g) * 2] - M);
+          lam = fmaf(f[g][w], mml[(w * G + g) * 2 + 1], lam);
+        }
+        inv[g] = lam > 0.f ? 1.f / lam : 0.f;
+        lse[g] = lam > 0.f ? M + __log2f(lam) : -INFINITY;
+      }
+      const int64_t rows_per_seq = static_cast<int64_t>(p.q_len) * p.num_q_heads;
+#pragma unroll
+      for (int cp = lane; cp < D / 2; cp += 32) {
+        const int dcol = 2 * cp;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float o0 = 0.f, o1 = 0.f;
+#pragma unroll
+          for (int w = 0; w < CW; ++w) {
+            const float2 a = *reinterpret_cast<const float2*>(macc + (w * G + g) * D + dcol);
+            o0 = fmaf(f[g][w], a.x, o0);
+            o1 = fmaf(f[g][w], a.y, o1);
+          }
+          o0 *= inv[g];
+          o1 *= inv[g];
+          // row g = (new token j, head gi of the group): query row j * Hq + h * group + gi
+          const int qh = (g >> p.group_log2) * p.num_q_heads + d.h * p.group + (g & (p.group - 1));
+          if (d.single) {
+            const int64_t o = (static_cast<int64_t>(d.b) * rows_per_seq + qh) * D + dcol;
+            if constexpr (BF16) {
+              const uint32_t packed = f32_to_bf16_bits(o0) | (f32_to_bf16_bits(o1) << 16);
+              *reinterpret_cast<uint32_t*>(static_cast<char*>(p.out) + o * 2) = packed;
+            } else {
+              *reinterpret_cast<float2*>(static_cast<float*>(p.out) + o) = make_float2(o0, o1);
+            }
+          } else {
+            const int64_t row = static_cast<int64_t>(d.gchunk) * rows_per_seq + qh;
+            *reinterpret_cast<float2*>(p.part_out + row * D + dcol) = make_float2(o0, o1);
+            if (dcol == 0) p.part_lse[row] = lse[g];
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(merge_free);
+    }
+    return;
+  }
+
   // -------------------------------------------------------------- consumers
   Consumer cs;
   cs.init(lane, ps_all + warp * Tr::UT * G);
@@ -1230,79 +1321,17 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
       }
     }
 
-    // ---- hand this warp's state to the merge; the last of the 8 warps to
-    // arrive merges while the others go on with their next item
+    // ---- hand this warp's state to the merge warp; the warps go on with their
+    // next item while it merges (the buffer is free again once it has read it)
     if (item_k > 0 && !mbar_wait(merge_free, (item_k - 1) & 1, p.wait_limit)) {
       report(p.device_errors, PA_DEVERR_TIMEOUT);
       *abort_flag = 1;
       aborted = true;
     }
     cs.store(macc + warp * G * D, mml + warp * G * 2);
+    __threadfence_block();
     __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-      __threadfence_block();
-      last = atomicAdd(merge_cnt, 1) == CW - 1;
-      __threadfence_block();
-    }
-    last = __shfl_sync(kFull, last, 0);
-    if (last) {
-      if (lane == 0) *merge_cnt = 0;
-      // out[g] = sum_w 2^(m_w - M) acc_w / sum_w 2^(m_w - M) l_w over the CW warps.
-      // The weights of every row first, then all rows' columns together, so
-      // that the merging warp has every row's loads in flight at once.
-      float f[G][CW], inv[G], lse[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < CW; ++w) M = fmaxf(M, mml[(w * G + g) * 2]);
-        float lam = 0.f;
-#pragma unroll
-        for (int w = 0; w < CW; ++w) {
-          // a row with no visible token in this item (a new token before the
-          // item's first position) has M = -inf: it contributes nothing
-          f[g][w] = M == -INFINITY ? 0.f : fast_exp2(mml[(w * G + g) * 2] - M);
-          lam = fmaf(f[g][w], mml[(w * G + g) * 2 + 1], lam);
-        }
-        inv[g] = lam > 0.f ? 1.f / lam : 0.f;
-        lse[g] = lam > 0.f ? M + __log2f(lam) : -INFINITY;
-      }
-      const int64_t rows_per_seq = static_cast<int64_t>(p.q_len) * p.num_q_heads;
-#pragma unroll
-      for (int cp = lane; cp < D / 2; cp += 32) {
-        const int dcol = 2 * cp;
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float o0 = 0.f, o1 = 0.f;
-#pragma unroll
-          for (int w = 0; w < CW; ++w) {
-            const float2 a = *reinterpret_cast<const float2*>(macc + (w * G + g) * D + dcol);
-            o0 = fmaf(f[g][w], a.x, o0);
-            o1 = fmaf(f[g][w], a.y, o1);
-          }
-          o0 *= inv[g];
-          o1 *= inv[g];
-          // row g = (new token j, head gi of the group): query row j * Hq + h * group + gi
-          const int qh = (g >> p.group_log2) * p.num_q_heads + d.h * p.group + (g & (p.group - 1));
-          if (d.single) {
-            const int64_t o = (static_cast<int64_t>(d.b) * rows_per_seq + qh) * D + dcol;
-            if constexpr (BF16) {
-              const uint32_t packed = f32_to_bf16_bits(o0) | (f32_to_bf16_bits(o1) << 16);
-              *reinterpret_cast<uint32_t*>(static_cast<char*>(p.out) + o * 2) = packed;
-            } else {
-              *reinterpret_cast<float2*>(static_cast<float*>(p.out) + o) = make_float2(o0, o1);
-            }
-          } else {
-            const int64_t row = static_cast<int64_t>(d.gchunk) * rows_per_seq + qh;
-            *reinterpret_cast<float2*>(p.part_out + row * D + dcol) = make_float2(o0, o1);
-            if (dcol == 0) p.part_lse[row] = lse[g];
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(merge_free);
-    }
+    if (lane == 0) mbar_arrive(merge_full);
     ++item_k;
     if (aborted) break;
   }
