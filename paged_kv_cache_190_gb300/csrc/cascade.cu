@@ -58,7 +58,6 @@ static_assert(kMaxPieceSpan == 32, "the plan scores one candidate span per lane 
 struct PrefixMaps {
   CUtensorMap k, v, q;
 };
-constexpr int kCascadeMergeWarps = 8;
 static_assert(kInlineSuffixTokens <= 32, "the merge attends to a short suffix one token per lane");
 
 // Group of sequence b: the last f with group_start[f] <= b.
@@ -1016,32 +1015,28 @@ __global__ void __launch_bounds__(kPrefixThreads, 1) prefix_attention_kernel(
 }
 
 // ------------------------------------------------------------ merge
-// One warp per (sequence b, kv head h): the G = group query rows of h.  Each
-// row's partials c (the prefix pieces, then any decode-kernel chunks of its own
-// tokens) combine as
-//   out = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M),  M = max_c lse_c,
-// each lane owning CPL = head_dim / 32 columns.  A short own suffix
-// [inline_start[b], L_b) (at most 32 tokens) is one more term per row, computed
-// here: the suffix's tokens share the warp, LPT = 32 / (its length rounded up to
-// a power of two) lanes each (at most one 16-byte piece of the row per lane
-// and token fewer), every lane forming the G partial scores of its part of its
-// token's K row (q rows as fp32 in shared memory), summed over the token's
-// lanes; the base-2 softmax of each row runs over the tokens; the weighted sum
-// of V uses every token's V columns of this lane, all loaded up front.  Every load of the warp (pages,
-// then K, V and the partials) is issued before the arithmetic that needs it.
+// One warp per (sequence b, kv head h): the G = group query rows of h, each
+// lane owning CPL = head_dim / 32 columns of every row.  Every row keeps a
+// running base-2 softmax state (maximum M, weight sum S, weighted sum acc) into
+// which terms enter as (log-sum-exp, normalised value):
+//   out = sum_c 2^(lse_c - M) o_c / sum_c 2^(lse_c - M),  M = max_c lse_c.
+// Blocks are small (two warps) and registers few (at most 80 a thread up to 4
+// rows, no shared memory), so that the whole grid finds room on the SMs beside
+// the prefix kernel's blocks and waits there for it; everything that does not
+// depend on the prefix kernel is done before that wait: the attention over a
+// short own suffix [inline_start[b], L_b) (at most 32 tokens), token by token,
+// each a term of its own (lse = its score, o = its V row), its score summed
+// across the warp from each lane's columns.  After the wait the row's partials
+// c (the prefix pieces, then any decode-kernel chunks of its own tokens) join.
 // Rows with neither (L_b = 0) were zeroed by the plan.
+constexpr int kCascadeMergeWarps = 2;          // warps per block
 template <int CPL, int G>
-__global__ void __launch_bounds__(kCascadeMergeWarps * 32) cascade_merge_kernel(
+__global__ void __launch_bounds__(kCascadeMergeWarps * 32, G <= 4 ? 12 : 8) cascade_merge_kernel(
     const __grid_constant__ DecodeKernelParams p, const int32_t* __restrict__ chunk_base,
     const int32_t* __restrict__ inline_start, const int32_t* __restrict__ context_lens,
     int max_len, int num_seqs) {
+  using Cols = typename std::conditional<CPL == 4, uint2, uint32_t>::type;   // CPL bf16
   constexpr int D = CPL * 32;
-  constexpr int KV = D / 8;                     // 16-byte pieces of a row
-  __shared__ __align__(16) float q_s[kCascadeMergeWarps][G * D];
-  // Launched as a programmatic dependent of the prefix kernel, which lets it
-  // start early: the plan's arrays, q and the suffix's pages are complete
-  // already (the plan ran before the prefix kernel's own wait returned), so
-  // they are loaded first; only the partials wait for the prefix kernel.
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int Hq = p.num_q_heads, Hkv = p.num_kv_heads;
   const int64_t item = static_cast<int64_t>(blockIdx.x) * kCascadeMergeWarps + warp;
@@ -1062,50 +1057,6 @@ __global__ void __launch_bounds__(kCascadeMergeWarps * 32) cascade_merge_kernel(
   const int L = s0 >= 0 ? min(max(context_lens[b], 0), max_len) : 0;
   const int nsuf = s0 >= 0 ? min(L - s0, 32) : 0;
   const int64_t row0 = static_cast<int64_t>(b) * Hq + h * G;   // first output row
-  // ---- the G q rows -> shared memory as fp32
-  if (nsuf > 0) {
-    const uint4* qsrc = reinterpret_cast<const uint4*>(p.q) + row0 * KV;
-    float4* qdst = reinterpret_cast<float4*>(q_s[warp]);
-    for (int e = lane; e < G * KV; e += 32) {
-      const uint4 w = qsrc[e];
-      qdst[2 * e] = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
-      qdst[2 * e + 1] = make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
-    }
-  }
-  // ---- this lane's token (LPT lanes per token), its page and its part of the K row
-  int p2 = 1;
-  while (p2 < nsuf) p2 <<= 1;
-  const int lpt = min(32 / p2, KV);              // lanes per token
-  const int per = KV / lpt;                      // 16-byte pieces per lane
-  const int tok = lane / lpt, part = lane - tok * lpt;
-  int page = -1;
-  if (tok < nsuf) {
-    const int t = s0 + tok;
-    page = p.block_tables[static_cast<int64_t>(b) * p.max_blocks_per_seq + t / bs];
-    if (page < 0 || page >= p.num_blocks) {
-      if (part == 0) report(p.device_errors, PA_DEVERR_BAD_BLOCK);
-      page = -1;
-    }
-  }
-  const int64_t kv_row =
-      page >= 0 ? ((static_cast<int64_t>(page) * Hkv + h) * bs + (s0 + tok) % bs) * D : 0;
-  uint4 kr[KV];
-#pragma unroll
-  for (int e = 0; e < KV; ++e)
-    kr[e] = page >= 0 && e < per
-                ? reinterpret_cast<const uint4*>(p.k_cache + kv_row * 2)[part * per + e]
-                : make_uint4(0, 0, 0, 0);
-  // ---- this lane's V columns of every token (token j's row from its first lane)
-  using VCols = typename std::conditional<CPL == 4, uint2, uint32_t>::type;
-  VCols vr[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const int64_t rj = __shfl_sync(kFull, kv_row, j < nsuf ? j * lpt : 0);
-    vr[j] = j < nsuf ? *reinterpret_cast<const VCols*>(p.v_cache + (rj + lane * CPL) * 2)
-                     : VCols{};
-  }
-  wait_prior_grids();                           // every partial is written
-  // ---- the partials of the G rows
   float M[G], S[G], acc[G][CPL];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -1114,6 +1065,7 @@ __global__ void __launch_bounds__(kCascadeMergeWarps * 32) cascade_merge_kernel(
 #pragma unroll
     for (int k = 0; k < CPL; ++k) acc[g][k] = 0.f;
   }
+  // one more term (lse, v) of row g
   auto add = [&](int g, float lse, const float* v) {
     const float Mn = fmaxf(M[g], lse);
     const float sc = fast_exp2(M[g] - Mn);
@@ -1123,116 +1075,81 @@ __global__ void __launch_bounds__(kCascadeMergeWarps * 32) cascade_merge_kernel(
     for (int k = 0; k < CPL; ++k) acc[g][k] = fmaf(acc[g][k], sc, w * v[k]);
     M[g] = Mn;
   };
-  // Each row's largest log-sum-exp first (lane i takes the (partial, row)
-  // entries i, i + 32, ...: row i % G, as 32 is a multiple of G), so that the
-  // weighted sum below has no chain from one partial to the next.
-  if (n > 0) {
-    float mloc = kNoScore;
-    for (int i = lane; i < n * G; i += 32)
-      mloc = fmaxf(mloc, p.part_lse[(static_cast<int64_t>(c0) + i / G) * Hq + h * G + i % G]);
-    for (int o2 = 16; o2 >= G; o2 >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, o2));
+  auto unpack = [](Cols c, float* f) {
+    if constexpr (CPL == 4) {
+      f[0] = bf16_lo(c.x); f[1] = bf16_hi(c.x); f[2] = bf16_lo(c.y); f[3] = bf16_hi(c.y);
+    } else {
+      f[0] = bf16_lo(c); f[1] = bf16_hi(c);
+    }
+  };
+  if (nsuf > 0) {
+    Cols qc[G];                                 // this lane's columns of the G q rows
 #pragma unroll
-    for (int g = 0; g < G; ++g) M[g] = __shfl_sync(kFull, mloc, g);   // lane g holds row g's
-#pragma unroll 4
-    for (int cc = 0; cc < n; ++cc) {
-      const int64_t prow = (static_cast<int64_t>(c0) + cc) * Hq + h * G;
+    for (int g = 0; g < G; ++g)
+      qc[g] = *reinterpret_cast<const Cols*>(p.q + ((row0 + g) * D + lane * CPL) * 2);
+    // lane j: the pool row of suffix token j (-1: its page is unreadable)
+    int64_t kv_row = -1;
+    if (lane < nsuf) {
+      const int t = s0 + lane;
+      const int page = p.block_tables[static_cast<int64_t>(b) * p.max_blocks_per_seq + t / bs];
+      if (page < 0 || page >= p.num_blocks)
+        report(p.device_errors, PA_DEVERR_BAD_BLOCK);
+      else
+        kv_row = ((static_cast<int64_t>(page) * Hkv + h) * bs + t % bs) * D;
+    }
+    // token by token, the loads of two tokens issued together
+    for (int t0 = 0; t0 < nsuf; t0 += 2) {
+      Cols kc[2], vc[2];
+      int64_t rr[2];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float* src = p.part_out + (prow + g) * D + lane * CPL;
-        const float w = fast_exp2(p.part_lse[prow + g] - M[g]);   // 0 for an empty partial
-        float v[CPL];
-        if constexpr (CPL == 4) {
-          const float4 t4 = *reinterpret_cast<const float4*>(src);
-          v[0] = t4.x; v[1] = t4.y; v[2] = t4.z; v[3] = t4.w;
-        } else {
-          const float2 t2 = *reinterpret_cast<const float2*>(src);
-          v[0] = t2.x; v[1] = t2.y;
+      for (int j = 0; j < 2; ++j) {
+        rr[j] = __shfl_sync(kFull, kv_row, min(t0 + j, 31));
+        if (t0 + j >= nsuf) rr[j] = -1;
+        kc[j] = rr[j] >= 0 ? *reinterpret_cast<const Cols*>(p.k_cache + (rr[j] + lane * CPL) * 2)
+                           : Cols{};
+        vc[j] = rr[j] >= 0 ? *reinterpret_cast<const Cols*>(p.v_cache + (rr[j] + lane * CPL) * 2)
+                           : Cols{};
+      }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        if (rr[j] < 0) continue;                // uniform over the warp
+        float kf[CPL], vf[CPL], d[G];
+        unpack(kc[j], kf);
+        unpack(vc[j], vf);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float qf[CPL];
+          unpack(qc[g], qf);
+          d[g] = 0.f;
+#pragma unroll
+          for (int k = 0; k < CPL; ++k) d[g] = fmaf(qf[k], kf[k], d[g]);
         }
-        S[g] += w;
 #pragma unroll
-        for (int k = 0; k < CPL; ++k) acc[g][k] = fmaf(w, v[k], acc[g][k]);
+        for (int o2 = 16; o2 > 0; o2 >>= 1)
+#pragma unroll
+          for (int g = 0; g < G; ++g) d[g] += __shfl_xor_sync(kFull, d[g], o2);
+#pragma unroll
+        for (int g = 0; g < G; ++g) add(g, d[g] * p.scale_log2, vf);
       }
     }
   }
-  // ---- the suffix term of each row
-  if (nsuf > 0) {
-    __syncwarp();
-    float s[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) s[g] = 0.f;
-    const float4* qv = reinterpret_cast<const float4*>(q_s[warp]);
-#pragma unroll
-    for (int e = 0; e < KV; ++e) {
-      if (e < per) {                              // uniform over the warp
-        const uint4 kk = kr[e];
-        const float k0 = bf16_lo(kk.x), k1 = bf16_hi(kk.x), k2 = bf16_lo(kk.y), k3 = bf16_hi(kk.y);
-        const float k4 = bf16_lo(kk.z), k5 = bf16_hi(kk.z), k6 = bf16_lo(kk.w), k7 = bf16_hi(kk.w);
-        const int ci = part * per + e;            // 16-byte piece of the row: 8 columns
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float4 qa = qv[(g * D) / 4 + 2 * ci], qb = qv[(g * D) / 4 + 2 * ci + 1];
-          float d = s[g];
-          d = fmaf(qa.x, k0, d);
-          d = fmaf(qa.y, k1, d);
-          d = fmaf(qa.z, k2, d);
-          d = fmaf(qa.w, k3, d);
-          d = fmaf(qb.x, k4, d);
-          d = fmaf(qb.y, k5, d);
-          d = fmaf(qb.z, k6, d);
-          d = fmaf(qb.w, k7, d);
-          s[g] = d;
-        }
-      }
-    }
-    // the token's score: the sum over its lanes
-    for (int o2 = 1; o2 < lpt; o2 <<= 1)
-#pragma unroll
-      for (int g = 0; g < G; ++g) s[g] += __shfl_xor_sync(kFull, s[g], o2);
-    float pj[G], mx[G], l[G];
+  wait_prior_grids();                           // every partial is written
+  // ---- the partials, each (lse, normalised rows) a term of its row
+#pragma unroll 2
+  for (int cc = 0; cc < n; ++cc) {
+    const int64_t prow = (static_cast<int64_t>(c0) + cc) * Hq + h * G;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      const float sg = page >= 0 ? s[g] * p.scale_log2 : -INFINITY;
-      float m = sg;
-#pragma unroll
-      for (int o2 = 16; o2 > 0; o2 >>= 1) m = fmaxf(m, __shfl_xor_sync(kFull, m, o2));
-      mx[g] = m;
-      pj[g] = m > -INFINITY ? fast_exp2(sg - m) : 0.f;
-      float t = part == 0 ? pj[g] : 0.f;          // each token once
-#pragma unroll
-      for (int o2 = 16; o2 > 0; o2 >>= 1) t += __shfl_xor_sync(kFull, t, o2);
-      l[g] = t;
-    }
-    float o[G][CPL];
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int k = 0; k < CPL; ++k) o[g][k] = 0.f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      if (j < nsuf) {                           // uniform over the warp
-        float v[CPL];
-        if constexpr (CPL == 4) {
-          v[0] = bf16_lo(vr[j].x); v[1] = bf16_hi(vr[j].x);
-          v[2] = bf16_lo(vr[j].y); v[3] = bf16_hi(vr[j].y);
-        } else {
-          v[0] = bf16_lo(vr[j]); v[1] = bf16_hi(vr[j]);
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float w = __shfl_sync(kFull, pj[g], j * lpt);   // 0 for an unreadable token
-#pragma unroll
-          for (int k = 0; k < CPL; ++k) o[g][k] = fmaf(w, w != 0.f ? v[k] : 0.f, o[g][k]);
-        }
+      const float* src = p.part_out + (prow + g) * D + lane * CPL;
+      float v[CPL];
+      if constexpr (CPL == 4) {
+        const float4 t4 = *reinterpret_cast<const float4*>(src);
+        v[0] = t4.x; v[1] = t4.y; v[2] = t4.z; v[3] = t4.w;
+      } else {
+        const float2 t2 = *reinterpret_cast<const float2*>(src);
+        v[0] = t2.x; v[1] = t2.y;
       }
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      if (l[g] > 0.f) {
-        const float inv = 1.f / l[g];
-#pragma unroll
-        for (int k = 0; k < CPL; ++k) o[g][k] *= inv;
-        add(g, mx[g] + __log2f(l[g]), o[g]);
-      }
+      add(g, p.part_lse[prow + g], v);          // -inf (an empty partial): weight 0
     }
   }
 #pragma unroll
@@ -1326,18 +1243,24 @@ cudaError_t launch_cascade_prefix(const DecodeArgs& a, const DecodeKernelParams&
   return cudaErrorInvalidValue;
 }
 
+template <int CPL, int G>
+cudaError_t launch_merge_instance(const DecodeArgs& a, const DecodeKernelParams& kp,
+                                  unsigned blocks, cudaStream_t stream) {
+  return launch_pdl(cascade_merge_kernel<CPL, G>, blocks, kCascadeMergeWarps * 32, 0, stream, kp,
+                    static_cast<const int32_t*>(a.ws.chunk_base),
+                    static_cast<const int32_t*>(a.ws.inline_start), a.context_lens,
+                    a.max_context_len, a.num_seqs);
+}
+
 cudaError_t launch_cascade_merge(const DecodeArgs& a, const DecodeKernelParams& kp,
                                  cudaStream_t stream) {
   const int64_t items = static_cast<int64_t>(a.num_seqs) * a.num_kv_heads;
   const unsigned blocks =
       static_cast<unsigned>((items + kCascadeMergeWarps - 1) / kCascadeMergeWarps);
   const int group = a.num_q_heads / a.num_kv_heads;
-#define PA_MERGE(CPL_, G_)                                                                   \
-  if (a.head_dim == CPL_ * 32 && group == G_)                                               \
-    return launch_pdl(cascade_merge_kernel<CPL_, G_>, blocks, kCascadeMergeWarps * 32, 0, stream, \
-                      kp, static_cast<const int32_t*>(a.ws.chunk_base),                     \
-                      static_cast<const int32_t*>(a.ws.inline_start), a.context_lens,        \
-                      a.max_context_len, a.num_seqs);
+#define PA_MERGE(CPL_, G_)                                    \
+  if (a.head_dim == CPL_ * 32 && group == G_)                \
+    return launch_merge_instance<CPL_, G_>(a, kp, blocks, stream);
   PA_MERGE(4, 1) PA_MERGE(4, 2) PA_MERGE(4, 4) PA_MERGE(4, 8)
   PA_MERGE(2, 1) PA_MERGE(2, 2) PA_MERGE(2, 4) PA_MERGE(2, 8)
 #undef PA_MERGE
