@@ -33,7 +33,7 @@
 namespace pa {
 namespace {
 
-constexpr int kCascadePlanThreads = 1024;
+constexpr int kCascadePlanThreads = 1024;               // the plan's largest block
 constexpr int kPlanGroupCache = 2048;                   // groups the plan keeps in shared memory
 constexpr int kPrefixSoftmaxWarps = 4;                  // one TMEM lane quadrant each
 // softmax warps, as many epilogue warps, two producer warps (K, V) and two MMA
@@ -70,9 +70,11 @@ __device__ __forceinline__ int group_of(const int32_t* group_start, int num_grou
   return lo;
 }
 
-// Block-wide exclusive scan of one value per thread (kCascadePlanThreads); the
+// Block-wide exclusive scan of one value per thread (THREADS of them); the
 // total lands in *total.
+template <int THREADS>
 __device__ __forceinline__ int block_scan(int x, int* warp_sums, int* total) {
+  constexpr int NW = THREADS / 32;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int incl = x;
 #pragma unroll
@@ -83,17 +85,17 @@ __device__ __forceinline__ int block_scan(int x, int* warp_sums, int* total) {
   if (lane == 31) warp_sums[warp] = incl;
   __syncthreads();
   if (warp == 0) {
-    int w = warp_sums[lane];
+    int w = lane < NW ? warp_sums[lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += y;
     }
-    warp_sums[lane] = w;
+    if (lane < NW) warp_sums[lane] = w;
   }
   __syncthreads();
   const int excl = incl - x + (warp > 0 ? warp_sums[warp - 1] : 0);
-  if (threadIdx.x == kCascadePlanThreads - 1) *total = excl + x;
+  if (threadIdx.x == THREADS - 1) *total = excl + x;
   __syncthreads();
   return excl;
 }
@@ -134,8 +136,9 @@ __device__ __forceinline__ PrefixShape prefix_shape(int sl, int members, int gro
 
 // One block.
 //  1. Groups: the prefix work (stages x row sets x kv heads) is cut into pieces
-//     of `span` stages, span chosen so that the prefix kernel's CTAs get about
-//     two items each; the item list holds (group, row set, piece, span).
+//     of `span` stages, span chosen so that the busiest prefix CTA's stages
+//     (with a per-item overhead) are fewest; an item holds the group's shared
+//     length, leader and member count, and its piece, row set and span.
 //  2. Sequences: b has p_b prefix partials (its group's pieces when its shared
 //     length is valid for it, else 0) and then its own tokens [start_b, L_b):
 //     up to kInlineSuffixTokens of them are left to the merge (inline_start[b]
@@ -144,7 +147,8 @@ __device__ __forceinline__ PrefixShape prefix_shape(int sl, int members, int gro
 //     partial of b.  Checks: a shared length that is not whole pages or not
 //     below a member's length sets PA_DEVERR_BAD_LENGTH, and that member is
 //     decoded without the sharing.
-__global__ void __launch_bounds__(kCascadePlanThreads) cascade_plan_kernel(
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) cascade_plan_kernel(
     const int32_t* __restrict__ context_lens, const int32_t* group_start,
     const int32_t* shared_lens, int num_groups, int num_seqs, int chunk_tokens,
     int max_len, int block_size, int max_blocks_per_seq, int group, int num_kv_heads,
@@ -152,19 +156,21 @@ __global__ void __launch_bounds__(kCascadePlanThreads) cascade_plan_kernel(
     int32_t* __restrict__ prefix_parts, int32_t* __restrict__ inline_start,
     int4* __restrict__ work, int4* __restrict__ prefix_items, uint4* __restrict__ out,
     int64_t row_chunks, int32_t* device_errors) {
-  __shared__ int warp_sums[kCascadePlanThreads / 32];
+  __shared__ int warp_sums[THREADS / 32];
   __shared__ int total_s;
   __shared__ int carry_parts, carry_work, carry_items, units_s;
   __shared__ unsigned span_items[kMaxPieceSpan + 1];
   __shared__ int32_t gs_cache[kPlanGroupCache + 1], sl_cache[kPlanGroupCache];
   allow_next_grid();                      // the next kernel may start its prologue
+  // the first sequences' lengths, loaded now: they are needed last
+  const int len_first = threadIdx.x < num_seqs ? context_lens[threadIdx.x] : 0;
   if (threadIdx.x == 0) carry_parts = carry_work = carry_items = units_s = 0;
   // the group arrays are read many times (a binary search per sequence): keep
   // them in shared memory when they fit
   const bool cached = num_groups <= kPlanGroupCache;
   if (cached) {
-    for (int i = threadIdx.x; i <= num_groups; i += kCascadePlanThreads) gs_cache[i] = group_start[i];
-    for (int i = threadIdx.x; i < num_groups; i += kCascadePlanThreads) sl_cache[i] = shared_lens[i];
+    for (int i = threadIdx.x; i <= num_groups; i += THREADS) gs_cache[i] = group_start[i];
+    for (int i = threadIdx.x; i < num_groups; i += THREADS) sl_cache[i] = shared_lens[i];
     group_start = gs_cache;
     shared_lens = sl_cache;
   }
@@ -172,13 +178,13 @@ __global__ void __launch_bounds__(kCascadePlanThreads) cascade_plan_kernel(
   // ---- 1a. the piece length: for every candidate span (stages per piece) the
   // items it makes, then the span whose busiest CTA (items per CTA x (span +
   // the per-item overhead, in stages)) finishes first
-  for (int i = threadIdx.x; i <= kMaxPieceSpan; i += kCascadePlanThreads) span_items[i] = 0;
+  for (int i = threadIdx.x; i <= kMaxPieceSpan; i += THREADS) span_items[i] = 0;
   __syncthreads();
   {
-    // warp w takes groups w, w + 32, ...; lane c - 1 counts candidate c's items
+    // warp w takes groups w, w + (warps), ...; lane c - 1 counts candidate c's items
     const int c = (threadIdx.x & 31) + 1;
     unsigned acc = 0;
-    for (int f = threadIdx.x >> 5; f < num_groups; f += kCascadePlanThreads / 32) {
+    for (int f = threadIdx.x >> 5; f < num_groups; f += THREADS / 32) {
       const int sl = usable_shared(shared_lens, f, block_size, max_blocks_per_seq, max_len);
       const int2 m = members_of(group_start, f, num_seqs);
       const PrefixShape s1 = prefix_shape(sl, m.y - m.x, group, 1);
@@ -213,30 +219,35 @@ __global__ void __launch_bounds__(kCascadePlanThreads) cascade_plan_kernel(
   __syncthreads();
   const int span = units_s;
   // ---- 1b. the item list
-  for (int base = 0; base < num_groups; base += kCascadePlanThreads) {
+  for (int base = 0; base < num_groups; base += THREADS) {
     const int f = base + threadIdx.x;
     PrefixShape s{0, 0, 1, 0};
+    int sl = 0;
+    int2 m = make_int2(0, 0);
     if (f < num_groups) {
-      const int sl = usable_shared(shared_lens, f, block_size, max_blocks_per_seq, max_len);
-      const int2 m = members_of(group_start, f, num_seqs);
+      sl = usable_shared(shared_lens, f, block_size, max_blocks_per_seq, max_len);
+      m = members_of(group_start, f, num_seqs);
       s = prefix_shape(sl, m.y - m.x, group, span);
     }
     const int n = s.rowsets * s.pieces;
-    const int first = block_scan(n, warp_sums, &total_s);
+    const int first = block_scan<THREADS>(n, warp_sums, &total_s);
     const int tot = total_s;
+    // an item carries what its producer needs, so that it starts with one load:
+    // {shared length, leader, members | piece << 24, row set | span << 16}
     for (int i = 0; i < n; ++i)
-      prefix_items[carry_items + first + i] = make_int4(f, i / s.pieces, i % s.pieces, s.span);
+      prefix_items[carry_items + first + i] =
+          make_int4(sl, m.x, (m.y - m.x) | ((i % s.pieces) << 24), (i / s.pieces) | (s.span << 16));
     __syncthreads();
     if (threadIdx.x == 0) carry_items += tot;
     __syncthreads();
   }
   // ---- 2. sequences
-  for (int base = 0; base < num_seqs; base += kCascadePlanThreads) {
+  for (int base = 0; base < num_seqs; base += THREADS) {
     const int b = base + threadIdx.x;
     int L = 0, start = 0, pb = 0, nb = 0;
     bool inl = false;
     if (b < num_seqs) {
-      L = context_lens[b];
+      L = base == 0 ? len_first : context_lens[b];
       if (L < 0 || L > max_len) {
         report(device_errors, PA_DEVERR_BAD_LENGTH);
         L = L < 0 ? 0 : max_len;
@@ -262,9 +273,9 @@ __global__ void __launch_bounds__(kCascadePlanThreads) cascade_plan_kernel(
         nb = inl ? 0 : (L - start + chunk_tokens - 1) / chunk_tokens;
       }
     }
-    const int parts = block_scan(pb + nb, warp_sums, &total_s);
+    const int parts = block_scan<THREADS>(pb + nb, warp_sums, &total_s);
     const int tparts = total_s;
-    const int wk = block_scan(nb, warp_sums, &total_s);
+    const int wk = block_scan<THREADS>(nb, warp_sums, &total_s);
     const int twork = total_s;
     if (b < num_seqs) {
       const int first = carry_parts + parts;
@@ -465,9 +476,8 @@ struct PrefixMeta {
 template <int D>
 __global__ void __launch_bounds__(kPrefixThreads, 1) prefix_attention_kernel(
     const __grid_constant__ DecodeKernelParams p, const __grid_constant__ PrefixMaps maps,
-    const int32_t* __restrict__ group_start, const int32_t* __restrict__ shared_lens,
     const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ prefix_parts,
-    const int4* __restrict__ items, int num_seqs) {
+    const int4* __restrict__ items) {
   using Ly = PrefixLayout<D>;
   constexpr int NK = kPrefixKStages, NV = kPrefixVStages;
   constexpr int NM = kPrefixMetaSlots;
@@ -602,11 +612,12 @@ __global__ void __launch_bounds__(kPrefixThreads, 1) prefix_attention_kernel(
     for (int it = blockIdx.x; it < n_items && ok; it += gridDim.x, ++ic) {
       const int4 item = items[it / Hkv];
       const int h = it % Hkv;
-      const int sl = shared_lens[item.x];
-      const int2 mem = members_of(group_start, item.x, num_seqs);
+      const int sl = item.x;
+      const int2 mem = make_int2(item.y, item.y + (item.z & 0xFFFFFF));
+      const int piece = item.z >> 24, rowset = item.w & 0xFFFF, span = item.w >> 16;
       const int32_t* table = p.block_tables + static_cast<int64_t>(mem.x) * p.max_blocks_per_seq;
       const int stages = (sl + kPrefixStageTokens - 1) / kPrefixStageTokens;
-      const int st0 = item.z * item.w, st1 = min(st0 + item.w, stages);
+      const int st0 = piece * span, st1 = min(st0 + span, stages);
       // the item's description, then its q rows
       bool waited = true;
       if (lane == 0) {
@@ -616,18 +627,18 @@ __global__ void __launch_bounds__(kPrefixThreads, 1) prefix_attention_kernel(
           PrefixMeta mt;
           mt.sl = sl;
           mt.st01 = st0 | (st1 << 16);
-          mt.rows = min((mem.y - mem.x) * G - item.y * kPrefixRows, kPrefixRows);
-          mt.base = item.y * kPrefixRows | (h << 24);
+          mt.rows = min((mem.y - mem.x) * G - rowset * kPrefixRows, kPrefixRows);
+          mt.base = rowset * kPrefixRows | (h << 24);
           mt.leader = mem.x;
           mt.members = mem.y;
-          mt.piece = item.z;
+          mt.piece = piece;
           mt.pad = 0;
           meta[ic % NM] = mt;
           mbar_arrive(&meta_full[ic % NM]);
           uint64_t* qb = &q_full[ic & 1];
           mbar_arrive_expect_tx(qb, Ly::Q_BYTES);
           unsigned char* qdst = smem + Ly::OFF_Q + (ic & 1) * Ly::Q_BYTES;
-          const int m0 = mem.x + item.y * kPrefixRows / G;
+          const int m0 = mem.x + rowset * kPrefixRows / G;
           // row set row rr = 16 quadrant + i lands in MMA rows 32 quadrant + i
           // and 32 quadrant + 16 + i: each a box of the quadrant's 16 / group
           // members (16 rows x 128 bytes)
@@ -1214,11 +1225,9 @@ cudaError_t run_prefix(const DecodeArgs& a, const DecodeKernelParams& kp, int de
   // blocks wait on the device for both, i.e. for the item list
   return launch_pdl(prefix_attention_kernel<D>, static_cast<unsigned>(prefix_grid(a.num_sms)),
                     kPrefixThreads, Ly::SMEM, stream, kp, maps,
-                    static_cast<const int32_t*>(a.group_start),
-                    static_cast<const int32_t*>(a.shared_lens),
                     static_cast<const int32_t*>(a.ws.chunk_base),
                     static_cast<const int32_t*>(a.ws.prefix_parts),
-                    static_cast<const int4*>(a.ws.prefix_items), a.num_seqs);
+                    static_cast<const int4*>(a.ws.prefix_items));
 }
 
 }  // namespace
@@ -1226,13 +1235,25 @@ cudaError_t run_prefix(const DecodeArgs& a, const DecodeKernelParams& kp, int de
 int prefix_grid(int num_sms) { return (num_sms > 0 ? num_sms : 1) * kPrefixCtasPerSm; }
 
 cudaError_t launch_cascade_plan(const DecodeArgs& a, cudaStream_t stream) {
+  // the item fields are packed: a group's members < 2^24 and row sets < 2^16,
+  // a piece's stages < 2^16
+  if (a.num_seqs >= (1 << 19) || a.max_context_len >= (1 << 27)) return cudaErrorInvalidValue;
   const int64_t row_chunks = static_cast<int64_t>(a.num_q_heads) * a.head_dim * 2 / 16;
-  cascade_plan_kernel<<<1, kCascadePlanThreads, 0, stream>>>(
-      a.context_lens, a.group_start, a.shared_lens, a.num_groups, a.num_seqs, a.chunk_tokens,
-      a.max_context_len, a.block_size, a.max_blocks_per_seq, a.num_q_heads / a.num_kv_heads,
-      a.num_kv_heads, prefix_grid(a.num_sms), a.ws.header, a.ws.chunk_base, a.ws.prefix_parts,
-      a.ws.inline_start, a.ws.work, a.ws.prefix_items, static_cast<uint4*>(a.out), row_chunks,
-      a.device_errors);
+  // the smallest block that takes every sequence and group in one pass (its
+  // block-wide scans and barriers cost less with fewer warps)
+  const int n = a.num_seqs > a.num_groups ? a.num_seqs : a.num_groups;
+  auto run = [&](auto kernel, int threads) {
+    kernel<<<1, threads, 0, stream>>>(
+        a.context_lens, a.group_start, a.shared_lens, a.num_groups, a.num_seqs, a.chunk_tokens,
+        a.max_context_len, a.block_size, a.max_blocks_per_seq, a.num_q_heads / a.num_kv_heads,
+        a.num_kv_heads, prefix_grid(a.num_sms), a.ws.header, a.ws.chunk_base, a.ws.prefix_parts,
+        a.ws.inline_start, a.ws.work, a.ws.prefix_items, static_cast<uint4*>(a.out), row_chunks,
+        a.device_errors);
+  };
+  if (n <= 128) run(cascade_plan_kernel<128>, 128);
+  else if (n <= 256) run(cascade_plan_kernel<256>, 256);
+  else if (n <= 512) run(cascade_plan_kernel<512>, 512);
+  else run(cascade_plan_kernel<kCascadePlanThreads>, kCascadePlanThreads);
   return cudaGetLastError();
 }
 

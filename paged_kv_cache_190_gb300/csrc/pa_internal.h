@@ -29,7 +29,8 @@ struct DecodeWorkspace {
   float* part_out;       // [max_chunks][num_q_heads][head_dim] chunk output, normalised
   unsigned char* q8;     // fp8 caches: [num_seqs * num_q_heads][2 * head_dim + 16] prepared q
   int32_t* prefix_parts; // cascade: [num_seqs] prefix partials of each sequence
-  int4* prefix_items;    // cascade: (group, row set, piece, stages per piece)
+  int4* prefix_items;    // cascade: {shared length, leader, members | piece << 24,
+                         //           row set | stages per piece << 16}
   int32_t* inline_start; // cascade: [num_seqs] first own token the merge attends to, or -1
   int64_t max_chunks;
 };

@@ -215,6 +215,21 @@ def test_more_groups_than_the_plan_caches():
     check_tolerance(out_as_f64(out), _oracle(case), "bf16", case.name)
 
 
+@pytest.mark.parametrize("num_seqs", [129, 257, 513])
+def test_plan_block_sizes(num_seqs):
+    """The plan runs with the smallest block (128, 256, 512 or 1024 threads)
+    that takes every sequence and group in one pass: batches just past each
+    step, in groups of eight sharing two pages, the last group partial."""
+    rng = np.random.default_rng(1330 + num_seqs)
+    sizes = [8] * (num_seqs // 8) + ([num_seqs % 8] if num_seqs % 8 else [])
+    lens = [32 + int(x) for x in rng.integers(1, 40, size=num_seqs)]
+    case, starts, shared = _grouped_case(f"cascade-plan-{num_seqs}", 1330 + num_seqs, 8, 4, 64, 16,
+                                         lens, sizes, [32] * len(sizes))
+    out, flags, _ = _cascade(case, starts, shared)
+    assert flags == 0
+    check_tolerance(out_as_f64(out), _oracle(case), "bf16", case.name)
+
+
 @pytest.mark.parametrize("limit", [0, 64])
 def test_expired_waits_in_the_prefix_kernel_leave_the_context_usable(limit):
     """The shared-prefix kernel's pipeline waits (TMA rings, tensor-core
