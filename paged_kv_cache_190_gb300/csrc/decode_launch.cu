@@ -17,7 +17,7 @@
 namespace pa {
 namespace {
 
-constexpr int kPlanThreads = 1024;
+constexpr int kPlanThreads = 1024;          // the plan's largest block
 constexpr int kQPrepWarps = 8;
 
 // q preparation of the fp8-cache decode (head_dim 128): each bf16 row q[b][i]
@@ -60,24 +60,28 @@ __global__ void __launch_bounds__(kQPrepWarps * 32) q_prep_fp8_kernel(
 
 // Lists every (sequence, chunk) pair in sequence order, records where each
 // sequence's chunks start, resets the work counter and writes zero rows for
-// empty sequences.  One block; sequences are taken 1024 at a time: a block scan
-// gives each sequence's first chunk, then all threads fill the tile's entries
-// together (entry -> sequence by binary search over the tile's offsets).
-__global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(
+// empty sequences.  One block of THREADS (the smallest of 128 .. 1024 that
+// covers the batch: its barriers and scans cost less with fewer warps);
+// sequences are taken THREADS at a time: a block scan gives each sequence's
+// first chunk, then all threads fill the tile's entries together (entry ->
+// sequence by binary search over the tile's offsets).
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) decode_plan_kernel(
     const int32_t* __restrict__ context_lens, int num_seqs, int chunk_tokens, int max_len,
     int q_len, int32_t* __restrict__ header, int32_t* __restrict__ chunk_base,
     int4* __restrict__ work, uint4* __restrict__ out, int64_t row_chunks,
     int32_t* device_errors) {
-  __shared__ int warp_sums[kPlanThreads / 32];
-  __shared__ int first_s[kPlanThreads + 1];     // tile-local exclusive offsets (+ total)
-  __shared__ int len_s[kPlanThreads];
+  constexpr int NW = THREADS / 32;
+  __shared__ int warp_sums[NW];
+  __shared__ int first_s[THREADS + 1];          // tile-local exclusive offsets (+ total)
+  __shared__ int len_s[THREADS];
   __shared__ int carry_s;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   allow_next_grid();                      // the decode kernel may start its prologue
   if (threadIdx.x == 0) carry_s = 0;
   __syncthreads();
-  for (int base = 0; base < num_seqs; base += kPlanThreads) {
+  for (int base = 0; base < num_seqs; base += THREADS) {
     const int b = base + threadIdx.x;
     int L = 0, n = 0;
     if (b < num_seqs) {
@@ -99,29 +103,29 @@ __global__ void __launch_bounds__(kPlanThreads) decode_plan_kernel(
     if (lane == 31) warp_sums[warp] = x;
     __syncthreads();
     if (warp == 0) {
-      int w = warp_sums[lane];
+      int w = lane < NW ? warp_sums[lane] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
         const int y = __shfl_up_sync(0xffffffffu, w, o);
         if (lane >= o) w += y;
       }
-      warp_sums[lane] = w;
+      if (lane < NW) warp_sums[lane] = w;
     }
     __syncthreads();
     const int excl = x - n + (warp > 0 ? warp_sums[warp - 1] : 0);
     const int carry = carry_s;
     first_s[threadIdx.x] = excl;
     len_s[threadIdx.x] = L;
-    if (threadIdx.x == kPlanThreads - 1) first_s[kPlanThreads] = excl + n;
+    if (threadIdx.x == THREADS - 1) first_s[THREADS] = excl + n;
     if (b < num_seqs) {
       chunk_base[b] = carry + excl;
       if (L == 0)
         for (int64_t k = 0; k < row_chunks; ++k) out[b * row_chunks + k] = make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
-    const int tile_total = first_s[kPlanThreads];
-    for (int e = threadIdx.x; e < tile_total; e += kPlanThreads) {
-      int lo = 0, hi = kPlanThreads - 1;          // last t with first_s[t] <= e
+    const int tile_total = first_s[THREADS];
+    for (int e = threadIdx.x; e < tile_total; e += THREADS) {
+      int lo = 0, hi = THREADS - 1;          // last t with first_s[t] <= e
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (first_s[mid] <= e) lo = mid; else hi = mid - 1;
@@ -437,9 +441,16 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t stream) {
   if (cascade) {
     e = launch_cascade_plan(a, stream);
   } else {
-    decode_plan_kernel<<<1, kPlanThreads, 0, stream>>>(
-        a.context_lens, a.num_seqs, a.chunk_tokens, a.max_context_len, a.q_len, a.ws.header,
-        a.ws.chunk_base, a.ws.work, static_cast<uint4*>(a.out), row_chunks, a.device_errors);
+    auto run = [&](auto kernel, int threads) {
+      kernel<<<1, threads, 0, stream>>>(a.context_lens, a.num_seqs, a.chunk_tokens,
+                                        a.max_context_len, a.q_len, a.ws.header, a.ws.chunk_base,
+                                        a.ws.work, static_cast<uint4*>(a.out), row_chunks,
+                                        a.device_errors);
+    };
+    if (a.num_seqs <= 128) run(decode_plan_kernel<128>, 128);
+    else if (a.num_seqs <= 256) run(decode_plan_kernel<256>, 256);
+    else if (a.num_seqs <= 512) run(decode_plan_kernel<512>, 512);
+    else run(decode_plan_kernel<kPlanThreads>, kPlanThreads);
     e = cudaGetLastError();
   }
   if (e != cudaSuccess) return e;

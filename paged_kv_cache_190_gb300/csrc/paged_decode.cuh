@@ -955,6 +955,9 @@ __global__ void __launch_bounds__(DecodeTraits<BF16, D, G, KV8>::THREADS, 1)
   wait_prior_grids();
   allow_next_grid();
   __syncthreads();
+  // no work listed (every sequence empty, or a shared-prefix batch whose own
+  // tokens all go to the merge): every warp leaves at once
+  if (p.header[1] == 0) return;
 
   const int Hkv = p.num_kv_heads;
   const int bs = p.block_size;

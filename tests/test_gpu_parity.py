@@ -265,6 +265,38 @@ def test_zero_length_rows_are_zero():
     check_tolerance(out, oracle_step(case), "bf16", "zero-length")
 
 
+def test_no_work_listed_leaves_zero_rows():
+    """Every length zero but a positive length bound: the plan lists no work
+    and zeroes every row, and the decode kernel leaves at once."""
+    case = pa_inputs.make_decode_case("nowork", seed=46, dtype="bf16", num_seqs=3, num_q_heads=8,
+                                      num_kv_heads=8, head_dim=64, block_size=16,
+                                      lens=("list", [40, 40, 40]))
+    dc = DeviceCase(case)
+    lens = torch.zeros_like(dc.lens)
+    out = torch.full(dc.q.shape, float("nan"), dtype=dc.tdt, device=DEV)
+    pa.pa_decode(out, dc.q, dc.k_cache, dc.v_cache, dc.tables, lens, case.scale,
+                 case.num_kv_heads, case.max_context_len, device_errors=dc.errs)
+    torch.cuda.synchronize()
+    assert dc.device_errors() == 0
+    assert torch.count_nonzero(out).item() == 0
+
+
+@pytest.mark.parametrize("num_seqs", [300, 600, 1500])
+def test_plan_block_sizes(num_seqs):
+    """The plan runs with the smallest block (128, 256, 512 or 1024 threads)
+    that takes the batch, 1024 at a time past that: batches in each range,
+    short lengths (several chunks for some), a few empty sequences."""
+    rng = np.random.default_rng(500 + num_seqs)
+    lens = [int(x) for x in rng.integers(0, 160, size=num_seqs)]
+    case = pa_inputs.make_decode_case(f"plan-{num_seqs}", seed=500 + num_seqs, dtype="bf16",
+                                      num_seqs=num_seqs, num_q_heads=8, num_kv_heads=2,
+                                      head_dim=64, block_size=16, lens=("list", lens))
+    dc = DeviceCase(case)
+    got = out_as_f64(dc.step(chunk_tokens=64))
+    assert dc.device_errors() == 0
+    check_tolerance(got, oracle_step(case), "bf16", case.name)
+
+
 def test_decode_is_deterministic():
     case = pa_inputs.scaled_workload("gqa_bf16", 32)
     dc = DeviceCase(case)
