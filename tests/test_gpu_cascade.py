@@ -52,8 +52,9 @@ LENS = [161, 300, 200, 225, 500, 77, 385, 700, 390, 65, 90, 1000, 66]
 GROUPS = [5, 1, 3, 4]
 SHARED = [160, 0, 384, 64]
 
+# every (group, head_dim) instance of the merge: groups 1, 2, 4, 8 at head_dim 128 and 64
 VARIANTS = [(32, 8, 128, 16), (8, 8, 128, 16), (16, 2, 128, 32), (8, 4, 64, 16), (4, 4, 64, 32),
-            (16, 16, 64, 16)]
+            (16, 16, 64, 16), (16, 8, 128, 16), (16, 4, 64, 16), (16, 2, 64, 32)]
 
 
 @pytest.mark.parametrize("Hq,Hkv,D,bs", VARIANTS)
