@@ -38,7 +38,8 @@ import pa_inputs  # noqa: E402
 METRIC = "paged decode KV-read GB/s (% of GB300 HBM peak); decode steps/s, µs/step"
 FALLBACK_HBM_GBS = 6800.0
 DEFAULT_WORKLOAD = "mha_bf16"   # Llama-2-7B-shaped MHA decode, bf16, batch 64
-DECODE_SOURCES = ["paged_decode.cuh", "decode_launch.cu", "decode_instances.cuh", "pa_device.cuh"]
+DECODE_SOURCES = ["paged_decode.cuh", "decode_launch.cu", "decode_instances.cuh", "pa_device.cuh",
+                  "pa_internal.h"]
 CASCADE_SOURCES = DECODE_SOURCES + ["cascade.cu"]
 
 

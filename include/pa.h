@@ -121,7 +121,8 @@ int pa_swap_blocks(const void* src_k, const void* src_v, void* dst_k, void* dst_
 /*
  * Split size (in tokens) pa_decode uses when chunk_tokens == 0: the work of each
  * (sequence, kv head) is cut into chunks of this many tokens, chosen from the
- * batch, the longest context and the current device's SM count.
+ * batch, the longest context and the current device's SM count (at most 64
+ * pages; pa_decode_fp8 starts from 128 pages, see there).
  */
 int pa_decode_chunk_tokens(int num_seqs, int num_kv_heads, int block_size, int max_context_len);
 
@@ -143,7 +144,7 @@ size_t pa_decode_workspace_size(int num_seqs, int num_q_heads, int num_kv_heads,
  * block_size (it sizes the launch and the workspace); a length outside
  * [0, max_context_len] sets PA_DEVERR_BAD_LENGTH and is clamped.
  * chunk_tokens: 0 chooses automatically (pa_decode_chunk_tokens); otherwise a
- * multiple of 16 and of block_size, at most 64 * block_size.  Contexts longer
+ * multiple of 16 and of block_size, at most 128 * block_size.  Contexts longer
  * than one chunk are split and merged by a second kernel (log-sum-exp).
  * workspace: caller-owned device scratch of at least pa_decode_workspace_size()
  * bytes with the same arguments, 256-byte aligned; it carries no state between
@@ -281,7 +282,9 @@ int pa_cascade_groups(const int32_t* block_tables, const int32_t* context_lens, 
  * (and infinities) saturate to +-448, NaN stores a NaN code.
  *
  * pa_decode_fp8: pa_decode over such pools, with the same arguments and
- * workspace (pa_decode_workspace_size with the same sizes).  The kernel uses
+ * workspace (pa_decode_workspace_size with the same sizes: enough, since with
+ * chunk_tokens == 0 its chunks start from 128 pages rather than 64 -- a page
+ * of codes is half the bytes -- and longer chunks need fewer partials).  The kernel uses
  * the codes as they are (e4m3 tensor-core products, fp32 accumulation) and
  * applies K's scale to the logits and V's to the output.  The other operand of
  * each product is carried as two e4m3 parts: q scaled per row by a power of

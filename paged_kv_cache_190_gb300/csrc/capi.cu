@@ -38,8 +38,9 @@ int current_sm_count() {
 
 // Split size: halve 512 until the (sequence, kv head, chunk) items give every
 // SM a few, but never below 64 tokens; at most 32 pages per chunk.
-int choose_chunk(int num_seqs, int num_kv_heads, int block_size, int max_context_len, int sms) {
-  int c = pa::kItemPages * block_size;
+int choose_chunk(int num_seqs, int num_kv_heads, int block_size, int max_context_len, int sms,
+                 bool kv8 = false) {
+  int c = (kv8 ? pa::kItemPages : pa::kAutoChunkPages) * block_size;
   const int64_t units = static_cast<int64_t>(num_seqs) * num_kv_heads;
   const int64_t target = 4 * static_cast<int64_t>(sms > 0 ? sms : 1);
   while (c > 64 && units * ((static_cast<int64_t>(max_context_len) + c - 1) / c) < target) c /= 2;
@@ -193,7 +194,7 @@ int decode_common(void* out, const void* q, const void* k_cache, const void* v_c
   if (sms <= 0) return PA_ERR_CUDA;
   int chunk = chunk_tokens;
   if (chunk == 0)
-    chunk = choose_chunk(num_seqs, num_kv_heads, block_size, max_context_len, sms);
+    chunk = choose_chunk(num_seqs, num_kv_heads, block_size, max_context_len, sms, kv8);
   else if (!valid_chunk(chunk, block_size))
     return PA_ERR_INVALID_ARG;
   const pa::WorkspaceLayout lay = pa::decode_workspace_layout(

@@ -87,12 +87,12 @@ def test_workspace_size_with_explicit_chunk_is_monotone():
     s2 = pa.pa_decode_workspace_size(4, 32, 8, 128, 16, 2000, 64)
     s3 = pa.pa_decode_workspace_size(4, 32, 8, 128, 16, 2000, 128)
     assert 0 < s1 < s2 and s3 < s2
-    # chunk must be a multiple of 16 and of the block size, at most 64 pages
+    # chunk must be a multiple of 16 and of the block size, at most 128 pages
     assert pa.pa_decode_workspace_size(4, 32, 8, 128, 32, 2000, 48) == 0
-    assert pa.pa_decode_workspace_size(4, 32, 8, 128, 16, 2000, 1024) > 0
-    assert pa.pa_decode_workspace_size(4, 32, 8, 128, 16, 2000, 2048) == 0
-    assert pa.pa_decode_workspace_size(4, 32, 8, 128, 32, 4000, 2048) > 0
-    assert pa.pa_decode_workspace_size(4, 32, 8, 128, 32, 4000, 4096) == 0
+    assert pa.pa_decode_workspace_size(4, 32, 8, 128, 16, 2000, 2048) > 0
+    assert pa.pa_decode_workspace_size(4, 32, 8, 128, 16, 2000, 4096) == 0
+    assert pa.pa_decode_workspace_size(4, 32, 8, 128, 32, 8000, 4096) > 0
+    assert pa.pa_decode_workspace_size(4, 32, 8, 128, 32, 8000, 8192) == 0
 
 
 def test_cascade_host_checks():
