@@ -96,9 +96,9 @@ struct DecodeTraits {
   static constexpr int G_ = G;
   static constexpr bool KV8_ = KV8;
   static constexpr bool TC = KV8 || decode_uses_tensor_cores(BF16, G);
-  // Consumer warps: 8, which with the producer and the scheduler puts three
-  // warps on two of the SM's four sub-partitions and so caps a thread at 168
-  // registers; every consumer fits that without spilling (the fp8 one too:
+  // Consumer warps: 8, which with the producer, the scheduler and the merger
+  // puts three warps on three of the SM's four sub-partitions and so caps a
+  // thread at 168 registers; every consumer fits that without spilling (the fp8 one too:
   // 8 warps against 6 measured 206 -> 187 us on the 128K workload, 212 -> 193
   // on MHA).  The bf16 8-row kernel keeps 6: its per-warp merge buffers (rows x
   // head_dim floats each) are half its shared memory's fixed part, and with 6
