@@ -100,11 +100,12 @@ struct DecodeTraits {
   // puts three warps on three of the SM's four sub-partitions and so caps a
   // thread at 168 registers; every consumer fits that without spilling (the fp8 one too:
   // 8 warps against 6 measured 206 -> 187 us on the 128K workload, 212 -> 193
-  // on MHA).  The 8-row kernels have fewer: their per-warp merge buffers (rows
-  // x head_dim floats each) are half their shared memory's fixed part.  bf16
-  // keeps 6 (18 stages instead of 16; measured on 2 draft tokens x GQA-4: 336
-  // -> 314 us), float8 7 (21 stages; GQA fp8 162.6 -> 160.0 us).
-  static constexpr int CW = G == 8 ? (KV8 ? 7 : 6) : kConsumerWarps;
+  // on MHA).  The 8-row kernels have 7: their per-warp merge buffers (rows x
+  // head_dim floats each) are half their shared memory's fixed part, and with
+  // 7 warps 21 stages fit instead of 16 (GQA fp8 162.6 -> 160.0 us; 2 draft
+  // tokens x GQA-4 248.0 -> 244.7 us against 6 warps and 18 stages).  The fp32
+  // one keeps 6 (its q rows take 128 registers).
+  static constexpr int CW = G == 8 ? (BF16 ? 7 : 6) : kConsumerWarps;
   // + producer + scheduler + merger
   static constexpr int THREADS = (CW + 3) * 32;
   static constexpr int ELT = KV8 ? 1 : (BF16 ? 2 : 4);         // cache element bytes
